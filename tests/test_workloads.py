@@ -1,0 +1,53 @@
+"""The seeded generators give the recipe each workload states (small shapes)."""
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+
+
+def test_deterministic_and_seeded():
+    a = wl.make(2, M=64, N=48, K=32)
+    b = wl.make(2, M=64, N=48, K=32)
+    c = wl.make(2, M=64, N=48, K=32, seed=7)
+    assert torch.equal(a.A, b.A) and torch.equal(a.B, b.B)
+    assert not torch.equal(a.A, c.A)
+
+
+def test_shapes_dtypes_layouts():
+    w1 = wl.make(1, M=40, N=24, K=16)
+    assert w1.A.dtype == torch.bfloat16 and w1.A.shape == (40, 16)
+    assert w1.B.shape == (16, 24) and w1.b_layout == "kn"
+    assert w1.C.dtype == torch.float32 and w1.C.shape == (40, 24)
+    assert (w1.alpha, w1.beta, w1.d_dtype) == (1.5, 0.5, "f32")
+    w3 = wl.make(3, M=32, N=40, K=64)
+    assert w3.A.dtype == torch.float8_e4m3fn and w3.B.shape == (40, 64) and w3.b_layout == "nk"
+    assert w3.a_scale.shape == (32,) and w3.b_scale.shape == (40,)
+    w4 = wl.make(4, M=16, N=256, K=128)
+    assert w4.B.shape == (256, 128) and w4.b_layout == "nk" and w4.A.dtype == torch.bfloat16
+    w5 = wl.make(5, M=32, N=64, K=64)
+    assert w5.bias.shape == (64,) and w5.act == "silu" and w5.out_quant == "e4m3_row_amax"
+
+
+def test_value_recipes():
+    w2 = wl.make(2, M=256, N=256, K=1024)
+    sd = w2.A.float().std().item()
+    assert abs(sd - 1 / 32) < 0.002                       # N(0,1)/sqrt(K)
+    w1 = wl.make(1, M=256, N=256, K=256)
+    assert w1.A.float().abs().max() <= 1 and w1.C.abs().max() <= 1
+    w4 = wl.make(4, M=16, N=512, K=512)
+    assert abs(w4.B.float().std().item() - 0.02) < 0.001   # sigma = 0.02
+
+
+def test_fp8_quantisation_recipe():
+    w = wl.make(3, M=64, N=96, K=256)
+    codes = wl.codes_u8(w.A)
+    dq = oracle.decode_e4m3(codes)
+    # every row uses its full range: the amax element quantises to +-448
+    assert np.all(np.abs(dq).max(axis=1) == 448.0)
+    # per-token magnitudes span the log-uniform [0.1, 10] range: the scales differ
+    s = w.a_scale.numpy()
+    assert s.max() / s.min() > 5
+    # per-channel weight scales near 0.02 * (max |N(0,1)| over K) / 448
+    sw = w.b_scale.numpy()
+    assert np.all((sw > 0.02 * 2 / 448) & (sw < 0.02 * 6 / 448))
