@@ -1,0 +1,140 @@
+"""GB300 (sm_103a) dense GEMM: Python binding of the C ABI in include/dgemm.h.
+
+The functions here only marshal arguments -- torch tensors to device pointers,
+shapes to M/N/K, strings to enums, the current torch stream to a cudaStream_t --
+and call libdgemm.so. Every step of the computation runs in the library's CUDA
+kernels; there is no other path. PyTorch supplies device memory and streams.
+
+    D = dgemm_bf16(A, B, D, b_layout="kn", C=None, alpha=1.0, beta=0.0, ...)
+    D = dgemm_fp8_scaled(Aq, Bq, a_scale, b_scale, D, b_layout="nk", ...)
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._lib import (ACT, B_KN, B_NK, BF16, E4M3, F32, QUANT, DgemmError, Epilogue, Plan, load,
+                   lib_path)
+
+__all__ = ["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_workspace_size", "dgemm_plan",
+           "dgemm_status_string", "dgemm_query_device_status", "DgemmError", "load", "lib_path"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dims(A, B, b_layout):
+    M, K = A.shape
+    if b_layout == "kn":
+        K2, N = B.shape
+    elif b_layout == "nk":
+        N, K2 = B.shape
+    else:
+        raise ValueError(f"b_layout must be 'kn' or 'nk', not {b_layout!r}")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A has K={K}, B has K={K2}")
+    return M, N, K
+
+
+def _epilogue(bias, act, out_quant, out_row_scale):
+    if bias is None and act == "none" and out_quant == "none":
+        return None
+    return Epilogue(None if bias is None else bias.data_ptr(), ACT[act], QUANT[out_quant],
+                    None if out_row_scale is None else out_row_scale.data_ptr())
+
+
+def _check(code, where):
+    if code != 0:
+        raise DgemmError(code, where)
+
+
+def dgemm_bf16(A, B, D, *, b_layout="kn", C=None, alpha=1.0, beta=0.0, bias=None, act="none",
+               out_quant="none", out_row_scale=None, ws=None, stream=None):
+    """D = epilogue(alpha * A . op(B) + beta * C) with BF16 A, B and FP32 accumulation.
+
+    A [M,K] bf16; B [K,N] ("kn") or [N,K] ("nk") bf16; C, D [M,N]; bias [N] fp32;
+    act in none/relu/gelu/silu; out_quant "e4m3_row_amax" writes E4M3 codes to D
+    and per-row scales to out_row_scale [M]. ws: workspace tensor (uint8) of at
+    least dgemm_workspace_size(...) bytes. Returns D.
+    """
+    M, N, K = _dims(A, B, b_layout)
+    epi = _epilogue(bias, act, out_quant, out_row_scale)
+    code = load().dgemm_bf16(_ptr(A), _ptr(B), B_KN if b_layout == "kn" else B_NK, _ptr(C),
+                             _dtype_code(C) if C is not None else F32, _ptr(D), _dtype_code(D),
+                             M, N, K, float(alpha), float(beta),
+                             ctypes.byref(epi) if epi is not None else None,
+                             _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(code, "dgemm_bf16")
+    return D
+
+
+def dgemm_fp8_scaled(Aq, Bq, a_scale, b_scale, D, *, b_layout="nk", k_group=0, C=None, alpha=1.0,
+                     beta=0.0, bias=None, act="none", out_quant="none", out_row_scale=None, ws=None,
+                     stream=None):
+    """D = epilogue(alpha * diag(a_scale) (Aq . op(Bq)) diag(b_scale) + beta * C), E4M3 inputs.
+
+    Aq [M,K] and Bq [N,K] ("nk") or [K,N] ("kn") are float8_e4m3fn (or uint8 codes);
+    a_scale [M] and b_scale [N] fp32. Other arguments as for dgemm_bf16. Returns D.
+    """
+    M, N, K = _dims(Aq, Bq, b_layout)
+    epi = _epilogue(bias, act, out_quant, out_row_scale)
+    code = load().dgemm_fp8_scaled(_ptr(Aq), _ptr(Bq), B_KN if b_layout == "kn" else B_NK, _ptr(a_scale),
+                                   _ptr(b_scale), int(k_group), _ptr(C),
+                                   _dtype_code(C) if C is not None else F32, _ptr(D), _dtype_code(D),
+                                   M, N, K, float(alpha), float(beta),
+                                   ctypes.byref(epi) if epi is not None else None,
+                                   _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                   _stream(stream))
+    _check(code, "dgemm_fp8_scaled")
+    return D
+
+
+def dgemm_workspace_size(is_fp8, M, N, K, b_layout="nk", *, out_quant="none", act="none") -> int:
+    epi = Epilogue(None, ACT[act], QUANT[out_quant], None)
+    return int(load().dgemm_workspace_size(int(bool(is_fp8)), M, N, K, B_KN if b_layout == "kn" else B_NK,
+                                           ctypes.byref(epi)))
+
+
+def dgemm_plan(is_fp8, M, N, K, b_layout="nk", d_dtype="bf16", *, out_quant="none", act="none",
+               num_sms=152) -> dict:
+    """The plan the library would use (host-only; no GPU needed)."""
+    epi = Epilogue(None, ACT[act], QUANT[out_quant], None)
+    plan = Plan()
+    d = {"f32": F32, "bf16": BF16, "e4m3": E4M3}[d_dtype]
+    code = load().dgemm_plan(int(bool(is_fp8)), M, N, K, B_KN if b_layout == "kn" else B_NK, d,
+                             ctypes.byref(epi), int(num_sms), ctypes.byref(plan))
+    _check(code, "dgemm_plan")
+    return {name: getattr(plan, name) for name, _ in Plan._fields_}
+
+
+def dgemm_status_string(code: int) -> str:
+    return load().dgemm_status_string(int(code)).decode()
+
+
+def dgemm_query_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the sticky device error code."""
+    return int(load().dgemm_query_device_status(_stream(stream)))

@@ -1,0 +1,390 @@
+// api.cu -- the C ABI: argument validation, planning, TMA tensor maps, launch,
+// and the sticky device-side status word. Interface as on the FP8 page
+// ("DeepGEMM: FP8 Tensor Core GEMM", bjdmk.com.cn/news/6078902, §5.1): pointers,
+// M/N/K, scale descriptor, a workspace whose size is queried beforehand, and a
+// stream; nothing is allocated per call.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "dgemm.h"
+#include "kernels.h"
+
+namespace {
+
+__device__ unsigned int g_status = 0;  // sticky device-side error bits, one word per device
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kWsHeader = 256;  // grid-barrier counter lives here
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int cc_major = 0, cc_minor = 0, num_sms = 0;
+    unsigned* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int g_nk = 0;
+const dg::KernelInfo* g_kernels[64];
+std::atomic<unsigned char> g_attr_set[64][kMaxDevices];
+std::once_flag g_kernels_once;
+
+void collect_kernels() {
+    int n1 = 0, n2 = 0;
+    const dg::KernelInfo* t1 = dg::kernels_bf16(&n1);
+    const dg::KernelInfo* t2 = dg::kernels_fp8(&n2);
+    for (int i = 0; i < n1 && g_nk < 64; ++i) g_kernels[g_nk++] = &t1[i];
+    for (int i = 0; i < n2 && g_nk < 64; ++i) g_kernels[g_nk++] = &t2[i];
+}
+
+int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode) {
+    std::call_once(g_kernels_once, collect_kernels);
+    for (int i = 0; i < g_nk; ++i) {
+        const dg::KernelInfo* k = g_kernels[i];
+        if (k->bn == bn && k->fp8 == fp8 && k->a_mn == a_mn && k->b_mn == b_mn && k->mode == mode) return i;
+    }
+    return -1;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t dtype_bytes(dgemm_dtype_t t) { return t == DGEMM_F32 ? 4 : t == DGEMM_BF16 ? 2 : 1; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+    dgemm_plan_t pub;
+    int kernel;        // index into g_kernels
+    int mode;
+    int a_mn, b_mn;
+    int64_t Mm, Nm;    // problem in the MMA's orientation
+    int bk;            // K elements per stage
+};
+
+// Validates the sizes, enums and epilogue; picks the kernel variant and grid.
+// Pure host logic: needs no GPU.
+dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t bl, dgemm_dtype_t d_dtype,
+                         const dgemm_epilogue_t* epi, int num_sms, Plan* out) {
+    if (M < 0 || N < 0 || K < 0 || num_sms <= 0) return DGEMM_ERR_INVALID_VALUE;
+    if (bl != DGEMM_B_KN && bl != DGEMM_B_NK) return DGEMM_ERR_INVALID_VALUE;
+    if (d_dtype != DGEMM_F32 && d_dtype != DGEMM_BF16 && d_dtype != DGEMM_E4M3) return DGEMM_ERR_INVALID_VALUE;
+    const int act = epi ? epi->act : DGEMM_ACT_NONE;
+    const int oq = epi ? epi->out_quant : DGEMM_QUANT_NONE;
+    if (act < DGEMM_ACT_NONE || act > DGEMM_ACT_SILU) return DGEMM_ERR_INVALID_VALUE;
+    if (oq != DGEMM_QUANT_NONE && oq != DGEMM_QUANT_E4M3_ROW_AMAX) return DGEMM_ERR_INVALID_VALUE;
+    if ((oq == DGEMM_QUANT_E4M3_ROW_AMAX) != (d_dtype == DGEMM_E4M3)) return DGEMM_ERR_INVALID_VALUE;
+    // Index arithmetic in the kernels is 32-bit per dimension.
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return DGEMM_ERR_NOT_SUPPORTED;
+    const size_t esz = fp8 ? 1 : 2;
+    // TMA: every row pitch a multiple of 16 bytes.
+    if ((static_cast<size_t>(K) * esz) % 16 != 0) return DGEMM_ERR_MISALIGNED;
+    if (bl == DGEMM_B_KN && (static_cast<size_t>(N) * esz) % 16 != 0) return DGEMM_ERR_MISALIGNED;
+    if ((static_cast<size_t>(N) * dtype_bytes(d_dtype)) % 16 != 0) return DGEMM_ERR_MISALIGNED;
+
+    Plan p{};
+    p.bk = static_cast<int>(128 / esz);
+    const bool swap = (oq == DGEMM_QUANT_NONE) && M <= 64;
+    int bn;
+    if (swap) {
+        p.mode = dg::MODE_SWAP;
+        p.Mm = N;
+        p.Nm = M;
+        p.a_mn = (bl == DGEMM_B_KN);  // the MMA's A operand is op(B)^T
+        p.b_mn = 0;
+        bn = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    } else {
+        p.mode = oq ? dg::MODE_ROWQ : dg::MODE_TILE;
+        p.Mm = M;
+        p.Nm = N;
+        p.a_mn = 0;
+        p.b_mn = (bl == DGEMM_B_KN);
+        if (p.mode == dg::MODE_ROWQ) {
+            bn = 256;
+        } else {
+            // Fewest waves of the widest tile: cost ~ waves x tile width, with a
+            // penalty for narrow tiles (more shared-memory traffic per FLOP).
+            const int cands[3] = {256, 128, 64};
+            const double penalty[3] = {1.0, 1.15, 1.6};
+            double best = 1e300;
+            bn = 256;
+            for (int i = 0; i < 3; ++i) {
+                if (fp8 && p.b_mn && cands[i] < 128) continue;
+                const int64_t tiles = ((M + 127) / 128) * ((N + cands[i] - 1) / cands[i]);
+                const int64_t waves = (tiles + num_sms - 1) / num_sms;
+                const double cost = static_cast<double>(waves) * cands[i] * penalty[i];
+                if (cost < best) {
+                    best = cost;
+                    bn = cands[i];
+                }
+            }
+        }
+    }
+    // DGEMM_TILE_N overrides the tile width when such a variant exists (used to
+    // exercise every variant in tests and for tuning sweeps).
+    if (const char* f = std::getenv("DGEMM_TILE_N")) {
+        const int v = std::atoi(f);
+        if (find_kernel(v, fp8, p.a_mn, p.b_mn, p.mode) >= 0) bn = v;
+    }
+    p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode);
+    if (p.kernel < 0) return DGEMM_ERR_NOT_SUPPORTED;
+    const dg::KernelInfo* k = g_kernels[p.kernel];
+    const int64_t tiles_m = (p.Mm + 127) / 128, tiles_n = (p.Nm + bn - 1) / bn;
+    if (tiles_m * tiles_n > INT32_MAX) return DGEMM_ERR_NOT_SUPPORTED;
+    p.pub.swap_ab = swap ? 1 : 0;
+    p.pub.tile_m = 128;
+    p.pub.tile_n = bn;
+    p.pub.cta_group = 1;
+    p.pub.stages = k->stages;
+    p.pub.num_tiles = static_cast<int>(tiles_m * tiles_n);
+    p.pub.grid = static_cast<int>(p.pub.num_tiles < num_sms ? p.pub.num_tiles : num_sms);
+    p.pub.cooperative = p.mode == dg::MODE_ROWQ ? 1 : 0;
+    p.pub.raster_group = static_cast<int>(tiles_m < 8 ? (tiles_m > 0 ? tiles_m : 1) : 8);
+    p.pub.smem_bytes = static_cast<size_t>(k->smem_bytes);
+    p.pub.workspace_bytes =
+        oq ? kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2 : 0;
+    *out = p;
+    return DGEMM_OK;
+}
+
+void init_encode() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+// 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows,
+// rows `pitch` bytes apart; box of box_inner x box_outer; 128-byte swizzle;
+// out-of-range elements load as zero and are not stored.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+    std::call_once(g_encode_once, init_encode);
+    if (!g_encode) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+dgemm_status_t device_state(DeviceState** out, int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return DGEMM_ERR_NOT_SUPPORTED;
+    DeviceState& d = g_dev[dev];
+    std::call_once(d.once, [&d, dev]() {
+        cudaError_t e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess && d.cc_major == 10 && d.cc_minor == 3)
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
+        d.err = e;
+    });
+    if (d.err != cudaSuccess) return DGEMM_ERR_CUDA;
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return DGEMM_ERR_ARCH;
+    *out = &d;
+    *dev_out = dev;
+    return DGEMM_OK;
+}
+
+CUtensorMapDataType tm_type(dgemm_dtype_t t) {
+    return t == DGEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                          : t == DGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+}
+
+dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, const float* a_scale,
+                   const float* b_scale, const void* C, dgemm_dtype_t c_dtype, void* D, dgemm_dtype_t d_dtype,
+                   int64_t M, int64_t N, int64_t K, float alpha, float beta, const dgemm_epilogue_t* epi, void* ws,
+                   size_t ws_bytes, cudaStream_t stream) {
+    // ---- arguments that need no device
+    Plan plan;
+    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 1, &plan);
+    if (st != DGEMM_OK) return st;
+    if (M == 0 || N == 0) return DGEMM_OK;
+    if (!D || (K > 0 && (!A || !B))) return DGEMM_ERR_INVALID_VALUE;
+    if (fp8 && (!a_scale || !b_scale)) return DGEMM_ERR_INVALID_VALUE;
+    if (beta != 0.0f) {
+        if (!C) return DGEMM_ERR_INVALID_VALUE;
+        if (c_dtype != DGEMM_F32 && c_dtype != DGEMM_BF16) return DGEMM_ERR_INVALID_VALUE;
+        if ((static_cast<size_t>(N) * dtype_bytes(c_dtype)) % 16 != 0) return DGEMM_ERR_MISALIGNED;
+        if (!aligned16(C)) return DGEMM_ERR_MISALIGNED;
+    }
+    const int oq = epi ? epi->out_quant : DGEMM_QUANT_NONE;
+    const float* bias = epi ? epi->bias : nullptr;
+    if (oq && !epi->out_row_scale) return DGEMM_ERR_INVALID_VALUE;
+    if ((K > 0 && (!aligned16(A) || !aligned16(B))) || !aligned16(D)) return DGEMM_ERR_MISALIGNED;
+    if ((a_scale && !aligned16(a_scale)) || (b_scale && !aligned16(b_scale)) || (bias && !aligned16(bias)) ||
+        (oq && !aligned16(epi->out_row_scale)) || (ws && !aligned16(ws)))
+        return DGEMM_ERR_MISALIGNED;
+    if (plan.pub.workspace_bytes > 0 && (!ws || ws_bytes < plan.pub.workspace_bytes))
+        return DGEMM_ERR_WORKSPACE_TOO_SMALL;
+
+    // ---- device
+    DeviceState* dev = nullptr;
+    int devid = 0;
+    st = device_state(&dev, &devid);
+    if (st != DGEMM_OK) return st;
+    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, &plan);
+    if (st != DGEMM_OK) return st;
+    const dg::KernelInfo* k = g_kernels[plan.kernel];
+    std::atomic<unsigned char>& attr = g_attr_set[plan.kernel][devid];
+    if (!attr.load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(k->func, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes) !=
+            cudaSuccess)
+            return DGEMM_ERR_CUDA;
+        attr.store(1, std::memory_order_release);
+    }
+
+    // ---- tensor maps
+    const dgemm_dtype_t in_t = fp8 ? DGEMM_E4M3 : DGEMM_BF16;
+    const size_t esz = fp8 ? 1 : 2;
+    const int mn_atom = static_cast<int>(128 / esz);
+    alignas(64) CUtensorMap tmA, tmB, tmD;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    std::memset(&tmD, 0, sizeof tmD);
+    // The MMA's operands: X (rows of the MMA's M) and Y (rows of its N).
+    const void* X = plan.pub.swap_ab ? B : A;
+    const void* Y = plan.pub.swap_ab ? A : B;
+    if (K > 0) {
+        bool ok;
+        if (plan.a_mn)  // X = op(B)^T with B stored K x N: MN-major
+            ok = encode_2d(&tmA, tm_type(in_t), X, N, K, N * esz, mn_atom, plan.bk);
+        else            // X stored Mm x K: K-major
+            ok = encode_2d(&tmA, tm_type(in_t), X, K, plan.Mm, K * esz, plan.bk, 128);
+        if (!ok) return DGEMM_ERR_CUDA;
+        if (plan.b_mn)  // Y = B stored K x N: MN-major
+            ok = encode_2d(&tmB, tm_type(in_t), Y, N, K, N * esz, mn_atom, plan.bk);
+        else            // Y stored Nm x K: K-major
+            ok = encode_2d(&tmB, tm_type(in_t), Y, K, plan.Nm, K * esz, plan.bk, plan.pub.tile_n);
+        if (!ok) return DGEMM_ERR_CUDA;
+    }
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    const size_t amax_bytes = round_up(static_cast<size_t>(M) * 4, 256);
+    if (plan.mode == dg::MODE_TILE) {
+        const size_t dsz = dtype_bytes(d_dtype);
+        if (!encode_2d(&tmD, tm_type(d_dtype), D, N, M, N * dsz, static_cast<uint32_t>(128 / dsz), 32))
+            return DGEMM_ERR_CUDA;
+    } else if (plan.mode == dg::MODE_ROWQ) {
+        if (!encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wsb + kWsHeader + amax_bytes, N, M, N * 2, 64, 32))
+            return DGEMM_ERR_CUDA;
+    }
+
+    // ---- parameters
+    dg::Params p{};
+    p.M = static_cast<int>(plan.Mm);
+    p.N = static_cast<int>(plan.Nm);
+    p.K = static_cast<int>(K);
+    p.tiles_m = static_cast<int>((plan.Mm + 127) / 128);
+    p.tiles_n = static_cast<int>((plan.Nm + plan.pub.tile_n - 1) / plan.pub.tile_n);
+    p.num_tiles = plan.pub.num_tiles;
+    p.k_blocks = static_cast<int>((K + plan.bk - 1) / plan.bk);
+    p.group_m = plan.pub.raster_group;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = beta != 0.0f ? C : nullptr;
+    p.ldc = N;
+    p.c_f32 = c_dtype == DGEMM_F32;
+    p.D = D;
+    p.ldd = N;
+    p.d_f32 = d_dtype == DGEMM_F32;
+    p.row_scale = plan.pub.swap_ab ? b_scale : a_scale;
+    p.col_scale = plan.pub.swap_ab ? a_scale : b_scale;
+    p.bias = bias;
+    p.act = epi ? epi->act : 0;
+    p.status = dev->status;
+    if (plan.mode == dg::MODE_ROWQ) {
+        p.barrier = reinterpret_cast<unsigned*>(wsb);
+        p.amax = reinterpret_cast<unsigned*>(wsb + kWsHeader);
+        p.stash = reinterpret_cast<const uint16_t*>(wsb + kWsHeader + amax_bytes);
+        p.q_out = static_cast<uint8_t*>(D);
+        p.out_row_scale = epi->out_row_scale;
+        if (cudaMemsetAsync(ws, 0, kWsHeader + amax_bytes, stream) != cudaSuccess) return DGEMM_ERR_CUDA;
+    }
+    if (k->launch(tmA, tmB, tmD, p, plan.pub.grid, stream, plan.pub.cooperative != 0) != cudaSuccess)
+        return DGEMM_ERR_CUDA;
+    return DGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dgemm_status_t dgemm_bf16(const void* A, const void* B, dgemm_b_layout_t b_layout, const void* C,
+                          dgemm_dtype_t c_dtype, void* D, dgemm_dtype_t d_dtype, int64_t M, int64_t N, int64_t K,
+                          float alpha, float beta, const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes,
+                          dgemm_stream_t stream) {
+    return run(0, A, B, b_layout, nullptr, nullptr, C, c_dtype, D, d_dtype, M, N, K, alpha, beta, epi, ws, ws_bytes,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t b_layout, const float* a_scale,
+                                const float* b_scale, int k_group, const void* C, dgemm_dtype_t c_dtype, void* D,
+                                dgemm_dtype_t d_dtype, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes, dgemm_stream_t stream) {
+    if (k_group != 0) return k_group < 0 ? DGEMM_ERR_INVALID_VALUE : DGEMM_ERR_NOT_SUPPORTED;
+    return run(1, Aq, Bq, b_layout, a_scale, b_scale, C, c_dtype, D, d_dtype, M, N, K, alpha, beta, epi, ws,
+               ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,
+                            const dgemm_epilogue_t* epi) {
+    Plan plan;
+    const dgemm_dtype_t d = (epi && epi->out_quant) ? DGEMM_E4M3 : DGEMM_BF16;
+    if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d, epi, 1, &plan) != DGEMM_OK) {
+        // the output dtype is not an argument here: retry with FP32 output
+        if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, DGEMM_F32, epi, 1, &plan) != DGEMM_OK) return 0;
+    }
+    return plan.pub.workspace_bytes;
+}
+
+dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,
+                          dgemm_dtype_t d_dtype, const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan) {
+    if (!plan) return DGEMM_ERR_INVALID_VALUE;
+    Plan p;
+    const dgemm_status_t st = make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, &p);
+    if (st == DGEMM_OK) *plan = p.pub;
+    return st;
+}
+
+const char* dgemm_status_string(dgemm_status_t s) {
+    switch (s) {
+        case DGEMM_OK: return "success";
+        case DGEMM_ERR_INVALID_VALUE: return "invalid argument (NULL pointer, negative size or bad enum)";
+        case DGEMM_ERR_NOT_SUPPORTED: return "request not supported by this build";
+        case DGEMM_ERR_MISALIGNED: return "pointer or leading dimension not 16-byte aligned";
+        case DGEMM_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than dgemm_workspace_size()";
+        case DGEMM_ERR_CUDA: return "a CUDA runtime or driver call failed";
+        case DGEMM_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait gave up";
+        case DGEMM_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    }
+    return "unknown status";
+}
+
+dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DGEMM_ERR_CUDA;
+    DeviceState* dev = nullptr;
+    int devid = 0;
+    const dgemm_status_t st = device_state(&dev, &devid);
+    if (st != DGEMM_OK) return st;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof v) != cudaSuccess) return DGEMM_ERR_CUDA;
+    if (v == 0) return DGEMM_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) return DGEMM_ERR_CUDA;
+    return DGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,563 @@
+// gemm_kernel.cuh -- the persistent, warp-specialised tcgen05 GEMM kernel.
+//
+// One CTA per SM loops over output tiles in a swizzled (grouped) raster order.
+// Its six warps split the work:
+//   warp 0     TMA producer: streams 128-byte-wide K slices of A and B into an
+//              S-stage shared-memory ring (128B swizzle), one mbarrier pair
+//              (full / empty) per stage.
+//   warp 1     MMA issuer: one thread issues tcgen05.mma for each K slice into
+//              one of two FP32 accumulators in Tensor Memory and commits the
+//              stage back to the producer; owns the TMEM allocation.
+//   warps 2-5  epilogue: read the finished accumulator with tcgen05.ld (each
+//              warp its 32-lane quarter, one output row per thread), apply
+//              scales, alpha/beta, bias and activation in FP32, convert once,
+//              and write through swizzled shared memory with TMA stores (or,
+//              for the transposed small-M form, with coalesced direct stores),
+//              while the MMA warp fills the other accumulator.
+//
+// The method is the one the pages describe -- tiles of C per block, K walked in
+// slices through a multi-buffered shared-memory pipeline, FP32 accumulation,
+// fused epilogue (DeepGEMM write-up, czchanglian.com/news/51329, §2-§3, §6;
+// "DeepGEMM: FP8 Tensor Core GEMM", bjdmk.com.cn/news/6078902, §2.2, §3.1-3.2) --
+// rebuilt for sm_103a: TMA replaces cp.async, mbarriers replace
+// __syncthreads/wait_prior, the hardware 128B swizzle replaces the hand XOR,
+// Tensor Memory replaces register accumulators, and a persistent tile loop
+// replaces the one-block-per-tile grid.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace dg {
+
+enum Mode : int {
+    MODE_TILE = 0,  // D tile stored as is (TMA store)
+    MODE_SWAP = 1,  // the MMA computed D^T: store transposed with direct stores
+    MODE_ROWQ = 2,  // stash y, per-row amax, grid barrier, E4M3 requantisation
+};
+
+enum ErrBits : unsigned {
+    ERR_TIMEOUT_PRODUCER = 1u,
+    ERR_TIMEOUT_MMA = 2u,
+    ERR_TIMEOUT_EPILOGUE = 4u,
+    ERR_TIMEOUT_GRID_BARRIER = 8u,
+    ERR_TIMEOUT_DRAIN = 16u,
+};
+
+struct Params {
+    // Problem in the MMA's orientation: rows M, columns N, reduction K.
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles, k_blocks, group_m;
+    float alpha, beta;
+    const void* C;  // beta != 0: C in the output's orientation
+    int64_t ldc;
+    int c_f32;      // 1: C is FP32, 0: BF16
+    void* D;        // direct-store modes: output pointer
+    int64_t ldd;
+    int d_f32;      // 1: D is FP32, 0: BF16 (MODE_TILE / MODE_SWAP)
+    const float* row_scale;  // per MMA row, or null
+    const float* col_scale;  // per MMA column, or null
+    const float* bias;       // per output channel, or null
+    int act;                 // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
+    // MODE_ROWQ
+    unsigned* amax;          // [M] |y| maxima as float bits; zero before launch
+    unsigned* barrier;       // grid barrier counter; zero before launch
+    const uint16_t* stash;   // [M,N] BF16 y values (what tmD writes)
+    uint8_t* q_out;          // [M,N] E4M3 codes
+    float* out_row_scale;    // [M]
+    unsigned* status;        // sticky device error word
+};
+
+template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_>
+struct Cfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr bool FP8 = FP8_;
+    static constexpr bool A_MN = A_MN_;
+    static constexpr bool B_MN = B_MN_;
+    static constexpr int MODE = MODE_;
+    static constexpr int ESZ = FP8 ? 1 : 2;       // operand bytes
+    static constexpr int BK = 128 / ESZ;          // K elements per stage (128 bytes)
+    static constexpr int UMMA_K = 32 / ESZ;       // K elements per MMA (32 bytes)
+    static constexpr int MN_ATOM = 128 / ESZ;     // MN elements per 128-byte row (MN-major)
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGING_BYTES = (MODE == MODE_SWAP) ? 0 : 4 * 2 * 4096;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_LIMIT = 232448;  // 227 KB opt-in maximum per CTA
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
+    static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
+    static constexpr uint32_t IDESC = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, BM, BN);
+    static constexpr int NUM_THREADS = 192;
+
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
+    static_assert(!B_MN || BN % MN_ATOM == 0, "MN-major B needs whole 128-byte atoms");
+    static_assert(MODE == MODE_SWAP || BN % 64 == 0, "tile epilogue works in 64-column boxes");
+    static_assert(STAGES >= 2, "pipeline depth");
+    static_assert(BN < 32 || BN % 32 == 0, "epilogue reads 32-column units");
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
+};
+
+__device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
+    // Grouped raster: bands of group_m tile-rows; inside a band, walk down the
+    // rows first, then across the columns, so CTAs resident at the same time
+    // share A row-strips and B column-strips in L2.
+    const int group_tiles = p.group_m * p.tiles_n;
+    const int g = t / group_tiles;
+    const int first_m = g * p.group_m;
+    const int rows = min(p.tiles_m - first_m, p.group_m);
+    const int r = t - g * group_tiles;
+    mb = first_m + r % rows;
+    nb = r / rows;
+}
+
+__device__ __forceinline__ float activation(float y, int act) {
+    switch (act) {
+        case 1: return fmaxf(y, 0.0f);
+        case 2: return 0.5f * y * (1.0f + erff(y * 0.70710678118654752f));
+        case 3: return y / (1.0f + expf(-y));
+        default: return y;
+    }
+}
+
+__device__ __forceinline__ void raise_error(const Params& p, unsigned bit, volatile int* abort) {
+    atomicOr(p.status, bit);
+    *abort = 1;
+}
+
+// Loads base[idx .. idx+3] (every lane of the warp reads the same address);
+// entries at or beyond n read as 0. base must be 16-byte aligned, idx % 4 == 0.
+__device__ __forceinline__ float4 ld_bcast4(const float* base, int idx, int n) {
+    if (idx + 3 < n) return __ldg(reinterpret_cast<const float4*>(base + idx));
+    float4 r;
+    r.x = idx < n ? __ldg(base + idx) : 0.0f;
+    r.y = idx + 1 < n ? __ldg(base + idx + 1) : 0.0f;
+    r.z = idx + 2 < n ? __ldg(base + idx + 2) : 0.0f;
+    r.w = 0.0f;
+    return r;
+}
+
+// The FP32 epilogue arithmetic shared by all modes for 32 consecutive columns
+// of one row: v = alpha * (rs * cs[j] * acc) + beta * c[j] + bias[j], then act.
+template <bool SWAP>
+__device__ __forceinline__ void epilogue_math(float (&v)[32], const Params& p, int row, int col0,
+                                              int ncols, float rs, float bias_row) {
+    const bool row_ok = row < p.M;
+    // column-indexed scale (per MMA column)
+    if (p.col_scale) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            if (j < ncols && col0 + j < p.N) {
+                const float4 s = ld_bcast4(p.col_scale, col0 + j, p.N);
+                v[j] *= s.x; v[j + 1] *= s.y; v[j + 2] *= s.z; v[j + 3] *= s.w;
+            }
+        }
+    }
+    const float a = p.alpha * rs;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= a;
+    if (p.beta != 0.0f && row_ok) {
+        if constexpr (!SWAP) {
+            // C row segment, in the output's orientation: row-major, this thread's row.
+            if (p.c_f32) {
+                const float* c = static_cast<const float*>(p.C) + row * p.ldc + col0;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    if (j < ncols && col0 + j < p.N) {
+                        const float4 cv = *reinterpret_cast<const float4*>(c + j);
+                        v[j] += p.beta * cv.x; v[j + 1] += p.beta * cv.y;
+                        v[j + 2] += p.beta * cv.z; v[j + 3] += p.beta * cv.w;
+                    }
+            } else {
+                const uint16_t* c = static_cast<const uint16_t*>(p.C) + row * p.ldc + col0;
+#pragma unroll
+                for (int j = 0; j < 32; j += 8)
+                    if (j < ncols && col0 + j < p.N) {
+                        const uint4 cv = *reinterpret_cast<const uint4*>(c + j);
+                        const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            v[j + 2 * h] += p.beta * bf16_lo(w[h]);
+                            v[j + 2 * h + 1] += p.beta * bf16_hi(w[h]);
+                        }
+                    }
+            }
+        } else {
+            // Transposed: MMA column j is output row j, MMA row is output column.
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < ncols && col0 + j < p.N) {
+                    const int64_t off = static_cast<int64_t>(col0 + j) * p.ldc + row;
+                    const float cv = p.c_f32 ? static_cast<const float*>(p.C)[off]
+                                             : __uint_as_float(static_cast<uint32_t>(
+                                                   static_cast<const uint16_t*>(p.C)[off]) << 16);
+                    v[j] += p.beta * cv;
+                }
+        }
+    }
+    if constexpr (SWAP) {
+        if (p.bias) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += bias_row;
+        }
+    } else {
+        if (p.bias) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                if (j < ncols && col0 + j < p.N) {
+                    const float4 b = ld_bcast4(p.bias, col0 + j, p.N);
+                    v[j] += b.x; v[j + 1] += b.y; v[j + 2] += b.z; v[j + 3] += b.w;
+                }
+        }
+    }
+    if (p.act) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = activation(v[j], p.act);
+    }
+}
+
+template <class CF>
+__global__ void __launch_bounds__(CF::NUM_THREADS, 1)
+    gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmD, const Params p) {
+    constexpr int S = CF::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    uint8_t* staging = smem + S * CF::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + CF::STAGING_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* acc_full = bars + 2 * S;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        if (p.k_blocks > 0) {  // with K == 0 the operand maps are not encoded
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+        if (CF::MODE != MODE_SWAP) tma_prefetch_desc(&tmD);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, CF::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = stages + stage * CF::STAGE_BYTES;
+                    uint8_t* sb = sa + CF::A_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
+                    const int k0 = kb * CF::BK;
+                    if constexpr (CF::A_MN) {
+#pragma unroll
+                        for (int i = 0; i < CF::BM / CF::MN_ATOM; ++i)
+                            tma_load_2d(sa + i * CF::BK * 128, &tmA, &full[stage], mb * CF::BM + i * CF::MN_ATOM,
+                                        k0, pol);
+                    } else {
+                        tma_load_2d(sa, &tmA, &full[stage], k0, mb * CF::BM, pol);
+                    }
+                    if constexpr (CF::B_MN) {
+#pragma unroll
+                        for (int i = 0; i < CF::BN / CF::MN_ATOM; ++i)
+                            tma_load_2d(sb + i * CF::BK * 128, &tmB, &full[stage], nb * CF::BN + i * CF::MN_ATOM,
+                                        k0, pol);
+                    } else {
+                        tma_load_2d(sb, &tmB, &full[stage], k0, nb * CF::BN, pol);
+                    }
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) raise_error(p, ERR_TIMEOUT_PRODUCER, abort_flag);
+            // Drain: every copy this thread issued must have landed before the
+            // CTA can exit (normally these waits return at once).
+            for (int s = 0; s < S; ++s) {
+                const int64_t cnt = issued > s ? (issued - s + S - 1) / S : 0;
+                if (cnt > 0 && !mbar_wait(&full[s], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
+                    raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+                const int buf = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * CF::BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(stages + stage * CF::STAGE_BYTES);
+                    const uint32_t b0 = a0 + CF::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < CF::BK / CF::UMMA_K; ++k) {
+                        const uint64_t ad = CF::A_MN ? smem_desc_sw128(a0 + k * CF::UMMA_K * 128, CF::BK * 128, 1024)
+                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = CF::B_MN ? smem_desc_sw128(b0 + k * CF::UMMA_K * 128, CF::BK * 128, 1024)
+                                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
+                        const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+                        if constexpr (CF::FP8)
+                            mma_f8(d_tmem, ad, bd, CF::IDESC, acc);
+                        else
+                            mma_bf16(d_tmem, ad, bd, CF::IDESC, acc);
+                    }
+                    mma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[buf]);     // accumulator ready for the epilogue
+            }
+            if (!ok) raise_error(p, ERR_TIMEOUT_MMA, abort_flag);
+            // Drain: all issued MMAs complete before TMEM is released.
+            mma_commit(drain);
+            if (!mbar_wait(drain, 0, nullptr)) raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                        // TMEM lane quarter this warp may access
+        uint8_t* stg = staging + (warp - 2) * 8192;    // two 4 KB staging boxes per warp
+        int stores = 0;
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const int buf = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int row = mb * CF::BM + q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * CF::BN);
+            const float rs = (p.row_scale && row < p.M) ? p.row_scale[row] : 1.0f;
+            float bias_row = 0.0f;
+            if constexpr (CF::MODE == MODE_SWAP)
+                if (p.bias && row < p.M) bias_row = p.bias[row];
+            float rowmax = 0.0f;
+            constexpr int UNIT = CF::BN < 32 ? CF::BN : 32;
+#pragma unroll 1
+            for (int u = 0; u < CF::BN / UNIT; ++u) {
+                const int col0 = nb * CF::BN + u * UNIT;
+                float v[32];
+                if constexpr (UNIT == 32) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + u * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                } else {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + u * 16, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+#pragma unroll
+                    for (int j = 16; j < 32; ++j) v[j] = 0.0f;
+                }
+                if (p.k_blocks == 0) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                }
+                if (u == CF::BN / UNIT - 1) {
+                    // Last read of this accumulator: hand it back to the MMA warp.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                }
+                epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row);
+
+                if constexpr (CF::MODE == MODE_SWAP) {
+                    // MMA column = output row; MMA row = output column.
+                    if (row < p.M) {
+#pragma unroll
+                        for (int j = 0; j < UNIT; ++j)
+                            if (col0 + j < p.N) {
+                                const int64_t off = static_cast<int64_t>(col0 + j) * p.ldd + row;
+                                if (p.d_f32)
+                                    static_cast<float*>(p.D)[off] = v[j];
+                                else
+                                    static_cast<uint16_t*>(p.D)[off] =
+                                        static_cast<uint16_t>(pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
+                            }
+                    }
+                } else {
+                    const bool f32_out = (CF::MODE == MODE_TILE) && p.d_f32;
+                    if constexpr (CF::MODE == MODE_ROWQ) {
+                        if (row < p.M) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (col0 + j < p.N) rowmax = fmaxf(rowmax, fabsf(v[j]));
+                        }
+                    }
+                    // 32 columns are a whole 128-byte box row for FP32 output and
+                    // half of one for BF16; a box is 32 rows (one per lane).
+                    const int half = f32_out ? 0 : (u & 1);
+                    uint8_t* box = stg + (stores & 1) * 4096;
+                    if (half == 0) {
+                        if (stores >= 2 && lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+                    }
+                    uint8_t* rowp = box + lane * 128;
+                    const int sw = lane & 7;
+                    if (f32_out) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 w = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                                       __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+                            *reinterpret_cast<uint4*>(rowp + ((c ^ sw) << 4)) = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 w = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                                                       pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                                       pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                                       pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+                            *reinterpret_cast<uint4*>(rowp + (((half * 4 + c) ^ sw) << 4)) = w;
+                        }
+                    }
+                    if (f32_out || half == 1) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int x = f32_out ? col0 : col0 - 32;
+                            tma_store_2d(&tmD, box, x, mb * CF::BM + q * 32);
+                            bulk_commit();
+                        }
+                        ++stores;
+                    }
+                }
+            }
+            if constexpr (CF::MODE == MODE_ROWQ) {
+                if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
+            }
+        }
+        if (!ok) raise_error(p, ERR_TIMEOUT_EPILOGUE, abort_flag);
+        if (lane == 0) {
+            bulk_wait_all();
+            if constexpr (CF::MODE == MODE_ROWQ) {
+                fence_proxy_async_global();
+                __threadfence();
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, CF::TMEM_COLS);
+    }
+
+    if constexpr (CF::MODE == MODE_ROWQ) {
+        // ---------------------------------------------------------- grid barrier
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(p.barrier, 1u);
+            const uint64_t t0 = globaltimer();
+            while (true) {
+                unsigned seen;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(p.barrier) : "memory");
+                if (seen >= gridDim.x) break;
+                if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
+                    raise_error(p, ERR_TIMEOUT_GRID_BARRIER, abort_flag);
+                    break;
+                }
+                __nanosleep(256);
+            }
+            __threadfence();
+        }
+        __syncthreads();
+        if (*abort_flag) return;
+        // ---------------------------------------------------------- requantise
+        // s[m] = amax[m] / 448; q = RN_E4M3(y * (1 / s[m])), saturating.
+        const int64_t groups_per_row = p.N / 16;
+        const int64_t total = static_cast<int64_t>(p.M) * groups_per_row;
+        for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+             g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+            const int64_t m = g / groups_per_row;
+            const int64_t n0 = (g - m * groups_per_row) * 16;
+            const float amax = __uint_as_float(__ldcg(p.amax + m));
+            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
+            const uint4* src = reinterpret_cast<const uint4*>(p.stash + m * p.N + n0);
+            const uint4 y0 = __ldcg(src), y1 = __ldcg(src + 1);
+            const uint32_t w[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
+                const uint32_t hi = pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
+                o[h] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(p.q_out + m * p.N + n0) = make_uint4(o[0], o[1], o[2], o[3]);
+            if (n0 == 0) p.out_row_scale[m] = s;
+        }
+    }
+}
+
+}  // namespace dg

@@ -1,0 +1,28 @@
+// inst_bf16.cu -- the BF16 (kind::f16) kernel variants.
+#include "kernels.h"
+
+namespace dg {
+
+const KernelInfo* kernels_bf16(int* count) {
+    //                  BN  FP8    A_MN   B_MN   MODE
+    static const KernelInfo table[] = {
+        make_info<Cfg<256, false, false, true, MODE_TILE>>(),   // B stored K x N
+        make_info<Cfg<128, false, false, true, MODE_TILE>>(),
+        make_info<Cfg<64, false, false, true, MODE_TILE>>(),
+        make_info<Cfg<256, false, false, false, MODE_TILE>>(),  // B stored N x K
+        make_info<Cfg<128, false, false, false, MODE_TILE>>(),
+        make_info<Cfg<64, false, false, false, MODE_TILE>>(),
+        make_info<Cfg<16, false, false, false, MODE_SWAP>>(),   // small M, B stored N x K
+        make_info<Cfg<32, false, false, false, MODE_SWAP>>(),
+        make_info<Cfg<64, false, false, false, MODE_SWAP>>(),
+        make_info<Cfg<16, false, true, false, MODE_SWAP>>(),    // small M, B stored K x N
+        make_info<Cfg<32, false, true, false, MODE_SWAP>>(),
+        make_info<Cfg<64, false, true, false, MODE_SWAP>>(),
+        make_info<Cfg<256, false, false, false, MODE_ROWQ>>(),  // E4M3 row requantisation
+        make_info<Cfg<256, false, false, true, MODE_ROWQ>>(),
+    };
+    *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
+    return table;
+}
+
+}  // namespace dg

@@ -1,0 +1,27 @@
+// inst_fp8.cu -- the FP8 E4M3 (kind::f8f6f4) kernel variants.
+#include "kernels.h"
+
+namespace dg {
+
+const KernelInfo* kernels_fp8(int* count) {
+    //                  BN  FP8   A_MN   B_MN   MODE
+    static const KernelInfo table[] = {
+        make_info<Cfg<256, true, false, false, MODE_TILE>>(),   // B stored N x K
+        make_info<Cfg<128, true, false, false, MODE_TILE>>(),
+        make_info<Cfg<64, true, false, false, MODE_TILE>>(),
+        make_info<Cfg<256, true, false, true, MODE_TILE>>(),    // B stored K x N
+        make_info<Cfg<128, true, false, true, MODE_TILE>>(),
+        make_info<Cfg<16, true, false, false, MODE_SWAP>>(),    // small M, B stored N x K
+        make_info<Cfg<32, true, false, false, MODE_SWAP>>(),
+        make_info<Cfg<64, true, false, false, MODE_SWAP>>(),
+        make_info<Cfg<16, true, true, false, MODE_SWAP>>(),     // small M, B stored K x N
+        make_info<Cfg<32, true, true, false, MODE_SWAP>>(),
+        make_info<Cfg<64, true, true, false, MODE_SWAP>>(),
+        make_info<Cfg<256, true, false, false, MODE_ROWQ>>(),   // E4M3 row requantisation
+        make_info<Cfg<256, true, false, true, MODE_ROWQ>>(),
+    };
+    *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
+    return table;
+}
+
+}  // namespace dg

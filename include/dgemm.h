@@ -1,0 +1,182 @@
+/*
+ * dgemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * The library computes, on one GPU,
+ *
+ *     D = epilogue( alpha * op(A) . op(B) + beta * C )
+ *
+ * in two forms: BF16 operands with FP32 accumulation (dgemm_bf16), and FP8
+ * E4M3 operands with one FP32 scale per row of A (per token) and one per
+ * output channel of B applied to the FP32 accumulator inside the kernel
+ * (dgemm_fp8_scaled). The epilogue (bias, activation, output conversion or
+ * per-row E4M3 requantisation) runs inside the same kernel, so no second
+ * kernel reads the product.
+ *
+ * Sources, cited by page title and section:
+ *   [W1] DeepGEMM write-up, czchanglian.com/news/51329: C = alpha*A*B + beta*C,
+ *        A is M x K, B is K x N (§1.1); FP32 accumulation of 16-bit inputs
+ *        (§3.1); fused bias + activation (§6.1); per-token output
+ *        quantisation in the epilogue (§6.2).
+ *   [W3] "DeepGEMM: FP8 Tensor Core GEMM", bjdmk.com.cn/news/6078902:
+ *        E4M3 operands with per-token x per-channel scales applied to the
+ *        accumulated result (§1.2, §3.2); the call takes pointers, M/N/K, a
+ *        scale descriptor, a workspace whose size is queried first so nothing
+ *        is allocated at run time, and a CUDA stream (§5.1).
+ *
+ * Conventions shared by every entry point
+ *   - All matrices are row-major and contiguous: A is M x K (leading
+ *     dimension K); B is K x N (DGEMM_B_KN, leading dimension N) or N x K
+ *     (DGEMM_B_NK, leading dimension K: the weight layout of a linear layer,
+ *     D = A . B^T); C and D are M x N (leading dimension N).
+ *   - Every pointer argument except `stream` is a DEVICE pointer, except the
+ *     `epi` and `plan` structs, which live in host memory and are read or
+ *     written before the call returns. The caller owns all memory; the library
+ *     allocates none, per call or otherwise (it only caches small host-side
+ *     state such as device properties).
+ *   - Device pointers must be 16-byte aligned and every leading dimension in
+ *     bytes a multiple of 16 (the tensor-memory-accelerator rule); otherwise
+ *     the call returns DGEMM_ERR_MISALIGNED before launching anything.
+ *   - M == 0 or N == 0: nothing to do, DGEMM_OK. K == 0 is valid: the product
+ *     is zero and D = epilogue(beta * C).
+ *   - beta == 0: C is not read and may be NULL (BLAS convention). C may equal
+ *     D (in-place update) when c_dtype == d_dtype.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream). Argument errors return synchronously, before launch.
+ *     A failed launch returns DGEMM_ERR_CUDA. A device-side wait that gives up
+ *     (bounded waits, about one second) sets a sticky per-device flag that
+ *     dgemm_query_device_status reports.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a); any other
+ *     device gives DGEMM_ERR_ARCH.
+ */
+#ifndef DGEMM_H
+#define DGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* The same type as cudaStream_t. */
+typedef struct CUstream_st* dgemm_stream_t;
+
+typedef enum {
+    DGEMM_OK = 0,
+    DGEMM_ERR_INVALID_VALUE = 1,       /* NULL pointer, negative size, bad enum  */
+    DGEMM_ERR_NOT_SUPPORTED = 2,       /* valid request this build cannot serve  */
+    DGEMM_ERR_MISALIGNED = 3,          /* pointer or leading dimension alignment */
+    DGEMM_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < dgemm_workspace_size(...)   */
+    DGEMM_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed      */
+    DGEMM_ERR_DEVICE_TIMEOUT = 6,      /* a bounded device-side wait gave up     */
+    DGEMM_ERR_ARCH = 7                 /* device is not sm_103                   */
+} dgemm_status_t;
+
+typedef enum { DGEMM_F32 = 0, DGEMM_BF16 = 1, DGEMM_E4M3 = 2 } dgemm_dtype_t;
+
+typedef enum {
+    DGEMM_B_KN = 0, /* B stored K x N row-major                      */
+    DGEMM_B_NK = 1  /* B stored N x K row-major (D = A . B^T)         */
+} dgemm_b_layout_t;
+
+typedef enum {
+    DGEMM_ACT_NONE = 0,
+    DGEMM_ACT_RELU = 1,
+    DGEMM_ACT_GELU = 2, /* erf form: y/2 (1 + erf(y / sqrt 2))          */
+    DGEMM_ACT_SILU = 3  /* y / (1 + exp(-y))                             */
+} dgemm_act_t;
+
+typedef enum {
+    DGEMM_QUANT_NONE = 0,
+    /* D is E4M3 with one FP32 scale per row: s[m] = max_n |y[m,n]| / 448 and
+     * D[m,n] = RN_E4M3(y[m,n] / s[m]), saturating; a row of zeros gets s = 1.
+     * [W1] §6.2 (per-token output quantisation fused in the epilogue). */
+    DGEMM_QUANT_E4M3_ROW_AMAX = 1
+} dgemm_out_quant_t;
+
+/* Fused epilogue, applied in this order after alpha*acc + beta*C:
+ * + bias[n] -> activation -> output conversion or requantisation.
+ * [W1] §6.1-6.2. A NULL dgemm_epilogue_t* means: no bias, no activation, no
+ * requantisation. */
+typedef struct {
+    const float* bias;    /* [N] FP32 device pointer, or NULL                   */
+    int act;              /* dgemm_act_t                                        */
+    int out_quant;        /* dgemm_out_quant_t; E4M3_ROW_AMAX needs d_dtype E4M3 */
+    float* out_row_scale; /* [M] FP32 device pointer, written when out_quant != 0 */
+} dgemm_epilogue_t;
+
+/* What the planner chose for a problem (filled by dgemm_plan). */
+typedef struct {
+    int swap_ab;           /* 1: computes D^T = op(B)^T . A^T so the 128-row MMA
+                              dimension runs over N (small-M, decode shapes)     */
+    int tile_m, tile_n;    /* output tile of one CTA, in the MMA's orientation  */
+    int cta_group;         /* CTAs that share one MMA (1 or 2)                  */
+    int stages;            /* shared-memory pipeline depth                      */
+    int num_tiles;         /* output tiles                                      */
+    int grid;              /* CTAs launched (persistent: <= SM count)           */
+    int cooperative;       /* 1: launched cooperatively (grid-wide barrier)     */
+    int raster_group;      /* tile rows per band of the swizzled raster         */
+    size_t smem_bytes;     /* dynamic shared memory per CTA                     */
+    size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
+} dgemm_plan_t;
+
+/* BF16 GEMM: D = epi(alpha * A . op(B) + beta * C), FP32 accumulation.
+ *   A        [M,K] BF16.          B [K,N] or [N,K] BF16 per b_layout.
+ *   C        [M,N] of c_dtype (F32 or BF16); read only when beta != 0.
+ *   D        [M,N] of d_dtype: F32 or BF16, or E4M3 with
+ *            epi->out_quant == DGEMM_QUANT_E4M3_ROW_AMAX.
+ *   ws       device workspace of ws_bytes >= dgemm_workspace_size(0, ...);
+ *            may be NULL when that size is 0.
+ * [W1] §1.1, §3.1, §6. */
+dgemm_status_t dgemm_bf16(const void* A, const void* B, dgemm_b_layout_t b_layout,
+                          const void* C, dgemm_dtype_t c_dtype,
+                          void* D, dgemm_dtype_t d_dtype,
+                          int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                          const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes,
+                          dgemm_stream_t stream);
+
+/* FP8 E4M3 scaled GEMM:
+ *   D = epi(alpha * diag(a_scale) . (Aq . op(Bq)) . diag(b_scale) + beta * C)
+ *   Aq       [M,K] E4M3 codes (1 byte each).   Bq [K,N] or [N,K] E4M3 codes.
+ *   a_scale  [M] FP32, one per row of A (per token), stride 1.
+ *   b_scale  [N] FP32, one per output channel n, stride 1.
+ *   k_group  0: the scales are constant along K and are applied once to the
+ *            FP32 accumulator (exact); other values: DGEMM_ERR_NOT_SUPPORTED.
+ *   C, D, epi, ws as for dgemm_bf16.
+ * [W3] §1.2, §3.2, §5.1. */
+dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t b_layout,
+                                const float* a_scale, const float* b_scale, int k_group,
+                                const void* C, dgemm_dtype_t c_dtype,
+                                void* D, dgemm_dtype_t d_dtype,
+                                int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes,
+                                dgemm_stream_t stream);
+
+/* Workspace bytes a call with these arguments needs (0 when none). Query it
+ * once and pass a buffer at least this large ([W3] §5.1). Host-only; no GPU
+ * needed. Returns 0 for invalid arguments. */
+size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K,
+                            dgemm_b_layout_t b_layout, const dgemm_epilogue_t* epi);
+
+/* The plan a call with these arguments would use on a GPU with num_sms SMs.
+ * Host-only; no GPU needed. Returns DGEMM_OK and fills *plan, or the same
+ * argument error the GEMM call would return for these sizes. */
+dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K,
+                          dgemm_b_layout_t b_layout, dgemm_dtype_t d_dtype,
+                          const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan);
+
+/* Static English description of a status code; never NULL. */
+const char* dgemm_status_string(dgemm_status_t status);
+
+/* Synchronises `stream`, then returns and clears the sticky device-side error
+ * flag of the current device (DGEMM_OK, or DGEMM_ERR_DEVICE_TIMEOUT if some
+ * kernel on this device gave up a bounded wait since the last query), or
+ * DGEMM_ERR_CUDA if the stream itself reports an error. */
+dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGEMM_H */

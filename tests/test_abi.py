@@ -1,0 +1,106 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and the host-side logic (validation, planning, workspace
+sizes, status strings) behaves as documented. No compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_persistent_gb300 as dg
+from dense_gemm_persistent_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return dg.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(dgemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert names == sorted(["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_workspace_size", "dgemm_plan",
+                            "dgemm_status_string", "dgemm_query_device_status"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, name
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = dg.dgemm_status_string(code)
+        assert s and s != "unknown status"
+    assert dg.dgemm_status_string(99) == "unknown status"
+
+
+def call_bf16(lib, **over):
+    args = dict(A=16, B=16, bl=1, C=None, c_dt=0, D=16, d_dt=1, M=128, N=128, K=128, alpha=1.0, beta=0.0,
+                epi=None, ws=None, ws_bytes=0, stream=None)
+    args.update(over)
+    return lib.dgemm_bf16(args["A"], args["B"], args["bl"], args["C"], args["c_dt"], args["D"], args["d_dt"],
+                          args["M"], args["N"], args["K"], args["alpha"], args["beta"], args["epi"], args["ws"],
+                          args["ws_bytes"], args["stream"])
+
+
+def test_argument_errors_return_before_any_device_call(lib):
+    # These return synchronously from validation (no CUDA call is reached).
+    assert call_bf16(lib, M=-1) == 1
+    assert call_bf16(lib, bl=7) == 1
+    assert call_bf16(lib, d_dt=9) == 1
+    assert call_bf16(lib, K=100) == 3                 # 200-byte A rows: not a multiple of 16
+    assert call_bf16(lib, bl=0, N=100) == 3           # K x N B with 200-byte rows
+    assert call_bf16(lib, A=8) == 3                   # misaligned pointer
+    assert call_bf16(lib, A=None) == 1                # NULL operand
+    assert call_bf16(lib, beta=1.0) == 1              # beta != 0 needs C
+    assert call_bf16(lib, d_dt=2) == 1                # E4M3 output needs the requant epilogue
+    epi = _lib.Epilogue(None, 0, 1, None)             # requant without a row-scale pointer
+    assert call_bf16(lib, d_dt=2, epi=ctypes.byref(epi)) == 1
+    epi = _lib.Epilogue(None, 0, 1, 16)
+    assert call_bf16(lib, d_dt=2, epi=ctypes.byref(epi)) == 4   # no workspace
+    epi = _lib.Epilogue(None, 9, 0, None)
+    assert call_bf16(lib, epi=ctypes.byref(epi)) == 1           # bad activation
+    # empty problems are a no-op and need no device
+    assert call_bf16(lib, M=0) == 0 and call_bf16(lib, N=0) == 0
+    # fp8 per-group scales are not built
+    assert lib.dgemm_fp8_scaled(16, 16, 1, 16, 16, 128, None, 0, 16, 1, 128, 128, 128, 1.0, 0.0, None,
+                                None, 0, None) == 2
+
+
+def test_workspace_sizes(lib):
+    assert dg.dgemm_workspace_size(1, 4096, 11008, 4096, "nk") == 0
+    ws = dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax")
+    assert ws == 256 + 8192 * 4 + 8192 * 8192 * 2
+
+
+def test_plans_for_the_five_workloads(lib):
+    p1 = dg.dgemm_plan(0, 512, 512, 512, "kn", "f32", num_sms=152)
+    assert p1["swap_ab"] == 0 and p1["grid"] <= 152 and p1["tile_n"] == 64
+    p2 = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
+    assert p2["tile_n"] == 256 and p2["num_tiles"] == 512 and p2["grid"] == 152
+    p3 = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
+    assert p3["num_tiles"] == 32 * 43 and p3["grid"] == 152
+    p4 = dg.dgemm_plan(0, 16, 18432, 7168, "nk", "bf16", num_sms=152)
+    assert p4["swap_ab"] == 1 and p4["tile_n"] == 16 and p4["num_tiles"] == 144 and p4["grid"] == 144
+    p5 = dg.dgemm_plan(1, 8192, 8192, 8192, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=152)
+    assert p5["cooperative"] == 1 and p5["tile_n"] == 256 and p5["num_tiles"] == 64 * 32
+    for p in (p1, p2, p3, p4, p5):
+        assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
+
+
+def test_tile_width_override(lib, monkeypatch):
+    monkeypatch.setenv("DGEMM_TILE_N", "128")
+    assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tile_n"] == 128
+    monkeypatch.setenv("DGEMM_TILE_N", "96")     # no such variant: ignored
+    assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tile_n"] == 256

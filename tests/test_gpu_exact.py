@@ -1,0 +1,110 @@
+"""Bit-exact GPU == oracle on small-integer inputs.
+
+With integer operands of magnitude <= 8 every product is exact and every FP32
+partial sum stays below 2^24, so the GPU result must equal the oracle exactly
+whatever the accumulation order. A wrong shared-memory descriptor, swizzle,
+operand layout, TMEM lane mapping or pipeline phase shows up here as a
+mismatch instead of hiding inside a tolerance. Shapes are ragged in M, N and K
+(tails of every tile dimension) and span several tiles.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_persistent_gb300 as dg
+import oracle
+import workloads as wl
+from gpu_util import dev
+
+pytestmark = pytest.mark.gpu
+
+
+def int_bf16(rng, shape, lo=-4, hi=4):
+    return torch.from_numpy(rng.integers(lo, hi + 1, size=shape).astype(np.float32)).to(torch.bfloat16)
+
+
+def int_e4m3(rng, shape, lo=-8, hi=8):
+    return torch.from_numpy(rng.integers(lo, hi + 1, size=shape).astype(np.float32)).to(torch.float8_e4m3fn)
+
+
+def bf16_case(M, N, K, layout, seed, d_dtype=torch.float32):
+    rng = np.random.default_rng(seed)
+    A = int_bf16(rng, (M, K))
+    B = int_bf16(rng, (K, N) if layout == "kn" else (N, K))
+    D = torch.empty(M, N, dtype=d_dtype, device=dev())
+    dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout=layout)
+    assert dg.dgemm_query_device_status() == 0
+    ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), layout)
+    return D.cpu().to(torch.float64).numpy(), ref
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_bf16_tile_exact(layout, bn, monkeypatch):
+    monkeypatch.setenv("DGEMM_TILE_N", str(bn))
+    got, ref = bf16_case(300, 520, 200, layout, seed=bn)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 64])
+def test_bf16_swap_exact(layout, M):
+    plan = dg.dgemm_plan(0, M, 304, 200, layout, "f32")
+    assert plan["swap_ab"] == 1
+    got, ref = bf16_case(M, 304, 200, layout, seed=M)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_bf16_exact_bf16_output(layout):
+    # the FP32 sums are exact integers, so one rounding to BF16 must give exactly
+    # the correctly rounded oracle value
+    got, ref = bf16_case(257, 384, 72, layout, seed=3, d_dtype=torch.bfloat16)
+    assert np.array_equal(got, oracle.round_bf16(ref))
+
+
+def fp8_case(M, N, K, layout, seed, scales="pow2"):
+    rng = np.random.default_rng(seed)
+    Aq = int_e4m3(rng, (M, K))
+    Bq = int_e4m3(rng, (K, N) if layout == "kn" else (N, K))
+    if scales == "pow2":   # powers of two keep everything exact
+        sa = torch.from_numpy(np.exp2(rng.integers(-3, 4, size=M)).astype(np.float32))
+        sb = torch.from_numpy(np.exp2(rng.integers(-3, 4, size=N)).astype(np.float32))
+    else:
+        sa, sb = torch.ones(M), torch.ones(N)
+    D = torch.empty(M, N, dtype=torch.float32, device=dev())
+    dg.dgemm_fp8_scaled(Aq.to(dev()), Bq.to(dev()), sa.to(dev()), sb.to(dev()), D, b_layout=layout)
+    assert dg.dgemm_query_device_status() == 0
+    ref = oracle.fp8_gemm_ref(wl.codes_u8(Aq), wl.codes_u8(Bq), layout, sa.numpy(), sb.numpy())
+    return D.cpu().to(torch.float64).numpy(), ref
+
+
+@pytest.mark.parametrize("layout,bn", [("nk", 64), ("nk", 128), ("nk", 256), ("kn", 128), ("kn", 256)])
+def test_fp8_tile_exact(layout, bn, monkeypatch):
+    monkeypatch.setenv("DGEMM_TILE_N", str(bn))
+    got, ref = fp8_case(300, 528, 272, layout, seed=100 + bn)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M", [1, 16, 40, 64])
+def test_fp8_swap_exact(layout, M):
+    got, ref = fp8_case(M, 400, 272, layout, seed=200 + M)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("kblocks", [1, 2, 3, 4, 5, 9, 13])
+def test_odd_k_block_counts_exact(kblocks, monkeypatch):
+    """Odd numbers of K slices expose pipeline-phase bugs (DeepGEMM write-up,
+    czchanglian.com/news/51329, §4.3); 640 tiles of 128x64 over at most 152 CTAs
+    also carry the stage and accumulator phases across several tiles per CTA."""
+    monkeypatch.setenv("DGEMM_TILE_N", "64")
+    got, ref = bf16_case(2560, 2048, 64 * kblocks, "nk", seed=kblocks)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("kblocks", [1, 3, 4, 5, 7])
+def test_odd_k_block_counts_wide_tile_exact(kblocks, monkeypatch):
+    monkeypatch.setenv("DGEMM_TILE_N", "256")
+    got, ref = bf16_case(2560, 4096, 64 * kblocks, "kn", seed=50 + kblocks)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
