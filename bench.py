@@ -1,0 +1,429 @@
+"""Benchmark of the GB300 dense GEMM library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+
+One step is one call of the library on one batch of synthetic input (the
+seeded workloads of workloads.py). The default workload is number 2, the BF16
+GEMM M = N = K = 4096, on which the headline metric (TFLOPS and fraction of the
+dense tensor-core peak) is quoted; --config picks another. Input sets are
+rotated so that the operands of every timed call were evicted from L2 (their
+total is several times the 129 MB L2).
+
+Rank 0 prints ONE JSON line. Under torchrun (N > 1) every rank runs the same
+workload on its own GPU (independent replicas: GEMM problems shard without any
+collective), the timed region is bracketed by barriers, and the time is the
+maximum over ranks.
+
+--impl reference times the oracle (oracle/, the float64 CPU restatement) on
+the host cores on a bounded sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS and % of GB300 dense BF16/FP8 peak (HBM % for skinny M)"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DESCRIPTIONS = {
+    1: "BF16 GEMM M=N=K=512, B KxN, alpha 1.5, beta 0.5, FP32 C0 -> FP32 D",
+    2: "BF16 GEMM M=N=K=4096, B KxN, N(0,1)/sqrt(K) entries -> BF16 D",
+    3: "FP8 E4M3 GEMM M=4096 N=11008 K=4096, per-token x per-channel scales -> BF16 D",
+    4: "decode BF16 GEMM M=16 N=18432 K=7168, weights NxK -> BF16 D",
+    5: "FP8 E4M3 GEMM M=N=K=8192 + bias -> SiLU -> per-row E4M3 requant",
+}
+DEFAULT_STEPS = {1: 20000, 2: 10000, 3: 4000, 4: 20000, 5: 2000}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_persistent_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: int):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if kv.get("workload") == str(workload) and kv.get("kernel_src_sha") == want:
+            return int(float(kv["dram_bytes_per_launch"]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(w, seconds: float):
+    """Time the oracle on whole rows of the workload until `seconds` have passed
+    (at least one row); returns (flops, elapsed, rows, threads)."""
+    import oracle
+    import workloads as wl
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    C = None if w.C is None else w.C.numpy()
+    if w.form == "bf16":
+        A, B = wl.bits_u16(w.A), wl.bits_u16(w.B)
+    else:
+        A, B = wl.codes_u8(w.A), wl.codes_u8(w.B)
+    done, chunk, t0 = 0, 1, time.perf_counter()
+    while done < w.M:
+        rows = (done, min(w.M, done + chunk))
+        if w.form == "bf16":
+            oracle.bf16_gemm_ref(A, B, w.b_layout, C, w.alpha, w.beta, rows=rows, nthreads=threads)
+        else:
+            y = oracle.fp8_gemm_ref(A, B, w.b_layout, w.a_scale.numpy(), w.b_scale.numpy(), C, w.alpha, w.beta,
+                                    None if w.bias is None else w.bias.numpy(), w.act, rows=rows,
+                                    nthreads=threads)
+            if w.out_quant != "none":
+                oracle.requant_rows(y)
+        done = rows[1]
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+        chunk = min(2 * chunk, max(1, threads * 4))
+    el = time.perf_counter() - t0
+    return 2.0 * done * w.N * w.K, el, done, threads
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import dense_gemm_persistent_gb300 as dg
+    import workloads as wl
+    from dense_gemm_persistent_gb300 import roofline
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dg.load()
+    w = wl.make(args.config)
+    peaks, peak_kind = measured_peaks()
+
+    # ---- rotating input sets (each timed call finds its operands out of L2)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}[w.d_dtype]
+    ws_bytes = dg.dgemm_workspace_size(w.form == "fp8", w.M, w.N, w.K, w.b_layout, out_quant=w.out_quant)
+    in_bytes = sum(t.numel() * t.element_size() for t in w.tensors().values())
+    out_bytes = w.M * w.N * torch.tensor([], dtype=tdt).element_size()
+    set_bytes = in_bytes + out_bytes + ws_bytes
+    nsets = max(2, min(160, math.ceil(3 * L2_BYTES / max(set_bytes, 1))))
+    sets = []
+    for _ in range(nsets):
+        g = w.to(dev)
+        D = torch.empty(w.M, w.N, dtype=tdt, device=dev)
+        s = torch.empty(w.M, dtype=torch.float32, device=dev) if w.out_quant != "none" else None
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+        sets.append((g, D, s, ws))
+    stream = torch.cuda.current_stream(dev)
+
+    def call(i):
+        g, D, s, ws = sets[i % nsets]
+        kw = dict(b_layout=w.b_layout, C=g.C, alpha=w.alpha, beta=w.beta, bias=g.bias, act=w.act,
+                  out_quant=w.out_quant, out_row_scale=s, ws=ws, stream=stream)
+        if w.form == "bf16":
+            dg.dgemm_bf16(g.A, g.B, D, **kw)
+        else:
+            dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, **kw)
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def barrier():
+        if dist:
+            tdist.barrier()
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize(dev)
+    if dg.dgemm_query_device_status(stream) != 0:
+        raise RuntimeError("device status after warm-up")
+
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    if dg.dgemm_query_device_status(stream) != 0:
+        raise RuntimeError("device status after the timed region")
+    ms_step = ms_total / args.steps
+    flops = w.flops
+    tflops = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device, call, result -> host
+    host = {k: t.pin_memory() for k, t in w.tensors().items()}
+    g, D, s, ws = sets[0]
+    Dh = torch.empty(D.shape, dtype=D.dtype, pin_memory=True)
+    sh = torch.empty(w.M, dtype=torch.float32, pin_memory=True) if s is not None else None
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = Dh.numel() * Dh.element_size() + (sh.numel() * 4 if sh is not None else 0)
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for k, t in host.items():
+            getattr(g, k).copy_(t, non_blocking=True)
+        call(0)
+        Dh.copy_(D, non_blocking=True)
+        if sh is not None:
+            sh.copy_(s, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = f0.elapsed_time(f1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- roofline of the kernel (one launch per step)
+    plan = dg.dgemm_plan(w.form == "fp8", w.M, w.N, w.K, w.b_layout, w.d_dtype, out_quant=w.out_quant,
+                         act=w.act, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+    skinny = args.config == 4
+    dsz = {"f32": 4, "bf16": 2, "e4m3": 1}[w.d_dtype]
+    esz = 2 if w.form == "bf16" else 1
+    c_in = 4 if (w.C is not None and w.beta != 0) else 0
+    comp = roofline.compulsory_bytes(w.M, w.N, w.K, esz, esz, c_in, dsz)
+    if skinny:
+        achieved = comp / (ms_step * 1e-3) / 1e9
+        peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+    else:
+        achieved = flops / (ms_step * 1e-3) / 1e12
+        base = peaks["bf16_tflops"]
+        peak = base if w.form == "bf16" else 2.0 * base   # FP8:BF16 dense ratio 2
+        unit, bound = "TFLOP/s", "tensor"
+    traffic = recorded_traffic(args.config)
+    roof = {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{peak_kind}" + ("" if w.form == "bf16" or skinny else " bf16 x 2 (FP8:BF16 ratio)"),
+            "compulsory_bytes": int(comp),
+            "tiled_traffic_bytes_no_l2": int(roofline.tiled_read_elements(w.M, w.N, w.K, plan["tile_m"],
+                                                                          plan["tile_n"]) * esz
+                                             + w.M * w.N * (dsz + c_in))}
+
+    result = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.form == "bf16" else "e4m3", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.config], "number": args.config, "M": w.M, "N": w.N, "K": w.K,
+                   "b_layout": w.b_layout, "parallelism": f"replicas x{world}",
+                   "l2": f"rotating {nsets} input sets of {set_bytes / 2**20:.0f} MiB (> L2 129 MiB)",
+                   "plan": {k: plan[k] for k in ("swap_ab", "tile_m", "tile_n", "stages", "num_tiles", "grid",
+                                                 "cooperative")}},
+        "clocks": clocks,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "roofline": roof,
+    }
+    if skinny:
+        result["hbm_gbs"] = round(achieved, 1)
+    return result, w
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU time spent on the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="wall time the reference arm spends on warm-up + steps")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.config]
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    result, w = run_ours(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, el, rows, threads = oracle_sample(w, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(fl / el / 1e12, 6), "unit": "TFLOPS", "cores": threads,
+                                  "kind": "oracle", "seconds": round(el, 2),
+                                  "sample": f"{rows} of {w.M} rows of the same workload "
+                                            f"(2*rows*N*K = {fl:.3g} FLOP), float64 oracle, OpenMP"}
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def run_reference(args, world):
+    """The reference arm: the oracle timed on the host cores, each step a bounded
+    sample (whole rows) of the same workload, sized so warm-up + steps take about
+    two minutes."""
+    import workloads as wl
+    w = wl.make(args.config)
+    budget = args.ref_seconds / (args.steps + args.warmup)
+    # calibrate rows per step on one row
+    fl, el, rows, threads = oracle_sample(w, 0.0)
+    per_row = el / max(rows, 1)
+    rows_per_step = max(1, min(w.M, int(budget / max(per_row, 1e-9))))
+    import oracle
+    C = None if w.C is None else w.C.numpy()
+    A = wl.bits_u16(w.A) if w.form == "bf16" else wl.codes_u8(w.A)
+    B = wl.bits_u16(w.B) if w.form == "bf16" else wl.codes_u8(w.B)
+
+    def step(i):
+        r0 = (i * rows_per_step) % w.M
+        rows = (r0, min(w.M, r0 + rows_per_step))
+        if w.form == "bf16":
+            oracle.bf16_gemm_ref(A, B, w.b_layout, C, w.alpha, w.beta, rows=rows, nthreads=threads)
+        else:
+            y = oracle.fp8_gemm_ref(A, B, w.b_layout, w.a_scale.numpy(), w.b_scale.numpy(), C, w.alpha, w.beta,
+                                    None if w.bias is None else w.bias.numpy(), w.act, rows=rows,
+                                    nthreads=threads)
+            if w.out_quant != "none":
+                oracle.requant_rows(y)
+        return rows[1] - rows[0]
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        done += step(i)
+    el = time.perf_counter() - t0
+    value = 2.0 * done * w.N * w.K / el / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.config], "number": args.config, "M": w.M, "N": w.N, "K": w.K,
+                   "b_layout": w.b_layout},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows of {w.M} per step of the same workload, float64 "
+                                   f"oracle, OpenMP"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+if __name__ == "__main__":
+    sys.exit(main())

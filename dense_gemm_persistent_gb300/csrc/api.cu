@@ -67,6 +67,7 @@ struct Plan {
     int a_mn, b_mn;
     int64_t Mm, Nm;    // problem in the MMA's orientation
     int bk;            // K elements per stage
+    int acc_stride;    // TMEM columns between the two accumulator buffers
 };
 
 // Validates the sizes, enums and epilogue; picks the kernel variant and grid.
@@ -148,6 +149,21 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.cooperative = p.mode == dg::MODE_ROWQ ? 1 : 0;
     p.pub.raster_group = static_cast<int>(tiles_m < 8 ? (tiles_m > 0 ? tiles_m : 1) : 8);
     p.pub.smem_bytes = static_cast<size_t>(k->smem_bytes);
+    // K-group promotion. The transposed small-M kernel owns all 512 TMEM
+    // columns but needs only BN per accumulator: it splits K into as many
+    // groups as fit (two buffers of 256 columns when a CTA runs several tiles,
+    // one of 512 when it runs one) and sums them in FP32, which cuts the
+    // tensor core's round-toward-zero accumulation error by about that factor.
+    const int64_t k_blocks = (K + p.bk - 1) / p.bk;
+    int groups = 1;
+    p.acc_stride = bn;
+    if (p.mode == dg::MODE_SWAP) {
+        const bool one_tile = p.pub.num_tiles <= p.pub.grid;
+        const int max_groups = (one_tile ? 512 : 256) / bn;
+        groups = static_cast<int>(k_blocks < max_groups ? (k_blocks > 0 ? k_blocks : 1) : max_groups);
+        p.acc_stride = groups * bn;
+    }
+    p.pub.k_groups = groups;
     p.pub.workspace_bytes =
         oq ? kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2 : 0;
     *out = p;
@@ -292,6 +308,8 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.num_tiles = plan.pub.num_tiles;
     p.k_blocks = static_cast<int>((K + plan.bk - 1) / plan.bk);
     p.group_m = plan.pub.raster_group;
+    p.acc_groups = plan.pub.k_groups;
+    p.acc_stride = plan.acc_stride;
     p.alpha = alpha;
     p.beta = beta;
     p.C = beta != 0.0f ? C : nullptr;

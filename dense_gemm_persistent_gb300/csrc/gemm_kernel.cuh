@@ -49,6 +49,11 @@ struct Params {
     // Problem in the MMA's orientation: rows M, columns N, reduction K.
     int M, N, K;
     int tiles_m, tiles_n, num_tiles, k_blocks, group_m;
+    // K-group promotion: the K slices of a tile are split into acc_groups
+    // contiguous groups, each accumulated by the tensor core into its own TMEM
+    // accumulator (BN columns apart) and summed in FP32 by the epilogue.
+    // acc_stride = TMEM columns between the two accumulator buffers.
+    int acc_groups, acc_stride;
     float alpha, beta;
     const void* C;  // beta != 0: C in the output's orientation
     int64_t ldc;
@@ -90,7 +95,8 @@ struct Cfg {
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
-    static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+    static constexpr int TMEM_COLS = (MODE == MODE_SWAP) ? 512
+                                   : (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr uint32_t IDESC = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, BM, BN);
     static constexpr int NUM_THREADS = 192;
@@ -337,13 +343,19 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * CF::BN);
+                const uint32_t acc_base = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
+                int group = -1;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    // contiguous, even split of the K slices over the groups
+                    const int g = static_cast<int>((static_cast<int64_t>(kb) * p.acc_groups) / p.k_blocks);
+                    const bool first_in_group = (g != group);
+                    group = g;
+                    const uint32_t d_tmem = acc_base + static_cast<uint32_t>(g * CF::BN);
                     const uint32_t a0 = smem_u32(stages + stage * CF::STAGE_BYTES);
                     const uint32_t b0 = a0 + CF::A_BYTES;
 #pragma unroll
@@ -352,7 +364,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                                      : smem_desc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bd = CF::B_MN ? smem_desc_sw128(b0 + k * CF::UMMA_K * 128, CF::BK * 128, 1024)
                                                      : smem_desc_sw128(b0 + k * 32, 16, 1024);
-                        const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+                        const uint32_t acc = (!first_in_group || k > 0) ? 1u : 0u;
                         if constexpr (CF::FP8)
                             mma_f8(d_tmem, ad, bd, CF::IDESC, acc);
                         else
@@ -391,7 +403,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             }
             tc_fence_after();
             const int row = mb * CF::BM + q * 32 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * CF::BN);
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(buf * p.acc_stride);
+            const int groups = p.k_blocks > 0 ? p.acc_groups : 1;
             const float rs = (p.row_scale && row < p.M) ? p.row_scale[row] : 1.0f;
             float bias_row = 0.0f;
             if constexpr (CF::MODE == MODE_SWAP)
@@ -402,20 +416,26 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             for (int u = 0; u < CF::BN / UNIT; ++u) {
                 const int col0 = nb * CF::BN + u * UNIT;
                 float v[32];
-                if constexpr (UNIT == 32) {
-                    uint32_t r[32];
-                    tmem_ld32(taddr + u * 32, r);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                } else {
-                    uint32_t r[16];
-                    tmem_ld16(taddr + u * 16, r);
-                    tmem_ld_wait();
+                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                // FP32 sum of the K-group partial accumulators (one group unless
+                // K-group promotion is on), added in group order.
+#pragma unroll 1
+                for (int g = 0; g < groups; ++g) {
+                    const uint32_t ta = taddr + static_cast<uint32_t>(g * CF::BN + u * UNIT);
+                    if constexpr (UNIT == 32) {
+                        uint32_t r[32];
+                        tmem_ld32(ta, r);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(r[j]);
+                    } else {
+                        uint32_t r[16];
+                        tmem_ld16(ta, r);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 16; j < 32; ++j) v[j] = 0.0f;
+                        for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+                    }
                 }
                 if (p.k_blocks == 0) {
 #pragma unroll
@@ -535,27 +555,48 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         if (*abort_flag) return;
         // ---------------------------------------------------------- requantise
         // s[m] = amax[m] / 448; q = RN_E4M3(y * (1 / s[m])), saturating.
+        // Each thread keeps RQ_UNROLL independent 32-byte loads in flight so the
+        // pass runs at memory bandwidth rather than at one load's latency.
+        constexpr int RQ_UNROLL = 8;
         const int64_t groups_per_row = p.N / 16;
         const int64_t total = static_cast<int64_t>(p.M) * groups_per_row;
-        for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
-             g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-            const int64_t m = g / groups_per_row;
-            const int64_t n0 = (g - m * groups_per_row) * 16;
-            const float amax = __uint_as_float(__ldcg(p.amax + m));
-            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
-            const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
-            const uint4* src = reinterpret_cast<const uint4*>(p.stash + m * p.N + n0);
-            const uint4 y0 = __ldcg(src), y1 = __ldcg(src + 1);
-            const uint32_t w[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-            uint32_t o[4];
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+        for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+             base += stride * RQ_UNROLL) {
+            uint4 y0[RQ_UNROLL], y1[RQ_UNROLL];
+            unsigned am[RQ_UNROLL];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
-                const uint32_t hi = pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
-                o[h] = lo | (hi << 16);
+            for (int u = 0; u < RQ_UNROLL; ++u) {
+                const int64_t g = base + u * stride;
+                if (g < total) {
+                    const int64_t m = g / groups_per_row;
+                    const int64_t n0 = (g - m * groups_per_row) * 16;
+                    const uint4* src = reinterpret_cast<const uint4*>(p.stash + m * p.N + n0);
+                    y0[u] = __ldcg(src);
+                    y1[u] = __ldcg(src + 1);
+                    am[u] = __ldcg(p.amax + m);
+                }
             }
-            *reinterpret_cast<uint4*>(p.q_out + m * p.N + n0) = make_uint4(o[0], o[1], o[2], o[3]);
-            if (n0 == 0) p.out_row_scale[m] = s;
+#pragma unroll
+            for (int u = 0; u < RQ_UNROLL; ++u) {
+                const int64_t g = base + u * stride;
+                if (g >= total) break;
+                const int64_t m = g / groups_per_row;
+                const int64_t n0 = (g - m * groups_per_row) * 16;
+                const float amax = __uint_as_float(am[u]);
+                const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+                const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
+                const uint32_t w[8] = {y0[u].x, y0[u].y, y0[u].z, y0[u].w, y1[u].x, y1[u].y, y1[u].z, y1[u].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
+                    const uint32_t hi = pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
+                    o[h] = lo | (hi << 16);
+                }
+                *reinterpret_cast<uint4*>(p.q_out + m * p.N + n0) = make_uint4(o[0], o[1], o[2], o[3]);
+                if (n0 == 0) p.out_row_scale[m] = s;
+            }
         }
     }
 }

@@ -117,6 +117,9 @@ typedef struct {
     int grid;              /* CTAs launched (persistent: <= SM count)           */
     int cooperative;       /* 1: launched cooperatively (grid-wide barrier)     */
     int raster_group;      /* tile rows per band of the swizzled raster         */
+    int k_groups;          /* K-group promotion: K is split into this many
+                              contiguous groups, each accumulated by the tensor
+                              core separately and summed in FP32 (1 = off)      */
     size_t smem_bytes;     /* dynamic shared memory per CTA                     */
     size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
 } dgemm_plan_t;

@@ -227,36 +227,41 @@ def requant_rows(Z: np.ndarray):
 
 # ---- whole-path references for the five workloads ------------------------------
 
+def _row_select(X, rows):
+    """Rows of X picked by a (row0, row1) range or an index array (None: all)."""
+    if X is None or rows is None:
+        return X
+    X = np.asarray(X)
+    if isinstance(rows, tuple):
+        return X[rows[0]:rows[1]]
+    return X[np.asarray(rows, dtype=np.int64)]
+
+
 def bf16_gemm_ref(A_bits, B_bits, b_layout, C=None, alpha=1.0, beta=0.0, rows=None,
                   nthreads=None) -> np.ndarray:
     """Reference for the BF16 form: inputs are the raw BF16 bit patterns (uint16) the
-    GPU receives; C is float32 or BF16 bits; the result is exact-ish float64."""
-    A = decode_bf16(A_bits)
+    GPU receives; C is float32 or BF16 bits. ``rows`` ((row0, row1) or an index
+    array) restricts the result to those rows of D: the same GEMM on those rows of A."""
+    A = decode_bf16(_row_select(A_bits, rows))
     B = decode_bf16(B_bits)
     Cd = None
     if beta != 0.0:
-        Cd = decode_bf16(C) if C.dtype == np.uint16 else decode(np.asarray(C, np.float32), F32)
-    return gemm(A, B, b_layout, Cd, alpha, beta, rows, nthreads)
+        Cs = _row_select(C, rows)
+        Cd = decode_bf16(Cs) if Cs.dtype == np.uint16 else decode(np.asarray(Cs, np.float32), F32)
+    return gemm(A, B, b_layout, Cd, alpha, beta, None, nthreads)
 
 
 def fp8_gemm_ref(Aq, Bq, b_layout, a_scale, b_scale, C=None, alpha=1.0, beta=0.0,
                  bias=None, act="none", rows=None, nthreads=None) -> np.ndarray:
     """Reference for the FP8 form: D = alpha * diag(sa) (Aq Bq) diag(sb) + beta*C,
     then + bias and the activation, on the dequantised E4M3 values ([W3] §3.2)."""
-    if rows is not None:
-        r0, r1 = rows
-        Ad = dequant(np.asarray(Aq)[r0:r1], np.asarray(a_scale)[r0:r1], 0)
-        Cs = None if C is None else np.asarray(C)[r0:r1]
-        local_rows = None
-    else:
-        Ad = dequant(Aq, a_scale, 0)
-        Cs = C
-        local_rows = None
+    Ad = dequant(_row_select(Aq, rows), _row_select(a_scale, rows), 0)
+    Cs = _row_select(C, rows)
     Bd = dequant(Bq, b_scale, 0 if b_layout == "nk" else 1)
     Cd = None
     if beta != 0.0:
         Cd = decode_bf16(Cs) if Cs.dtype == np.uint16 else decode(np.asarray(Cs, np.float32), F32)
-    D = gemm(Ad, Bd, b_layout, Cd, alpha, beta, local_rows, nthreads)
+    D = gemm(Ad, Bd, b_layout, Cd, alpha, beta, None, nthreads)
     if bias is not None or act != "none":
         D = epilogue(D, bias, act)
     return D

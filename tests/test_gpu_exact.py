@@ -108,3 +108,14 @@ def test_odd_k_block_counts_wide_tile_exact(kblocks, monkeypatch):
     monkeypatch.setenv("DGEMM_TILE_N", "256")
     got, ref = bf16_case(2560, 4096, 64 * kblocks, "kn", seed=50 + kblocks)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("M,kblocks", [(16, 37), (16, 5), (40, 23), (64, 9)])
+def test_k_group_promotion_exact(M, kblocks):
+    """The small-M kernel splits K into several tensor-core accumulators summed in
+    FP32 (uneven splits here); integer inputs keep the result exact."""
+    K = 64 * kblocks
+    plan = dg.dgemm_plan(0, M, 304, K, "nk", "f32")
+    assert plan["swap_ab"] == 1 and plan["k_groups"] == min(kblocks, 512 // plan["tile_n"])
+    got, ref = bf16_case(M, 304, K, "nk", seed=300 + kblocks)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"

@@ -1,0 +1,65 @@
+"""The five workloads at their full sizes, in the launch configuration the
+benchmark times (the library's own plan), checked on sampled rows that the
+oracle computes one by one (whole rows, so every column tile is covered), and
+in full where the oracle is fast enough (workloads 1 and 4)."""
+import numpy as np
+import pytest
+
+import dense_gemm_persistent_gb300 as dg
+import oracle
+import workloads as wl
+from gpu_util import run_workload, to_f64
+from test_gpu_parity import ref_of
+from tolerances import bf16_ulp_ok, c1_ok, frob_ok, requant_ok
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def sample_rows(M, n=32, seed=0):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(M, size=min(n, M), replace=False).tolist()) | {0, 1, M - 2, M - 1}
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def test_workload1_full():
+    w = wl.make(1)
+    D, _ = run_workload(w)
+    ok, msg = c1_ok(to_f64(D), ref_of(w), w.K)
+    assert ok, msg
+
+
+def test_workload2_full_size_sampled_rows():
+    w = wl.make(2)
+    D, _ = run_workload(w)
+    rows = sample_rows(w.M, 48, seed=2)
+    ok, msg = bf16_ulp_ok(to_f64(D)[rows], ref_of(w, rows=rows))
+    assert ok, msg
+
+
+def test_workload3_full_size_sampled_rows():
+    w = wl.make(3)
+    D, _ = run_workload(w)
+    rows = sample_rows(w.M, 32, seed=3)
+    ok, msg = frob_ok(to_f64(D)[rows], ref_of(w, rows=rows))
+    assert ok, msg
+
+
+def test_workload4_full():
+    w = wl.make(4)
+    assert dg.dgemm_plan(0, w.M, w.N, w.K, "nk", "bf16")["swap_ab"] == 1
+    D, _ = run_workload(w)
+    ok, msg = bf16_ulp_ok(to_f64(D), ref_of(w))
+    assert ok, msg
+
+
+def test_workload5_full_size_sampled_rows():
+    w = wl.make(5)
+    q, s = run_workload(w)
+    rows = sample_rows(w.M, 24, seed=5)
+    ok, msg = requant_ok(q.numpy()[rows], s.numpy()[rows], ref_of(w, rows=rows))
+    assert ok, msg
+    # properties that hold on every row: each row's scale is positive and its
+    # largest code magnitude is the E4M3 maximum (448) unless the row is zero
+    qa = q.numpy() & 0x7F
+    assert np.all(s.numpy() > 0)
+    assert np.all(qa.max(axis=1) == 0x7E)

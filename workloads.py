@@ -76,7 +76,7 @@ def _bf16(x: np.ndarray) -> torch.Tensor:
 def quantize_e4m3_rows(X: np.ndarray):
     """E4M3 codes of X with one FP32 scale per row, s = amax_row / 448."""
     X32 = np.ascontiguousarray(X, dtype=np.float32)
-    amax = np.abs(X32).max(axis=1)
+    amax = np.abs(X32).max(axis=1, initial=0.0)
     s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
     s[s == 0] = 1.0
     q = torch.from_numpy(X32 / s[:, None]).to(torch.float8_e4m3fn)
