@@ -15,7 +15,7 @@ import ctypes
 from ._lib import (ACT, B_KN, B_NK, BF16, E4M3, F32, QUANT, DgemmError, Epilogue, Plan, load,
                    lib_path)
 
-__all__ = ["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_workspace_size", "dgemm_plan",
+__all__ = ["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_fp8_rowquant_noalloc", "dgemm_workspace_size", "dgemm_plan",
            "dgemm_status_string", "dgemm_query_device_status", "DgemmError", "load", "lib_path"]
 
 
@@ -111,6 +111,23 @@ def dgemm_fp8_scaled(Aq, Bq, a_scale, b_scale, D, *, b_layout="nk", k_group=0, C
                                    _stream(stream))
     _check(code, "dgemm_fp8_scaled")
     return D
+
+
+def dgemm_fp8_rowquant_noalloc(Aq, Bq, a_scale, b_scale, Dq, out_row_scale, *, b_layout="nk", C=None,
+                               alpha=1.0, beta=0.0, bias=None, act="none", stream=None):
+    """The requantising FP8 GEMM without a workspace, for callers that cannot
+    allocate device memory at call time: its scratch is a static 32 MiB device
+    array inside the library (M*N up to about 16.7 million; calls that overlap
+    on the GPU race on it). Dq [M,N] uint8 E4M3 codes, out_row_scale [M] fp32."""
+    M, N, K = _dims(Aq, Bq, b_layout)
+    epi = _epilogue(bias, act, "e4m3_row_amax", out_row_scale)
+    code = load().dgemm_fp8_rowquant_noalloc(_ptr(Aq), _ptr(Bq), B_KN if b_layout == "kn" else B_NK,
+                                             _ptr(a_scale), _ptr(b_scale), _ptr(C),
+                                             _dtype_code(C) if C is not None else F32, _ptr(Dq),
+                                             M, N, K, float(alpha), float(beta), ctypes.byref(epi),
+                                             _stream(stream))
+    _check(code, "dgemm_fp8_rowquant_noalloc")
+    return Dq
 
 
 def dgemm_workspace_size(is_fp8, M, N, K, b_layout="nk", *, out_quant="none", act="none") -> int:

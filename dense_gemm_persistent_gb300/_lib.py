@@ -45,7 +45,10 @@ SIGNATURES = {
                           ctypes.POINTER(Plan)]),
     "dgemm_status_string": (ctypes.c_char_p, [_i32]),
     "dgemm_query_device_status": (_i32, [_vp]),
+    "dgemm_fp8_rowquant_noalloc": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, _f32, _f32,
+                                          ctypes.POINTER(Epilogue), _vp]),
 }
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None

@@ -406,3 +406,45 @@ dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---- Allocation-free variant of the requantising FP8 GEMM -------------------
+// For callers that cannot allocate device memory when they run the GEMM (see
+// dgemm.h): the scratch the requantising kernel needs comes from this
+// file-scope device array instead of a caller workspace. In host code the name
+// g_noalloc_scratch is only a host-side stand-in, never a device address; the
+// device address is looked up once per device with cudaGetSymbolAddress and
+// passed to the kernel through the workspace argument of run().
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DGEMM_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocScratch {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void* ptr = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocScratch g_noalloc[kMaxDevices];
+
+}  // namespace
+
+extern "C" dgemm_status_t dgemm_fp8_rowquant_noalloc(const void* Aq, const void* Bq, dgemm_b_layout_t b_layout,
+                                                     const float* a_scale, const float* b_scale, const void* C,
+                                                     dgemm_dtype_t c_dtype, void* Dq, int64_t M, int64_t N,
+                                                     int64_t K, float alpha, float beta,
+                                                     const dgemm_epilogue_t* epi, dgemm_stream_t stream) {
+    if (!epi || epi->out_quant != DGEMM_QUANT_E4M3_ROW_AMAX) return DGEMM_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return DGEMM_ERR_INVALID_VALUE;
+    if (dgemm_workspace_size(1, M, N, K, b_layout, epi) > DGEMM_NOALLOC_SCRATCH_BYTES)
+        return DGEMM_ERR_WORKSPACE_TOO_SMALL;
+    DeviceState* dev = nullptr;
+    int devid = 0;
+    const dgemm_status_t st = device_state(&dev, &devid);  // also rejects devices other than sm_103
+    if (st != DGEMM_OK) return st;
+    NoAllocScratch& s = g_noalloc[devid];
+    std::call_once(s.once, [&s]() {
+        s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch);
+    });
+    if (s.err != cudaSuccess || s.ptr == nullptr) return DGEMM_ERR_CUDA;
+    return run(1, Aq, Bq, b_layout, a_scale, b_scale, C, c_dtype, Dq, DGEMM_E4M3, M, N, K, alpha, beta, epi, s.ptr,
+               DGEMM_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -178,6 +178,42 @@ const char* dgemm_status_string(dgemm_status_t status);
  * DGEMM_ERR_CUDA if the stream itself reports an error. */
 dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream);
 
+/* ---- Allocation-free variant (no counterpart in the paper) ----------------
+ *
+ * Some callers cannot allocate device memory at the point where they run a
+ * GEMM: code inside a custom memory pool or allocator callback, a real-time
+ * path that must not block on cudaMalloc's device-wide synchronisation, or an
+ * embedded runtime whose memory is carved out once at start-up. The per-row
+ * E4M3 requantisation epilogue needs scratch memory (a barrier counter, the
+ * row maxima and a BF16 copy of the pre-quantisation tile values), which
+ * dgemm_fp8_scaled takes from a caller-provided workspace. This entry point
+ * takes it instead from one statically sized device array inside the library,
+ * so the caller passes only inputs and outputs and nothing is allocated.
+ *
+ *   - The array is DGEMM_NOALLOC_SCRATCH_BYTES (32 MiB) per device and is held
+ *     by every GPU that loads the library until the process exits.
+ *   - A call needs dgemm_workspace_size(1, M, N, K, b_layout, epi) bytes of it
+ *     (about 2*M*N + 4*M + 512); larger problems return
+ *     DGEMM_ERR_WORKSPACE_TOO_SMALL before anything is launched. M*N up to
+ *     about 16.7 million elements fits (e.g. 2048 x 8192).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     CUDA stream capture begins.
+ *   - All calls share the one array, which keeps the last call's contents; the
+ *     call clears the parts that must start at zero. Calls whose kernels
+ *     overlap on the GPU (different streams, or different host threads) race
+ *     on the array and give wrong results: serialise them.
+ *   - Arguments and results are those of dgemm_fp8_scaled with k_group = 0,
+ *     d_dtype E4M3 and epi->out_quant == DGEMM_QUANT_E4M3_ROW_AMAX (required,
+ *     with epi->out_row_scale). */
+#define DGEMM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+dgemm_status_t dgemm_fp8_rowquant_noalloc(const void* Aq, const void* Bq, dgemm_b_layout_t b_layout,
+                                          const float* a_scale, const float* b_scale,
+                                          const void* C, dgemm_dtype_t c_dtype, void* Dq,
+                                          int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                          const dgemm_epilogue_t* epi, dgemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

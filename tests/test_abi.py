@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_workspace_size", "dgemm_plan",
-                            "dgemm_status_string", "dgemm_query_device_status"])
+                            "dgemm_status_string", "dgemm_query_device_status",
+                            "dgemm_fp8_rowquant_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(lib):
