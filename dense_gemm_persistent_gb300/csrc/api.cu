@@ -45,11 +45,13 @@ void collect_kernels() {
     for (int i = 0; i < n2 && g_nk < 64; ++i) g_kernels[g_nk++] = &t2[i];
 }
 
-int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode) {
+int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode, int pair) {
     std::call_once(g_kernels_once, collect_kernels);
     for (int i = 0; i < g_nk; ++i) {
         const dg::KernelInfo* k = g_kernels[i];
-        if (k->bn == bn && k->fp8 == fp8 && k->a_mn == a_mn && k->b_mn == b_mn && k->mode == mode) return i;
+        if (k->bn == bn && k->fp8 == fp8 && k->a_mn == a_mn && k->b_mn == b_mn && k->mode == mode &&
+            k->pair == pair)
+            return i;
     }
     return -1;
 }
@@ -73,7 +75,7 @@ struct Plan {
 // Validates the sizes, enums and epilogue; picks the kernel variant and grid.
 // Pure host logic: needs no GPU.
 dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t bl, dgemm_dtype_t d_dtype,
-                         const dgemm_epilogue_t* epi, int num_sms, Plan* out) {
+                         const dgemm_epilogue_t* epi, int num_sms, int max_pairs, Plan* out) {
     if (M < 0 || N < 0 || K < 0 || num_sms <= 0) return DGEMM_ERR_INVALID_VALUE;
     if (bl != DGEMM_B_KN && bl != DGEMM_B_NK) return DGEMM_ERR_INVALID_VALUE;
     if (d_dtype != DGEMM_F32 && d_dtype != DGEMM_BF16 && d_dtype != DGEMM_E4M3) return DGEMM_ERR_INVALID_VALUE;
@@ -93,7 +95,10 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     Plan p{};
     p.bk = static_cast<int>(128 / esz);
     const bool swap = (oq == DGEMM_QUANT_NONE) && M <= 64;
+    const char* pair_env = std::getenv("DGEMM_CTA_PAIR");  // "0" disables, "1" forces CTA pairs (tests, sweeps)
+    const bool pairs_ok = max_pairs > 0 && !(pair_env && pair_env[0] == '0');
     int bn;
+    int pair = 0;
     if (swap) {
         p.mode = dg::MODE_SWAP;
         p.Mm = N;
@@ -107,24 +112,29 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         p.Nm = N;
         p.a_mn = 0;
         p.b_mn = (bl == DGEMM_B_KN);
-        if (p.mode == dg::MODE_ROWQ) {
-            bn = 256;
-        } else {
-            // Fewest waves of the widest tile: cost ~ waves x tile width, with a
-            // penalty for narrow tiles (more shared-memory traffic per FLOP).
-            const int cands[3] = {256, 128, 64};
-            const double penalty[3] = {1.0, 1.15, 1.6};
-            double best = 1e300;
-            bn = 256;
-            for (int i = 0; i < 3; ++i) {
-                if (fp8 && p.b_mn && cands[i] < 128) continue;
-                const int64_t tiles = ((M + 127) / 128) * ((N + cands[i] - 1) / cands[i]);
-                const int64_t waves = (tiles + num_sms - 1) / num_sms;
-                const double cost = static_cast<double>(waves) * cands[i] * penalty[i];
-                if (cost < best) {
-                    best = cost;
-                    bn = cands[i];
-                }
+        // Wave-cost model: cost = waves x (tile area per SM) x inefficiency.
+        // A CTA pair's 256 x 256 tile is the most efficient per FLOP (least L2
+        // traffic per SM, deepest pipeline); narrower single-CTA tiles need
+        // more operand bandwidth per FLOP but quantise into waves more finely.
+        struct Cand { int bn, pair; double penalty; };
+        // Penalties from measurement: 128 x 128 tiles ran at 0.55x the per-SM
+        // rate of 128 x 256 tiles (8192^3 FP8), being shared-memory-bound.
+        const Cand cands[4] = {{256, 1, 1.0}, {256, 0, 1.15}, {128, 0, 2.1}, {64, 0, 3.0}};
+        double best = 1e300;
+        bn = 256;
+        for (const Cand& c : cands) {
+            if (p.mode == dg::MODE_ROWQ && c.bn != 256) continue;
+            if (c.pair && (!pairs_ok || M <= 128)) continue;
+            if (fp8 && p.b_mn && c.bn < 128) continue;
+            const int64_t tm = c.pair ? 256 : 128;
+            const int64_t units = c.pair ? max_pairs : num_sms;
+            const int64_t tiles = ((M + tm - 1) / tm) * ((N + c.bn - 1) / c.bn);
+            const int64_t waves = (tiles + units - 1) / units;
+            const double cost = static_cast<double>(waves) * (128.0 * c.bn) * c.penalty;
+            if (cost < best) {
+                best = cost;
+                bn = c.bn;
+                pair = c.pair;
             }
         }
     }
@@ -132,20 +142,29 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     // exercise every variant in tests and for tuning sweeps).
     if (const char* f = std::getenv("DGEMM_TILE_N")) {
         const int v = std::atoi(f);
-        if (find_kernel(v, fp8, p.a_mn, p.b_mn, p.mode) >= 0) bn = v;
+        if (v != bn && find_kernel(v, fp8, p.a_mn, p.b_mn, p.mode, 0) >= 0) {
+            bn = v;
+            pair = 0;
+        }
     }
-    p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode);
+    // DGEMM_CTA_PAIR=1 forces the CTA-pair variant when one exists for this tile.
+    if (pair_env && pair_env[0] == '1' && !swap && M > 128 && max_pairs > 0 &&
+        find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, 1) >= 0)
+        pair = 1;
+    p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair);
     if (p.kernel < 0) return DGEMM_ERR_NOT_SUPPORTED;
     const dg::KernelInfo* k = g_kernels[p.kernel];
-    const int64_t tiles_m = (p.Mm + 127) / 128, tiles_n = (p.Nm + bn - 1) / bn;
+    const int tile_m = pair ? 256 : 128;
+    const int64_t tiles_m = (p.Mm + tile_m - 1) / tile_m, tiles_n = (p.Nm + bn - 1) / bn;
     if (tiles_m * tiles_n > INT32_MAX) return DGEMM_ERR_NOT_SUPPORTED;
     p.pub.swap_ab = swap ? 1 : 0;
-    p.pub.tile_m = 128;
+    p.pub.tile_m = tile_m;
     p.pub.tile_n = bn;
-    p.pub.cta_group = 1;
+    p.pub.cta_group = pair ? 2 : 1;
     p.pub.stages = k->stages;
     p.pub.num_tiles = static_cast<int>(tiles_m * tiles_n);
-    p.pub.grid = static_cast<int>(p.pub.num_tiles < num_sms ? p.pub.num_tiles : num_sms);
+    const int units = pair ? max_pairs : num_sms;
+    p.pub.grid = (pair ? 2 : 1) * static_cast<int>(p.pub.num_tiles < units ? p.pub.num_tiles : units);
     p.pub.cooperative = p.mode == dg::MODE_ROWQ ? 1 : 0;
     p.pub.raster_group = static_cast<int>(tiles_m < 8 ? (tiles_m > 0 ? tiles_m : 1) : 8);
     p.pub.smem_bytes = static_cast<size_t>(k->smem_bytes);
@@ -158,7 +177,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     int groups = 1;
     p.acc_stride = bn;
     if (p.mode == dg::MODE_SWAP) {
-        const bool one_tile = p.pub.num_tiles <= p.pub.grid;
+        const bool one_tile = p.pub.num_tiles <= p.pub.grid;  // (no pairs in this mode)
         const int max_groups = (one_tile ? 512 : 256) / bn;
         groups = static_cast<int>(k_blocks < max_groups ? (k_blocks > 0 ? k_blocks : 1) : max_groups);
         p.acc_stride = groups * bn;
@@ -215,6 +234,50 @@ dgemm_status_t device_state(DeviceState** out, int* dev_out) {
     return DGEMM_OK;
 }
 
+// Dynamic shared memory opt-in, once per kernel variant and device.
+cudaError_t configure_kernel(int kernel, int devid) {
+    std::atomic<unsigned char>& flag = g_attr_set[kernel][devid];
+    if (flag.load(std::memory_order_acquire)) return cudaSuccess;
+    const dg::KernelInfo* k = g_kernels[kernel];
+    const cudaError_t e = cudaFuncSetAttribute(k->func, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes);
+    if (e == cudaSuccess) flag.store(1, std::memory_order_release);
+    return e;
+}
+
+// How many CTA pairs (2-CTA clusters) of the pair kernels fit on the device at
+// once, measured once per device with the occupancy API (0: no pairs).
+int g_max_pairs[kMaxDevices][2];
+std::once_flag g_pairs_once[kMaxDevices][2];
+
+int max_pairs(DeviceState* dev, int devid, int fp8) {
+    std::call_once(g_pairs_once[devid][fp8], [&]() {
+        int best = 0;
+        std::call_once(g_kernels_once, collect_kernels);
+        for (int i = 0; i < g_nk; ++i) {
+            const dg::KernelInfo* k = g_kernels[i];
+            if (!k->pair || k->fp8 != fp8 || k->mode != dg::MODE_TILE) continue;
+            if (configure_kernel(i, devid) != cudaSuccess) continue;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * static_cast<unsigned>(dev->num_sms));
+            cfg.blockDim = dim3(static_cast<unsigned>(k->threads));
+            cfg.dynamicSmemBytes = static_cast<size_t>(k->smem_bytes);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k->func, &cfg) == cudaSuccess) best = n;
+            else (void)cudaGetLastError();
+            break;
+        }
+        g_max_pairs[devid][fp8] = best > dev->num_sms / 2 ? dev->num_sms / 2 : best;
+    });
+    return g_max_pairs[devid][fp8];
+}
+
 CUtensorMapDataType tm_type(dgemm_dtype_t t) {
     return t == DGEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                           : t == DGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -226,7 +289,7 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
                    size_t ws_bytes, cudaStream_t stream) {
     // ---- arguments that need no device
     Plan plan;
-    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 1, &plan);
+    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, &plan);
     if (st != DGEMM_OK) return st;
     if (M == 0 || N == 0) return DGEMM_OK;
     if (!D || (K > 0 && (!A || !B))) return DGEMM_ERR_INVALID_VALUE;
@@ -252,16 +315,10 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     int devid = 0;
     st = device_state(&dev, &devid);
     if (st != DGEMM_OK) return st;
-    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, &plan);
+    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, max_pairs(dev, devid, fp8), &plan);
     if (st != DGEMM_OK) return st;
     const dg::KernelInfo* k = g_kernels[plan.kernel];
-    std::atomic<unsigned char>& attr = g_attr_set[plan.kernel][devid];
-    if (!attr.load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(k->func, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes) !=
-            cudaSuccess)
-            return DGEMM_ERR_CUDA;
-        attr.store(1, std::memory_order_release);
-    }
+    if (configure_kernel(plan.kernel, devid) != cudaSuccess) return DGEMM_ERR_CUDA;
 
     // ---- tensor maps
     const dgemm_dtype_t in_t = fp8 ? DGEMM_E4M3 : DGEMM_BF16;
@@ -284,7 +341,8 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
         if (plan.b_mn)  // Y = B stored K x N: MN-major
             ok = encode_2d(&tmB, tm_type(in_t), Y, N, K, N * esz, mn_atom, plan.bk);
         else            // Y stored Nm x K: K-major
-            ok = encode_2d(&tmB, tm_type(in_t), Y, K, plan.Nm, K * esz, plan.bk, plan.pub.tile_n);
+            ok = encode_2d(&tmB, tm_type(in_t), Y, K, plan.Nm, K * esz, plan.bk,
+                           static_cast<uint32_t>(plan.pub.tile_n / plan.pub.cta_group));
         if (!ok) return DGEMM_ERR_CUDA;
     }
     uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -303,7 +361,7 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.M = static_cast<int>(plan.Mm);
     p.N = static_cast<int>(plan.Nm);
     p.K = static_cast<int>(K);
-    p.tiles_m = static_cast<int>((plan.Mm + 127) / 128);
+    p.tiles_m = static_cast<int>((plan.Mm + plan.pub.tile_m - 1) / plan.pub.tile_m);
     p.tiles_n = static_cast<int>((plan.Nm + plan.pub.tile_n - 1) / plan.pub.tile_n);
     p.num_tiles = plan.pub.num_tiles;
     p.k_blocks = static_cast<int>((K + plan.bk - 1) / plan.bk);
@@ -361,9 +419,9 @@ size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b
                             const dgemm_epilogue_t* epi) {
     Plan plan;
     const dgemm_dtype_t d = (epi && epi->out_quant) ? DGEMM_E4M3 : DGEMM_BF16;
-    if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d, epi, 1, &plan) != DGEMM_OK) {
+    if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d, epi, 2, 1, &plan) != DGEMM_OK) {
         // the output dtype is not an argument here: retry with FP32 output
-        if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, DGEMM_F32, epi, 1, &plan) != DGEMM_OK) return 0;
+        if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, DGEMM_F32, epi, 2, 1, &plan) != DGEMM_OK) return 0;
     }
     return plan.pub.workspace_bytes;
 }
@@ -372,7 +430,7 @@ dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_l
                           dgemm_dtype_t d_dtype, const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan) {
     if (!plan) return DGEMM_ERR_INVALID_VALUE;
     Plan p;
-    const dgemm_status_t st = make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, &p);
+    const dgemm_status_t st = make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, num_sms / 2, &p);
     if (st == DGEMM_OK) *plan = p.pub;
     return st;
 }

@@ -1,15 +1,20 @@
 // gemm_kernel.cuh -- the persistent, warp-specialised tcgen05 GEMM kernel.
 //
 // One CTA per SM loops over output tiles in a swizzled (grouped) raster order.
-// Its six warps split the work:
+// With PAIR, two CTAs of a cluster (two SMs) share one 256-row tile: each loads
+// its own 128 rows of A and half of the B tile, the even CTA issues
+// tcgen05.mma.cta_group::2 over both, and each CTA's Tensor Memory holds its
+// 128 rows of the accumulator. Per SM this halves the B traffic from L2 and
+// leaves room for more pipeline stages. Each CTA's six warps split the work:
 //   warp 0     TMA producer: streams 128-byte-wide K slices of A and B into an
 //              S-stage shared-memory ring (128B swizzle), one mbarrier pair
 //              (full / empty) per stage.
 //   warp 1     MMA issuer: one thread issues tcgen05.mma for each K slice into
 //              one of two FP32 accumulators in Tensor Memory and commits the
 //              stage back to the producer; owns the TMEM allocation.
-//   warps 2-5  epilogue: read the finished accumulator with tcgen05.ld (each
-//              warp its 32-lane quarter, one output row per thread), apply
+//   warps 2-9  epilogue (2-5 for the small-M form): read the finished
+//              accumulator with tcgen05.ld (each warp a 32-lane quarter and half
+//              of the columns, one output row per thread), apply
 //              scales, alpha/beta, bias and activation in FP32, convert once,
 //              and write through swizzled shared memory with TMA stores (or,
 //              for the transposed small-M form, with coalesced direct stores),
@@ -74,9 +79,12 @@ struct Params {
     unsigned* status;        // sticky device error word
 };
 
-template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_>
+template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false>
 struct Cfg {
-    static constexpr int BM = 128;
+    static constexpr int BM = 128;                // accumulator rows per CTA
+    static constexpr bool PAIR = PAIR_;
+    static constexpr int CTAS = PAIR ? 2 : 1;     // CTAs sharing one tile
+    static constexpr int TILE_M = BM * CTAS;      // output rows per tile
     static constexpr int BN = BN_;
     static constexpr bool FP8 = FP8_;
     static constexpr bool A_MN = A_MN_;
@@ -87,9 +95,15 @@ struct Cfg {
     static constexpr int UMMA_K = 32 / ESZ;       // K elements per MMA (32 bytes)
     static constexpr int MN_ATOM = 128 / ESZ;     // MN elements per 128-byte row (MN-major)
     static constexpr int A_BYTES = BM * 128;
-    static constexpr int B_BYTES = BN * 128;
+    static constexpr int BN_CTA = BN / CTAS;      // B rows (N) each CTA loads
+    static constexpr int B_BYTES = BN_CTA * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGING_BYTES = (MODE == MODE_SWAP) ? 0 : 4 * 2 * 4096;
+    // Epilogue warps: two per TMEM lane quarter (each takes half of the tile's
+    // columns) for tiles of 128 columns or more, whose FP8 mainloop per tile can
+    // be shorter than one warp-quarter's epilogue; one per quarter otherwise.
+    static constexpr int EPI_WARPS = (MODE == MODE_SWAP || BN < 128) ? 4 : 8;
+    static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);   // columns per epilogue warp
+    static constexpr int STAGING_BYTES = (MODE == MODE_SWAP) ? 0 : EPI_WARPS * 4096;  // one 4 KB box each
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_LIMIT = 232448;  // 227 KB opt-in maximum per CTA
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
@@ -98,12 +112,13 @@ struct Cfg {
     static constexpr int TMEM_COLS = (MODE == MODE_SWAP) ? 512
                                    : (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
-    static constexpr uint32_t IDESC = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, BM, BN);
-    static constexpr int NUM_THREADS = 192;
+    static constexpr uint32_t IDESC = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, TILE_M, BN);
+    static constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
-    static_assert(!B_MN || BN % MN_ATOM == 0, "MN-major B needs whole 128-byte atoms");
-    static_assert(MODE == MODE_SWAP || BN % 64 == 0, "tile epilogue works in 64-column boxes");
+    static_assert(!B_MN || BN_CTA % MN_ATOM == 0, "MN-major B needs whole 128-byte atoms");
+    static_assert(!PAIR || (MODE != MODE_SWAP && !A_MN && BN == 256), "CTA pairs: 256 x 256 tiles");
+    static_assert(MODE == MODE_SWAP || EPI_COLS % 64 == 0, "tile epilogue works in 64-column boxes");
     static_assert(STAGES >= 2, "pipeline depth");
     static_assert(BN < 32 || BN % 32 == 0, "epilogue reads 32-column units");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
@@ -122,12 +137,26 @@ __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int
     nb = r / rows;
 }
 
-__device__ __forceinline__ float activation(float y, int act) {
+// Activations applied to 32 values at once; the switch is taken once per
+// 32-column unit so the per-element code is straight-line and interleaves.
+// SiLU uses the fast exponential and division: their relative error (a few
+// units of 2^-22) is far below the BF16 / E4M3 output rounding.
+__device__ __forceinline__ void activation32(float (&v)[32], int act) {
     switch (act) {
-        case 1: return fmaxf(y, 0.0f);
-        case 2: return 0.5f * y * (1.0f + erff(y * 0.70710678118654752f));
-        case 3: return y / (1.0f + expf(-y));
-        default: return y;
+        case 1:
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.0f);
+            break;
+        case 2:
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.5f * v[j] * (1.0f + erff(v[j] * 0.70710678118654752f));
+            break;
+        case 3:
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __fdividef(v[j], 1.0f + __expf(-v[j]));
+            break;
+        default:
+            break;
     }
 }
 
@@ -221,10 +250,7 @@ __device__ __forceinline__ void epilogue_math(float (&v)[32], const Params& p, i
                 }
         }
     }
-    if (p.act) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = activation(v[j], p.act);
-    }
+    activation32(v, p.act);
 }
 
 template <class CF>
@@ -247,6 +273,11 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pairs: rank 0 is the leader that issues the MMAs; a tile is shared by
+    // the pair, so the tile loop runs over pairs.
+    const uint32_t rank = CF::PAIR ? cluster_ctarank() : 0u;
+    const int unit0 = static_cast<int>(blockIdx.x) / CF::CTAS;
+    const int units = static_cast<int>(gridDim.x) / CF::CTAS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -255,7 +286,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], CF::EPI_WARPS * CF::CTAS);  // every epilogue warp of the pair
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -268,12 +299,25 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         }
         if (CF::MODE != MODE_SWAP) tma_prefetch_desc(&tmD);
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, CF::TMEM_COLS);
-        tmem_relinquish();
+    if constexpr (CF::PAIR) {
+        // the peer's barriers must be initialised before any cross-CTA signal
+        __syncthreads();
+        cluster_sync();
+        if (warp == 1) {
+            tmem_alloc_pair(tmem_slot, CF::TMEM_COLS);
+            tmem_relinquish_pair();
+        }
+        tc_fence_before();
+        __syncthreads();
+        cluster_sync();
+    } else {
+        if (warp == 1) {
+            tmem_alloc(tmem_slot, CF::TMEM_COLS);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
     }
-    tc_fence_before();
-    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -284,9 +328,11 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = unit0; ok && t < p.num_tiles; t += units) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
+                const int row0 = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM;   // this CTA's A rows
+                const int col0 = nb * CF::BN + static_cast<int>(rank) * CF::BN_CTA;  // this CTA's B rows
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                         ok = false;
@@ -294,23 +340,37 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     }
                     uint8_t* sa = stages + stage * CF::STAGE_BYTES;
                     uint8_t* sb = sa + CF::A_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
                     const int k0 = kb * CF::BK;
-                    if constexpr (CF::A_MN) {
+                    if constexpr (CF::PAIR) {
+                        // both CTAs' copies complete on the leader's full barrier
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], CF::CTAS * CF::STAGE_BYTES);
+                        const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+                        tma_load_2d_pair(sa, &tmA, fb, k0, row0, pol);
+                        if constexpr (CF::B_MN) {
 #pragma unroll
-                        for (int i = 0; i < CF::BM / CF::MN_ATOM; ++i)
-                            tma_load_2d(sa + i * CF::BK * 128, &tmA, &full[stage], mb * CF::BM + i * CF::MN_ATOM,
-                                        k0, pol);
+                            for (int i = 0; i < CF::BN_CTA / CF::MN_ATOM; ++i)
+                                tma_load_2d_pair(sb + i * CF::BK * 128, &tmB, fb, col0 + i * CF::MN_ATOM, k0, pol);
+                        } else {
+                            tma_load_2d_pair(sb, &tmB, fb, k0, col0, pol);
+                        }
                     } else {
-                        tma_load_2d(sa, &tmA, &full[stage], k0, mb * CF::BM, pol);
-                    }
-                    if constexpr (CF::B_MN) {
+                        mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
+                        if constexpr (CF::A_MN) {
 #pragma unroll
-                        for (int i = 0; i < CF::BN / CF::MN_ATOM; ++i)
-                            tma_load_2d(sb + i * CF::BK * 128, &tmB, &full[stage], nb * CF::BN + i * CF::MN_ATOM,
-                                        k0, pol);
-                    } else {
-                        tma_load_2d(sb, &tmB, &full[stage], k0, nb * CF::BN, pol);
+                            for (int i = 0; i < CF::BM / CF::MN_ATOM; ++i)
+                                tma_load_2d(sa + i * CF::BK * 128, &tmA, &full[stage], row0 + i * CF::MN_ATOM, k0,
+                                            pol);
+                        } else {
+                            tma_load_2d(sa, &tmA, &full[stage], k0, row0, pol);
+                        }
+                        if constexpr (CF::B_MN) {
+#pragma unroll
+                            for (int i = 0; i < CF::BN_CTA / CF::MN_ATOM; ++i)
+                                tma_load_2d(sb + i * CF::BK * 128, &tmB, &full[stage], col0 + i * CF::MN_ATOM, k0,
+                                            pol);
+                        } else {
+                            tma_load_2d(sb, &tmB, &full[stage], k0, col0, pol);
+                        }
                     }
                     ++issued;
                     if (++stage == S) {
@@ -321,21 +381,36 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             }
             if (!ok) raise_error(p, ERR_TIMEOUT_PRODUCER, abort_flag);
             // Drain: every copy this thread issued must have landed before the
-            // CTA can exit (normally these waits return at once).
+            // CTA can exit (normally these waits return at once). The peer of a
+            // pair signals the leader's full barriers, so it waits instead for
+            // the MMA's release of its last use of each stage.
             for (int s = 0; s < S; ++s) {
                 const int64_t cnt = issued > s ? (issued - s + S - 1) / S : 0;
-                if (cnt > 0 && !mbar_wait(&full[s], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
+                uint64_t* bar = (CF::PAIR && rank != 0) ? &empty[s] : &full[s];
+                if (cnt > 0 && !mbar_wait(bar, static_cast<uint32_t>((cnt - 1) & 1), nullptr))
                     raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
+            // The tensor core's instruction queue is shallow (issue time equals
+            // execution time), so this loop must spend almost nothing between
+            // MMAs: descriptors are built once and advanced by additions, and
+            // K-group boundaries are tracked incrementally (a division per K
+            // slice here measurably starves the tensor pipe).
+            const uint32_t s0 = smem_u32(stages);
+            const uint64_t a_desc0 = smem_desc_sw128(s0, CF::A_MN ? CF::BK * 128 : 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(s0 + CF::A_BYTES, CF::B_MN ? CF::BK * 128 : 16, 1024);
+            constexpr uint32_t A_KSTEP = (CF::A_MN ? CF::UMMA_K * 128 : 32) >> 4;
+            constexpr uint32_t B_KSTEP = (CF::B_MN ? CF::UMMA_K * 128 : 32) >> 4;
+            constexpr uint32_t STAGE_STEP = CF::STAGE_BYTES >> 4;
+            const int kblocks = p.k_blocks, ngroups = p.acc_groups;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int local = 0;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+            for (int t = unit0; ok && t < p.num_tiles; t += units, ++local) {
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, abort_flag)) {
@@ -344,55 +419,76 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t acc_base = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
-                int group = -1;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                // group g covers K slices [ceil(g*KB/G), ceil((g+1)*KB/G))
+                int group = 0;
+                int next_group_start = ngroups > 1 ? (kblocks + ngroups - 1) / ngroups : kblocks;
+                uint32_t d_tmem = acc_base;
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // contiguous, even split of the K slices over the groups
-                    const int g = static_cast<int>((static_cast<int64_t>(kb) * p.acc_groups) / p.k_blocks);
-                    const bool first_in_group = (g != group);
-                    group = g;
-                    const uint32_t d_tmem = acc_base + static_cast<uint32_t>(g * CF::BN);
-                    const uint32_t a0 = smem_u32(stages + stage * CF::STAGE_BYTES);
-                    const uint32_t b0 = a0 + CF::A_BYTES;
+                    bool first_in_group = (kb == 0);
+                    if (kb == next_group_start) {
+                        ++group;
+                        first_in_group = true;
+                        next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
+                        d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
+                    }
+                    const uint64_t ad = a_desc0 + stage * STAGE_STEP;
+                    const uint64_t bd = b_desc0 + stage * STAGE_STEP;
 #pragma unroll
                     for (int k = 0; k < CF::BK / CF::UMMA_K; ++k) {
-                        const uint64_t ad = CF::A_MN ? smem_desc_sw128(a0 + k * CF::UMMA_K * 128, CF::BK * 128, 1024)
-                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
-                        const uint64_t bd = CF::B_MN ? smem_desc_sw128(b0 + k * CF::UMMA_K * 128, CF::BK * 128, 1024)
-                                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
                         const uint32_t acc = (!first_in_group || k > 0) ? 1u : 0u;
-                        if constexpr (CF::FP8)
-                            mma_f8(d_tmem, ad, bd, CF::IDESC, acc);
-                        else
-                            mma_bf16(d_tmem, ad, bd, CF::IDESC, acc);
+                        if constexpr (CF::PAIR) {
+                            if constexpr (CF::FP8)
+                                mma_f8_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                            else
+                                mma_bf16_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                        } else {
+                            if constexpr (CF::FP8)
+                                mma_f8(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                            else
+                                mma_bf16(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                        }
                     }
-                    mma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
+                    // the stage is free (in both CTAs of a pair) once these MMAs have read it
+                    if constexpr (CF::PAIR)
+                        mma_commit_pair(&empty[stage], 3);
+                    else
+                        mma_commit(&empty[stage]);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                mma_commit(&acc_full[buf]);     // accumulator ready for the epilogue
+                // accumulator ready for the epilogue (of both CTAs of a pair)
+                if constexpr (CF::PAIR)
+                    mma_commit_pair(&acc_full[buf], 3);
+                else
+                    mma_commit(&acc_full[buf]);
             }
             if (!ok) raise_error(p, ERR_TIMEOUT_MMA, abort_flag);
             // Drain: all issued MMAs complete before TMEM is released.
-            mma_commit(drain);
+            if constexpr (CF::PAIR)
+                mma_commit_pair(drain, 1);
+            else
+                mma_commit(drain);
             if (!mbar_wait(drain, 0, nullptr)) raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                        // TMEM lane quarter this warp may access
-        uint8_t* stg = staging + (warp - 2) * 8192;    // two 4 KB staging boxes per warp
+        const int ew = warp - 2;                       // epilogue warp index
+        const int cbase = (ew >> 2) * CF::EPI_COLS;    // first tile column this warp handles
+        uint8_t* stg = staging + ew * 4096;            // this warp's 4 KB staging box
         int stores = 0;
         int local = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+        for (int t = unit0; t < p.num_tiles; t += units, ++local) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
             const int buf = local & 1;
@@ -402,7 +498,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int row = mb * CF::BM + q * 32 + lane;
+            const int row_base = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM + q * 32;
+            const int row = row_base + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * p.acc_stride);
             const int groups = p.k_blocks > 0 ? p.acc_groups : 1;
@@ -411,10 +508,12 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             if constexpr (CF::MODE == MODE_SWAP)
                 if (p.bias && row < p.M) bias_row = p.bias[row];
             float rowmax = 0.0f;
-            constexpr int UNIT = CF::BN < 32 ? CF::BN : 32;
+            constexpr int UNIT = CF::EPI_COLS < 32 ? CF::EPI_COLS : 32;
+            constexpr int NUNITS = CF::EPI_COLS / UNIT;
 #pragma unroll 1
-            for (int u = 0; u < CF::BN / UNIT; ++u) {
-                const int col0 = nb * CF::BN + u * UNIT;
+            for (int u = 0; u < NUNITS; ++u) {
+                const int tcol = cbase + u * UNIT;            // column within the tile
+                const int col0 = nb * CF::BN + tcol;
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
@@ -422,7 +521,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 // K-group promotion is on), added in group order.
 #pragma unroll 1
                 for (int g = 0; g < groups; ++g) {
-                    const uint32_t ta = taddr + static_cast<uint32_t>(g * CF::BN + u * UNIT);
+                    const uint32_t ta = taddr + static_cast<uint32_t>(g * CF::BN + tcol);
                     if constexpr (UNIT == 32) {
                         uint32_t r[32];
                         tmem_ld32(ta, r);
@@ -441,11 +540,16 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 }
-                if (u == CF::BN / UNIT - 1) {
+                if (u == NUNITS - 1) {
                     // Last read of this accumulator: hand it back to the MMA warp.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                    if (lane == 0) {
+                        if (CF::PAIR && rank != 0)
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
+                        else
+                            mbar_arrive(&acc_empty[buf]);
+                    }
                 }
                 epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row);
 
@@ -475,9 +579,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     // 32 columns are a whole 128-byte box row for FP32 output and
                     // half of one for BF16; a box is 32 rows (one per lane).
                     const int half = f32_out ? 0 : (u & 1);
-                    uint8_t* box = stg + (stores & 1) * 4096;
+                    uint8_t* box = stg;
                     if (half == 0) {
-                        if (stores >= 2 && lane == 0) bulk_wait_read<1>();
+                        // the previous box's TMA store must have read the staging buffer
+                        if (stores >= 1 && lane == 0) bulk_wait_read<0>();
                         __syncwarp();
                     }
                     uint8_t* rowp = box + lane * 128;
@@ -504,7 +609,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) {
                             const int x = f32_out ? col0 : col0 - 32;
-                            tma_store_2d(&tmD, box, x, mb * CF::BM + q * 32);
+                            tma_store_2d(&tmD, box, x, row_base);
                             bulk_commit();
                         }
                         ++stores;
@@ -528,9 +633,18 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, CF::TMEM_COLS);
+    if constexpr (CF::PAIR) {
+        // neither CTA may leave while the pair's MMAs can still read its shared memory
+        cluster_sync();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc_pair(tmem_base, CF::TMEM_COLS);
+        }
+    } else {
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, CF::TMEM_COLS);
+        }
     }
 
     if constexpr (CF::MODE == MODE_ROWQ) {
@@ -555,47 +669,48 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         if (*abort_flag) return;
         // ---------------------------------------------------------- requantise
         // s[m] = amax[m] / 448; q = RN_E4M3(y * (1 / s[m])), saturating.
-        // Each thread keeps RQ_UNROLL independent 32-byte loads in flight so the
-        // pass runs at memory bandwidth rather than at one load's latency.
+        // One warp per output row at a time: lane l converts the 16-element
+        // groups l, l + 32, ... of the row, RQ_UNROLL of them with their loads in
+        // flight together, so the pass runs at memory bandwidth. The row scale
+        // s[m] = amax[m] / 448 is written once per row.
         constexpr int RQ_UNROLL = 8;
-        const int64_t groups_per_row = p.N / 16;
-        const int64_t total = static_cast<int64_t>(p.M) * groups_per_row;
-        const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-        for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
-             base += stride * RQ_UNROLL) {
-            uint4 y0[RQ_UNROLL], y1[RQ_UNROLL];
-            unsigned am[RQ_UNROLL];
+        const int warps_per_cta = static_cast<int>(blockDim.x) >> 5;
+        const int warps_total = static_cast<int>(gridDim.x) * warps_per_cta;
+        const int groups_per_row = p.N / 16;
+        for (int m = static_cast<int>(blockIdx.x) * warps_per_cta + warp; m < p.M; m += warps_total) {
+            const float amax = __uint_as_float(__ldcg(p.amax + m));
+            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
+            if (lane == 0) p.out_row_scale[m] = s;
+            const uint4* src = reinterpret_cast<const uint4*>(p.stash + static_cast<int64_t>(m) * p.N);
+            uint4* dst = reinterpret_cast<uint4*>(p.q_out + static_cast<int64_t>(m) * p.N);
+            for (int g0 = lane; g0 < groups_per_row; g0 += 32 * RQ_UNROLL) {
+                uint4 y0[RQ_UNROLL], y1[RQ_UNROLL];
 #pragma unroll
-            for (int u = 0; u < RQ_UNROLL; ++u) {
-                const int64_t g = base + u * stride;
-                if (g < total) {
-                    const int64_t m = g / groups_per_row;
-                    const int64_t n0 = (g - m * groups_per_row) * 16;
-                    const uint4* src = reinterpret_cast<const uint4*>(p.stash + m * p.N + n0);
-                    y0[u] = __ldcg(src);
-                    y1[u] = __ldcg(src + 1);
-                    am[u] = __ldcg(p.amax + m);
+                for (int u = 0; u < RQ_UNROLL; ++u) {
+                    const int g = g0 + 32 * u;
+                    if (g < groups_per_row) {
+                        y0[u] = __ldcg(src + 2 * g);
+                        y1[u] = __ldcg(src + 2 * g + 1);
+                    }
                 }
-            }
 #pragma unroll
-            for (int u = 0; u < RQ_UNROLL; ++u) {
-                const int64_t g = base + u * stride;
-                if (g >= total) break;
-                const int64_t m = g / groups_per_row;
-                const int64_t n0 = (g - m * groups_per_row) * 16;
-                const float amax = __uint_as_float(am[u]);
-                const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
-                const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
-                const uint32_t w[8] = {y0[u].x, y0[u].y, y0[u].z, y0[u].w, y1[u].x, y1[u].y, y1[u].z, y1[u].w};
-                uint32_t o[4];
+                for (int u = 0; u < RQ_UNROLL; ++u) {
+                    const int g = g0 + 32 * u;
+                    if (g < groups_per_row) {
+                        const uint32_t w[8] = {y0[u].x, y0[u].y, y0[u].z, y0[u].w,
+                                               y1[u].x, y1[u].y, y1[u].z, y1[u].w};
+                        uint32_t o[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
-                    const uint32_t hi = pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
-                    o[h] = lo | (hi << 16);
+                        for (int h = 0; h < 4; ++h) {
+                            const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
+                            const uint32_t hi =
+                                pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
+                            o[h] = lo | (hi << 16);
+                        }
+                        dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
                 }
-                *reinterpret_cast<uint4*>(p.q_out + m * p.N + n0) = make_uint4(o[0], o[1], o[2], o[3]);
-                if (n0 == 0) p.out_row_scale[m] = s;
             }
         }
     }

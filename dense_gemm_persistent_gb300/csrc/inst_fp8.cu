@@ -19,6 +19,11 @@ const KernelInfo* kernels_fp8(int* count) {
         make_info<Cfg<64, true, true, false, MODE_SWAP>>(),
         make_info<Cfg<256, true, false, false, MODE_ROWQ>>(),   // E4M3 row requantisation
         make_info<Cfg<256, true, false, true, MODE_ROWQ>>(),
+        // CTA pairs: 256 x 256 tiles over two SMs
+        make_info<Cfg<256, true, false, false, MODE_TILE, true>>(),
+        make_info<Cfg<256, true, false, true, MODE_TILE, true>>(),
+        make_info<Cfg<256, true, false, false, MODE_ROWQ, true>>(),
+        make_info<Cfg<256, true, false, true, MODE_ROWQ, true>>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;

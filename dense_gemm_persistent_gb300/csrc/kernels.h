@@ -14,8 +14,8 @@ using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, con
                                  const Params& p, int grid, cudaStream_t s, bool cooperative);
 
 struct KernelInfo {
-    int bn, fp8, a_mn, b_mn, mode;
-    int stages, smem_bytes, tmem_cols;
+    int bn, fp8, a_mn, b_mn, mode, pair;
+    int stages, smem_bytes, tmem_cols, threads;
     const void* func;  // host stub of the __global__ function (for attributes)
     LaunchFn launch;
 };
@@ -28,20 +28,29 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
     cfg.blockDim = dim3(CF::NUM_THREADS);
     cfg.dynamicSmemBytes = CF::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    if (cooperative) {
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (CF::PAIR) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, gemm_persistent<CF>, a, b, d, p);
 }
 
 template <class CF>
 KernelInfo make_info() {
-    return KernelInfo{CF::BN,     CF::FP8,        CF::A_MN,      CF::B_MN,
-                      CF::MODE,   CF::STAGES,     CF::SMEM_BYTES, CF::TMEM_COLS,
+    return KernelInfo{CF::BN,     CF::FP8,    CF::A_MN,       CF::B_MN,      CF::MODE,
+                      CF::PAIR ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
                       reinterpret_cast<const void*>(&gemm_persistent<CF>), &launch_variant<CF>};
 }
 

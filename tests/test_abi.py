@@ -89,19 +89,24 @@ def test_plans_for_the_five_workloads(lib):
     p1 = dg.dgemm_plan(0, 512, 512, 512, "kn", "f32", num_sms=152)
     assert p1["swap_ab"] == 0 and p1["grid"] <= 152 and p1["tile_n"] == 64
     p2 = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
-    assert p2["tile_n"] == 256 and p2["num_tiles"] == 512 and p2["grid"] == 152
+    assert (p2["cta_group"], p2["tile_m"], p2["tile_n"]) == (2, 256, 256)
+    assert p2["num_tiles"] == 256 and p2["grid"] == 152 and p2["stages"] == 6
     p3 = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
-    assert p3["num_tiles"] == 32 * 43 and p3["grid"] == 152
+    assert p3["cta_group"] == 2 and p3["num_tiles"] == 16 * 43 and p3["grid"] == 152
     p4 = dg.dgemm_plan(0, 16, 18432, 7168, "nk", "bf16", num_sms=152)
     assert p4["swap_ab"] == 1 and p4["tile_n"] == 16 and p4["num_tiles"] == 144 and p4["grid"] == 144
     p5 = dg.dgemm_plan(1, 8192, 8192, 8192, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=152)
-    assert p5["cooperative"] == 1 and p5["tile_n"] == 256 and p5["num_tiles"] == 64 * 32
+    assert p5["cooperative"] == 1 and p5["tile_n"] == 256 and p5["cta_group"] == 2 and p5["num_tiles"] == 32 * 32
     for p in (p1, p2, p3, p4, p5):
         assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
 
 
-def test_tile_width_override(lib, monkeypatch):
+def test_tile_width_and_pair_overrides(lib, monkeypatch):
     monkeypatch.setenv("DGEMM_TILE_N", "128")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tile_n"] == 128
     monkeypatch.setenv("DGEMM_TILE_N", "96")     # no such variant: ignored
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tile_n"] == 256
+    monkeypatch.delenv("DGEMM_TILE_N")
+    monkeypatch.setenv("DGEMM_CTA_PAIR", "0")
+    p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")
+    assert (p["cta_group"], p["tile_m"], p["tile_n"], p["num_tiles"], p["stages"]) == (1, 128, 256, 512, 4)

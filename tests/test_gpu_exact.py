@@ -119,3 +119,37 @@ def test_k_group_promotion_exact(M, kblocks):
     assert plan["swap_ab"] == 1 and plan["k_groups"] == min(kblocks, 512 // plan["tile_n"])
     got, ref = bf16_case(M, 304, K, "nk", seed=300 + kblocks)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_bf16_wide_tile_single_and_pair_exact(layout, pair, monkeypatch):
+    """128 x 256 tiles on one CTA and 256 x 256 tiles on a CTA pair (cta_group::2),
+    with M, N and K tails."""
+    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
+    monkeypatch.setenv("DGEMM_TILE_N", "256")
+    plan = dg.dgemm_plan(0, 700, 776, 328, layout, "f32")
+    assert plan["cta_group"] == (2 if pair == "1" else 1) and plan["tile_n"] == 256
+    got, ref = bf16_case(700, 776, 328, layout, seed=400 + int(pair))
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_fp8_wide_tile_single_and_pair_exact(layout, pair, monkeypatch):
+    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
+    monkeypatch.setenv("DGEMM_TILE_N", "256")
+    plan = dg.dgemm_plan(1, 700, 784, 400, layout, "f32")
+    assert plan["cta_group"] == (2 if pair == "1" else 1) and plan["tile_n"] == 256
+    got, ref = fp8_case(700, 784, 400, layout, seed=500 + int(pair))
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("kblocks", [1, 5, 6, 7, 13])
+def test_pair_phases_across_many_tiles_exact(kblocks):
+    """CTA pairs with several tiles each (4096 x 8192 -> 512 tiles over <= 76 pairs)
+    and K-slice counts around the 6-stage ring depth."""
+    plan = dg.dgemm_plan(0, 4096, 8192, 64 * kblocks, "nk", "f32")
+    assert plan["cta_group"] == 2
+    got, ref = bf16_case(4096, 8192, 64 * kblocks, "nk", seed=600 + kblocks)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
