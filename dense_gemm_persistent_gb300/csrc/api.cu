@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -20,6 +21,7 @@ __device__ unsigned int g_status = 0;  // sticky device-side error bits, one wor
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kWsHeader = 256;  // grid-barrier counter lives here
+constexpr int64_t kMinTailSlices = 48;  // shortest tile (K slices) worth splitting
 
 struct DeviceState {
     std::once_flag once;
@@ -62,6 +64,27 @@ size_t dtype_bytes(dgemm_dtype_t t) { return t == DGEMM_F32 ? 4 : t == DGEMM_BF1
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+int pair_ctas(int pair) { return pair ? 2 : 1; }
+
+// Launch epochs for the tail-split arrival counters: 56-bit values, unique per
+// launch within a process and started from a per-process pseudo-random point,
+// so counter words left in a reused workspace (by any earlier call, or by other
+// data) are not mistaken for this launch's arrivals.
+std::atomic<unsigned long long> g_epoch{0};
+std::once_flag g_epoch_once;
+
+unsigned long long next_epoch() {
+    std::call_once(g_epoch_once, []() {
+        unsigned long long x = static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count());
+        x ^= reinterpret_cast<uintptr_t>(&g_epoch) * 0x9E3779B97F4A7C15ull;
+        x ^= x >> 31;
+        x *= 0xBF58476D1CE4E5B9ull;
+        x ^= x >> 29;
+        g_epoch.store(x, std::memory_order_relaxed);
+    });
+    return (g_epoch.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 56) - 1);
+}
+
 struct Plan {
     dgemm_plan_t pub;
     int kernel;        // index into g_kernels
@@ -70,12 +93,14 @@ struct Plan {
     int64_t Mm, Nm;    // problem in the MMA's orientation
     int bk;            // K elements per stage
     int acc_stride;    // TMEM columns between the two accumulator buffers
+    int dp_tiles, split, tail_items;   // tail splitting (MODE_TILE)
+    size_t tail_count_bytes;           // workspace: per-warp arrival counters
 };
 
 // Validates the sizes, enums and epilogue; picks the kernel variant and grid.
 // Pure host logic: needs no GPU.
 dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t bl, dgemm_dtype_t d_dtype,
-                         const dgemm_epilogue_t* epi, int num_sms, int max_pairs, Plan* out) {
+                         const dgemm_epilogue_t* epi, int num_sms, int max_pairs, bool allow_split, Plan* out) {
     if (M < 0 || N < 0 || K < 0 || num_sms <= 0) return DGEMM_ERR_INVALID_VALUE;
     if (bl != DGEMM_B_KN && bl != DGEMM_B_NK) return DGEMM_ERR_INVALID_VALUE;
     if (d_dtype != DGEMM_F32 && d_dtype != DGEMM_BF16 && d_dtype != DGEMM_E4M3) return DGEMM_ERR_INVALID_VALUE;
@@ -183,8 +208,41 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         p.acc_stride = groups * bn;
     }
     p.pub.k_groups = groups;
-    p.pub.workspace_bytes =
-        oq ? kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2 : 0;
+    // Tail splitting: when the tiles do not fill the last wave, run the full
+    // waves whole and split each leftover tile along K into as many segments
+    // as there are idle units (2), so the wave ends after half a tile instead
+    // of a whole one. Needs workspace for FP32 partials, bounded by one
+    // tile-sized partial per unit. The partials' round trip through L2 costs a
+    // few microseconds, so only long tiles (>= kMinTailSlices K slices) are
+    // split, and problems with no full wave are left alone.
+    // DGEMM_TAIL_SPLIT=0 disables splitting, =force drops the length rule.
+    p.dp_tiles = p.pub.num_tiles;
+    p.split = 1;
+    p.tail_items = 0;
+    p.tail_count_bytes = 0;
+    const char* split_env = std::getenv("DGEMM_TAIL_SPLIT");
+    const bool force_split = split_env && split_env[0] == 'f';
+    if (p.mode == dg::MODE_TILE && allow_split && !(split_env && split_env[0] == '0') && k_blocks > 0) {
+        const int rem = p.pub.num_tiles % units;
+        if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks >= kMinTailSlices)) {
+            int64_t split64 = units / rem;
+            if (split64 > k_blocks / 8) split64 = k_blocks / 8;
+            if (split64 > 2) split64 = 2;   // a third or fourth partial costs more than it saves
+            const int split = static_cast<int>(split64);
+            if (split >= 2) {
+                p.dp_tiles = p.pub.num_tiles - rem;
+                p.split = split;
+                p.tail_items = rem * split;
+                p.pub.grid = pair_ctas(pair) * units;   // every unit takes a tail segment
+                p.tail_count_bytes = round_up(static_cast<size_t>(units) * pair_ctas(pair) * k->epi_warps * 8, 256);
+                p.pub.workspace_bytes = p.tail_count_bytes + static_cast<size_t>(units) * pair_ctas(pair) * 128 *
+                                                                 static_cast<size_t>(bn) * 4;
+            }
+        }
+    }
+    p.pub.tail_tiles = p.pub.num_tiles - p.dp_tiles;
+    p.pub.tail_split = p.split;
+    if (oq) p.pub.workspace_bytes = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
     *out = p;
     return DGEMM_OK;
 }
@@ -289,7 +347,7 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
                    size_t ws_bytes, cudaStream_t stream) {
     // ---- arguments that need no device
     Plan plan;
-    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, &plan);
+    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, false, &plan);
     if (st != DGEMM_OK) return st;
     if (M == 0 || N == 0) return DGEMM_OK;
     if (!D || (K > 0 && (!A || !B))) return DGEMM_ERR_INVALID_VALUE;
@@ -315,8 +373,13 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     int devid = 0;
     st = device_state(&dev, &devid);
     if (st != DGEMM_OK) return st;
-    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, max_pairs(dev, devid, fp8), &plan);
+    const int pairs = max_pairs(dev, devid, fp8);
+    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, true, &plan);
     if (st != DGEMM_OK) return st;
+    if (plan.split > 1 && (!ws || ws_bytes < plan.pub.workspace_bytes)) {
+        st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, false, &plan);  // no room: whole tiles
+        if (st != DGEMM_OK) return st;
+    }
     const dg::KernelInfo* k = g_kernels[plan.kernel];
     if (configure_kernel(plan.kernel, devid) != cudaSuccess) return DGEMM_ERR_CUDA;
 
@@ -381,6 +444,14 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.bias = bias;
     p.act = epi ? epi->act : 0;
     p.status = dev->status;
+    p.dp_tiles = plan.dp_tiles;
+    p.split = plan.split;
+    p.tail_items = plan.tail_items;
+    if (plan.split > 1) {
+        p.tail_count = reinterpret_cast<unsigned long long*>(wsb);
+        p.partials = reinterpret_cast<float*>(wsb + plan.tail_count_bytes);
+        p.epoch = next_epoch();
+    }
     if (plan.mode == dg::MODE_ROWQ) {
         p.barrier = reinterpret_cast<unsigned*>(wsb);
         p.amax = reinterpret_cast<unsigned*>(wsb + kWsHeader);
@@ -417,11 +488,25 @@ dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t
 
 size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,
                             const dgemm_epilogue_t* epi) {
+    // SM count of the current device if there is one, else a GB300's 152.
+    int sms = 152, pairs = 76;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        DeviceState* ds = nullptr;
+        int devid = 0;
+        if (device_state(&ds, &devid) == DGEMM_OK) {
+            sms = ds->num_sms;
+            pairs = max_pairs(ds, devid, is_fp8 ? 1 : 0);
+        }
+    } else {
+        (void)cudaGetLastError();
+    }
     Plan plan;
     const dgemm_dtype_t d = (epi && epi->out_quant) ? DGEMM_E4M3 : DGEMM_BF16;
-    if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d, epi, 2, 1, &plan) != DGEMM_OK) {
+    if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d, epi, sms, pairs, true, &plan) != DGEMM_OK) {
         // the output dtype is not an argument here: retry with FP32 output
-        if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, DGEMM_F32, epi, 2, 1, &plan) != DGEMM_OK) return 0;
+        if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, DGEMM_F32, epi, sms, pairs, true, &plan) != DGEMM_OK)
+            return 0;
     }
     return plan.pub.workspace_bytes;
 }
@@ -429,8 +514,18 @@ size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b
 dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,
                           dgemm_dtype_t d_dtype, const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan) {
     if (!plan) return DGEMM_ERR_INVALID_VALUE;
+    int pairs = num_sms / 2;
+    if (num_sms <= 0) {  // the current device: its SM count and measured CTA-pair occupancy
+        DeviceState* ds = nullptr;
+        int devid = 0;
+        const dgemm_status_t dst = device_state(&ds, &devid);
+        if (dst != DGEMM_OK) return dst;
+        num_sms = ds->num_sms;
+        pairs = max_pairs(ds, devid, is_fp8 ? 1 : 0);
+    }
     Plan p;
-    const dgemm_status_t st = make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, num_sms / 2, &p);
+    const dgemm_status_t st =
+        make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, pairs, true, &p);
     if (st == DGEMM_OK) *plan = p.pub;
     return st;
 }

@@ -77,7 +77,45 @@ struct Params {
     uint8_t* q_out;          // [M,N] E4M3 codes
     float* out_row_scale;    // [M]
     unsigned* status;        // sticky device error word
+    // Tail splitting (MODE_TILE): tiles [0, dp_tiles) run whole; each of the
+    // remaining tiles is split along K into `split` segments (tail_items in
+    // all), every unit taking at most one. Each epilogue warp writes its region
+    // of a segment's FP32 accumulator to `partials` and counts it in
+    // tail_count; the last warp to arrive for a region sums the region's
+    // partials and runs the epilogue on it.
+    int dp_tiles, split, tail_items;
+    float* partials;         // [tail_items][CTAS][EPI_WARPS][units][8][32 lanes] float4
+    unsigned long long* tail_count;  // [num_tiles - dp_tiles][CTAS][EPI_WARPS]: (epoch << 8) | arrivals
+    unsigned long long epoch;        // unique per launch (56 bits): stale counters need no clearing
 };
+
+// One unit of work: a whole tile (item < 0) or one K segment of a split tile.
+struct Work {
+    int tile, kb0, kb1, item;
+};
+
+// The iter-th work item of a unit (a CTA, or a CTA pair): first its whole
+// tiles unit, unit + units, ... below dp_tiles, then tail items likewise.
+__device__ __forceinline__ bool next_work(const Params& p, int unit, int units, int iter, Work& w) {
+    const int dp_count = p.dp_tiles > unit ? (p.dp_tiles - unit + units - 1) / units : 0;
+    if (iter < dp_count) {
+        w.tile = unit + iter * units;
+        w.kb0 = 0;
+        w.kb1 = p.k_blocks;
+        w.item = -1;
+        return true;
+    }
+    const int j = unit + (iter - dp_count) * units;
+    if (j >= p.tail_items) return false;
+    const int seg = j % p.split;
+    w.tile = p.dp_tiles + j / p.split;
+    w.kb0 = (seg * p.k_blocks) / p.split;
+    w.kb1 = ((seg + 1) * p.k_blocks) / p.split;
+    w.item = j;
+    return true;
+}
+
+
 
 template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false>
 struct Cfg {
@@ -253,6 +291,48 @@ __device__ __forceinline__ void epilogue_math(float (&v)[32], const Params& p, i
     activation32(v, p.act);
 }
 
+// Converts 32 finished values of this thread's row and stages them; every
+// 128-byte box row (32 FP32 or 64 BF16 columns) is sent with one TMA store per
+// warp (32 rows). One 4 KB staging box per warp: before refilling it, the
+// previous box's store must have finished reading it.
+template <class CF>
+__device__ __forceinline__ void tile_store_unit(const float (&v)[32], const Params& p, int u, int col0, int row_base,
+                                                int lane, uint8_t* box, int& stores, const CUtensorMap* tmD) {
+    const bool f32_out = (CF::MODE == MODE_TILE) && p.d_f32;
+    const int half = f32_out ? 0 : (u & 1);
+    if (half == 0) {
+        if (stores >= 1 && lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+    }
+    uint8_t* rowp = box + lane * 128;
+    const int sw = lane & 7;
+    if (f32_out) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 wv = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                        __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+            *reinterpret_cast<uint4*>(rowp + ((c ^ sw) << 4)) = wv;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 wv = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                        pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                        pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+            *reinterpret_cast<uint4*>(rowp + (((half * 4 + c) ^ sw) << 4)) = wv;
+        }
+    }
+    if (f32_out || half == 1) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmD, box, f32_out ? col0 : col0 - 32, row_base);
+            bulk_commit();
+        }
+        ++stores;
+    }
+}
+
 template <class CF>
 __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -328,12 +408,13 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int t = unit0; ok && t < p.num_tiles; t += units) {
+            Work w;
+            for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it) {
                 int mb, nb;
-                tile_coords(t, p, mb, nb);
+                tile_coords(w.tile, p, mb, nb);
                 const int row0 = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM;   // this CTA's A rows
                 const int col0 = nb * CF::BN + static_cast<int>(rank) * CF::BN_CTA;  // this CTA's B rows
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                         ok = false;
                         break;
@@ -410,7 +491,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int local = 0;
-            for (int t = unit0; ok && t < p.num_tiles; t += units, ++local) {
+            Work w;
+            for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it, ++local) {
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, abort_flag)) {
@@ -419,17 +501,19 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t acc_base = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
-                // group g covers K slices [ceil(g*KB/G), ceil((g+1)*KB/G))
+                // group g covers K slices [ceil(g*KB/G), ceil((g+1)*KB/G)) of
+                // the item's range (the small-M form, the only one with G > 1,
+                // never splits a tile, so there the range is the whole K)
                 int group = 0;
-                int next_group_start = ngroups > 1 ? (kblocks + ngroups - 1) / ngroups : kblocks;
+                int next_group_start = ngroups > 1 ? (kblocks + ngroups - 1) / ngroups : w.kb1;
                 uint32_t d_tmem = acc_base;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    bool first_in_group = (kb == 0);
+                    bool first_in_group = (kb == w.kb0);
                     if (kb == next_group_start) {
                         ++group;
                         first_in_group = true;
@@ -488,9 +572,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         int stores = 0;
         int local = 0;
         bool ok = true;
-        for (int t = unit0; t < p.num_tiles; t += units, ++local) {
+        Work w;
+        for (int it = 0; next_work(p, unit0, units, it, w); ++it, ++local) {
             int mb, nb;
-            tile_coords(t, p, mb, nb);
+            tile_coords(w.tile, p, mb, nb);
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) {
@@ -540,6 +625,18 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 }
+                if constexpr (CF::MODE == MODE_TILE) {
+                    if (w.item >= 0) {
+                        // tail segment: park the raw FP32 accumulator, laid out
+                        // so that each warp-wide store writes 512 contiguous bytes
+                        float4* dst = reinterpret_cast<float4*>(p.partials) +
+                                      (((static_cast<int64_t>(w.item) * CF::CTAS + rank) * CF::EPI_WARPS + ew) *
+                                           NUNITS + u) * 256 + lane;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                    }
+                }
                 if (u == NUNITS - 1) {
                     // Last read of this accumulator: hand it back to the MMA warp.
                     tc_fence_before();
@@ -551,6 +648,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             mbar_arrive(&acc_empty[buf]);
                     }
                 }
+                if (CF::MODE == MODE_TILE && w.item >= 0) continue;   // finished by the last segment
                 epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row);
 
                 if constexpr (CF::MODE == MODE_SWAP) {
@@ -568,7 +666,6 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             }
                     }
                 } else {
-                    const bool f32_out = (CF::MODE == MODE_TILE) && p.d_f32;
                     if constexpr (CF::MODE == MODE_ROWQ) {
                         if (row < p.M) {
 #pragma unroll
@@ -576,48 +673,75 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                 if (col0 + j < p.N) rowmax = fmaxf(rowmax, fabsf(v[j]));
                         }
                     }
-                    // 32 columns are a whole 128-byte box row for FP32 output and
-                    // half of one for BF16; a box is 32 rows (one per lane).
-                    const int half = f32_out ? 0 : (u & 1);
-                    uint8_t* box = stg;
-                    if (half == 0) {
-                        // the previous box's TMA store must have read the staging buffer
-                        if (stores >= 1 && lane == 0) bulk_wait_read<0>();
-                        __syncwarp();
-                    }
-                    uint8_t* rowp = box + lane * 128;
-                    const int sw = lane & 7;
-                    if (f32_out) {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 w = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
-                                                       __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
-                            *reinterpret_cast<uint4*>(rowp + ((c ^ sw) << 4)) = w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 w = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
-                                                       pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
-                                                       pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
-                                                       pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
-                            *reinterpret_cast<uint4*>(rowp + (((half * 4 + c) ^ sw) << 4)) = w;
-                        }
-                    }
-                    if (f32_out || half == 1) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const int x = f32_out ? col0 : col0 - 32;
-                            tma_store_2d(&tmD, box, x, row_base);
-                            bulk_commit();
-                        }
-                        ++stores;
-                    }
+                    tile_store_unit<CF>(v, p, u, col0, row_base, lane, stg, stores, &tmD);
                 }
             }
             if constexpr (CF::MODE == MODE_ROWQ) {
                 if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
+            }
+            if constexpr (CF::MODE == MODE_TILE) {
+                if (w.item >= 0) {
+                    // This warp's region (32 rows x EPI_COLS columns) of the
+                    // segment is in place: count it; the warp that brings the
+                    // count to `split` sums the region's partials and stores them.
+                    // Each warp counts and reduces on its own (no cross-warp wait).
+                    __syncwarp();
+                    unsigned last = 0;
+                    if (lane == 0) {
+                        // The counter word holds (launch epoch << 8) | arrivals; a
+                        // word left by any earlier launch counts as zero arrivals.
+                        unsigned long long* cnt =
+                            p.tail_count + ((w.tile - p.dp_tiles) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
+                        __threadfence();
+                        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), next = 0;
+                        for (int tries = 0; tries < 4096; ++tries) {
+                            next = ((old >> 8) == p.epoch) ? old + 1 : ((p.epoch << 8) | 1ull);
+                            const unsigned long long seen = atomicCAS(cnt, old, next);
+                            if (seen == old) break;
+                            old = seen;
+                        }
+                        last = ((next >> 8) == p.epoch && (next & 0xFFull) == static_cast<unsigned long long>(p.split))
+                                   ? 1u : 0u;
+                        __threadfence();
+                    }
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    if (last) {
+                        const int item0 = (w.tile - p.dp_tiles) * p.split;
+                        // item stride of the partial layout, in float4
+                        constexpr int64_t ITEM_F4 = static_cast<int64_t>(CF::CTAS) * CF::EPI_WARPS * NUNITS * 256;
+#pragma unroll 1
+                        for (int u = 0; u < NUNITS; ++u) {
+                            const int tcol = cbase + u * UNIT;
+                            const int col0 = nb * CF::BN + tcol;
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                            const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
+                                                ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) * 256 +
+                                                lane;
+                            // two segments' loads in flight at a time
+#pragma unroll 1
+                            for (int sgi = 0; sgi < p.split; sgi += 2) {
+                                const bool two = sgi + 1 < p.split;
+                                float4 f0[8], f1[8];
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    f0[j] = __ldcg(src + sgi * ITEM_F4 + 32 * j);
+                                    f1[j] = two ? __ldcg(src + (sgi + 1) * ITEM_F4 + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                }
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    v[4 * j] += f0[j].x + f1[j].x;
+                                    v[4 * j + 1] += f0[j].y + f1[j].y;
+                                    v[4 * j + 2] += f0[j].z + f1[j].z;
+                                    v[4 * j + 3] += f0[j].w + f1[j].w;
+                                }
+                            }
+                            epilogue_math<false>(v, p, row, col0, UNIT, rs, bias_row);
+                            tile_store_unit<CF>(v, p, u, col0, row_base, lane, stg, stores, &tmD);
+                        }
+                    }
+                }
             }
         }
         if (!ok) raise_error(p, ERR_TIMEOUT_EPILOGUE, abort_flag);

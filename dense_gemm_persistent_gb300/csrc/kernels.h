@@ -15,7 +15,7 @@ using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, con
 
 struct KernelInfo {
     int bn, fp8, a_mn, b_mn, mode, pair;
-    int stages, smem_bytes, tmem_cols, threads;
+    int stages, smem_bytes, tmem_cols, threads, epi_warps;
     const void* func;  // host stub of the __global__ function (for attributes)
     LaunchFn launch;
 };
@@ -50,7 +50,7 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
 template <class CF>
 KernelInfo make_info() {
     return KernelInfo{CF::BN,     CF::FP8,    CF::A_MN,       CF::B_MN,      CF::MODE,
-                      CF::PAIR ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
+                      CF::PAIR ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS, CF::EPI_WARPS,
                       reinterpret_cast<const void*>(&gemm_persistent<CF>), &launch_variant<CF>};
 }
 

@@ -120,6 +120,9 @@ typedef struct {
     int k_groups;          /* K-group promotion: K is split into this many
                               contiguous groups, each accumulated by the tensor
                               core separately and summed in FP32 (1 = off)      */
+    int tail_tiles;        /* tiles of the last, partial wave that are split
+                              along K so the wave finishes sooner (0 = none)    */
+    int tail_split;        /* K segments per tail tile (1 = no splitting)       */
     size_t smem_bytes;     /* dynamic shared memory per CTA                     */
     size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
 } dgemm_plan_t;
@@ -129,8 +132,11 @@ typedef struct {
  *   C        [M,N] of c_dtype (F32 or BF16); read only when beta != 0.
  *   D        [M,N] of d_dtype: F32 or BF16, or E4M3 with
  *            epi->out_quant == DGEMM_QUANT_E4M3_ROW_AMAX.
- *   ws       device workspace of ws_bytes >= dgemm_workspace_size(0, ...);
- *            may be NULL when that size is 0.
+ *   ws       device workspace of ws_bytes bytes. Required (at least
+ *            dgemm_workspace_size(0, ...)) with the requantising epilogue.
+ *            Otherwise optional: when it is at least that size, the last
+ *            partial wave of tiles is split along K across the idle SMs (FP32
+ *            partials in the workspace); with less, tiles are never split.
  * [W1] §1.1, §3.1, §6. */
 dgemm_status_t dgemm_bf16(const void* A, const void* B, dgemm_b_layout_t b_layout,
                           const void* C, dgemm_dtype_t c_dtype,
@@ -156,15 +162,19 @@ dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t
                                 const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes,
                                 dgemm_stream_t stream);
 
-/* Workspace bytes a call with these arguments needs (0 when none). Query it
- * once and pass a buffer at least this large ([W3] §5.1). Host-only; no GPU
- * needed. Returns 0 for invalid arguments. */
+/* Workspace bytes a call with these arguments can use (0 when none). Query it
+ * once and pass a buffer at least this large ([W3] §5.1). Uses the current
+ * device's SM count when a device is present (else 152, a GB300); no kernel
+ * runs. Returns 0 for invalid arguments. */
 size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K,
                             dgemm_b_layout_t b_layout, const dgemm_epilogue_t* epi);
 
-/* The plan a call with these arguments would use on a GPU with num_sms SMs.
- * Host-only; no GPU needed. Returns DGEMM_OK and fills *plan, or the same
- * argument error the GEMM call would return for these sizes. */
+/* The plan a call with these arguments would use on a GPU with num_sms SMs
+ * (host-only, no GPU needed; CTA pairs assumed to fill half the SMs), or, with
+ * num_sms <= 0, on the current device (its SM count and measured CTA-pair
+ * occupancy). Assumes a workspace of at least dgemm_workspace_size bytes.
+ * Returns DGEMM_OK and fills *plan, or the same argument error the GEMM call
+ * would return for these sizes. */
 dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K,
                           dgemm_b_layout_t b_layout, dgemm_dtype_t d_dtype,
                           const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan);

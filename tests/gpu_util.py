@@ -21,11 +21,11 @@ def run_workload(w: wl.Workload, d_dtype: str | None = None):
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}[d_dtype]
     D = torch.empty(w.M, w.N, dtype=tdt, device=dev())
     s = None
-    ws = None
     if w.out_quant != "none":
         s = torch.empty(w.M, dtype=torch.float32, device=dev())
-        nbytes = dg.dgemm_workspace_size(w.form == "fp8", w.M, w.N, w.K, w.b_layout, out_quant=w.out_quant)
-        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev())
+    # the workspace the library can use (tail splitting, requantisation)
+    nbytes = dg.dgemm_workspace_size(w.form == "fp8", w.M, w.N, w.K, w.b_layout, out_quant=w.out_quant)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev()) if nbytes else None
     kw = dict(b_layout=w.b_layout, C=g.C, alpha=w.alpha, beta=w.beta, bias=g.bias, act=w.act,
               out_quant=w.out_quant, out_row_scale=s, ws=ws)
     if w.form == "bf16":

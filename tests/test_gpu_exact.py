@@ -27,12 +27,17 @@ def int_e4m3(rng, shape, lo=-8, hi=8):
     return torch.from_numpy(rng.integers(lo, hi + 1, size=shape).astype(np.float32)).to(torch.float8_e4m3fn)
 
 
-def bf16_case(M, N, K, layout, seed, d_dtype=torch.float32):
+def workspace(fp8, M, N, K, layout):
+    n = dg.dgemm_workspace_size(fp8, M, N, K, layout)
+    return torch.empty(n, dtype=torch.uint8, device=dev()) if n else None
+
+
+def bf16_case(M, N, K, layout, seed, d_dtype=torch.float32, ws=False):
     rng = np.random.default_rng(seed)
     A = int_bf16(rng, (M, K))
     B = int_bf16(rng, (K, N) if layout == "kn" else (N, K))
     D = torch.empty(M, N, dtype=d_dtype, device=dev())
-    dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout=layout)
+    dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout=layout, ws=workspace(0, M, N, K, layout) if ws else None)
     assert dg.dgemm_query_device_status() == 0
     ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), layout)
     return D.cpu().to(torch.float64).numpy(), ref
@@ -63,7 +68,7 @@ def test_bf16_exact_bf16_output(layout):
     assert np.array_equal(got, oracle.round_bf16(ref))
 
 
-def fp8_case(M, N, K, layout, seed, scales="pow2"):
+def fp8_case(M, N, K, layout, seed, scales="pow2", ws=False):
     rng = np.random.default_rng(seed)
     Aq = int_e4m3(rng, (M, K))
     Bq = int_e4m3(rng, (K, N) if layout == "kn" else (N, K))
@@ -73,7 +78,8 @@ def fp8_case(M, N, K, layout, seed, scales="pow2"):
     else:
         sa, sb = torch.ones(M), torch.ones(N)
     D = torch.empty(M, N, dtype=torch.float32, device=dev())
-    dg.dgemm_fp8_scaled(Aq.to(dev()), Bq.to(dev()), sa.to(dev()), sb.to(dev()), D, b_layout=layout)
+    dg.dgemm_fp8_scaled(Aq.to(dev()), Bq.to(dev()), sa.to(dev()), sb.to(dev()), D, b_layout=layout,
+                        ws=workspace(1, M, N, K, layout) if ws else None)
     assert dg.dgemm_query_device_status() == 0
     ref = oracle.fp8_gemm_ref(wl.codes_u8(Aq), wl.codes_u8(Bq), layout, sa.numpy(), sb.numpy())
     return D.cpu().to(torch.float64).numpy(), ref
@@ -152,4 +158,55 @@ def test_pair_phases_across_many_tiles_exact(kblocks):
     plan = dg.dgemm_plan(0, 4096, 8192, 64 * kblocks, "nk", "f32")
     assert plan["cta_group"] == 2
     got, ref = bf16_case(4096, 8192, 64 * kblocks, "nk", seed=600 + kblocks)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("shape,layout,pair", [((4096, 4096, 1024), "kn", "1"), ((4096, 4096, 1024), "nk", "0"),
+                                               ((2304, 2816, 1024), "nk", "1"), ((2560, 2048, 1024), "kn", "0"),
+                                               ((4000, 1288, 1024), "kn", "1")])
+def test_tail_split_exact(shape, layout, pair, monkeypatch):
+    """The last partial wave's tiles split along K (FP32 partials in the
+    workspace, last-arriving warp sums them): still bit-exact."""
+    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
+    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")   # split even these short tiles
+    M, N, K = shape
+    plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
+    assert plan["tail_split"] >= 2
+    got, ref = bf16_case(M, N, K, layout, seed=700 + K, ws=True)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_tail_split_fp8_exact(layout, monkeypatch):
+    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
+    plan = dg.dgemm_plan(1, 4096, 11008, 2048, layout, "f32")
+    assert plan["tail_split"] >= 2
+    got, ref = fp8_case(4096, 11008, 2048, layout, seed=800, ws=True)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+def test_tail_split_repeated_calls_reuse_workspace(monkeypatch):
+    """Arrival counters are tagged with a per-launch epoch: the same workspace,
+    even filled with garbage first, serves consecutive calls."""
+    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
+    M, N, K = 4096, 4096, 1024
+    ws = workspace(0, M, N, K, "nk")
+    ws.fill_(0xA5)
+    rng = np.random.default_rng(5)
+    for i in range(3):
+        A = int_bf16(rng, (M, K)); B = int_bf16(rng, (N, K))
+        D = torch.empty(M, N, dtype=torch.float32, device=dev())
+        dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout="nk", ws=ws)
+        assert dg.dgemm_query_device_status() == 0
+        ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), "nk")
+        assert np.array_equal(D.cpu().double().numpy(), ref)
+
+
+def test_tail_split_default_rule_on_long_tiles():
+    """Without forcing, a tail is split only for long tiles: 4096^3 BF16 (64 K
+    slices) splits its 28-tile tail, the same shape at K = 2048 does not."""
+    assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tail_split"] == 2
+    assert dg.dgemm_plan(0, 4096, 4096, 2048, "kn", "bf16")["tail_split"] == 1
+    got, ref = bf16_case(2304, 2816, 3072, "nk", seed=900, ws=True)
+    assert dg.dgemm_plan(0, 2304, 2816, 3072, "nk", "f32")["tail_split"] == 2
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
