@@ -190,7 +190,13 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.num_tiles = static_cast<int>(tiles_m * tiles_n);
     const int units = pair ? max_pairs : num_sms;
     p.pub.grid = (pair ? 2 : 1) * static_cast<int>(p.pub.num_tiles < units ? p.pub.num_tiles : units);
-    p.pub.cooperative = p.mode == dg::MODE_ROWQ ? 1 : 0;
+    // The requantising kernel's grid barrier needs every CTA resident: it is
+    // launched cooperatively (the grid is sized from the measured occupancy
+    // too). DGEMM_COOPERATIVE=0 drops the attribute, because Nsight Compute
+    // cannot launch cooperative cluster grids; on an otherwise idle GPU the
+    // grid is still co-resident, and the barrier's wait is bounded regardless.
+    const char* coop_env = std::getenv("DGEMM_COOPERATIVE");
+    p.pub.cooperative = (p.mode == dg::MODE_ROWQ && !(coop_env && coop_env[0] == '0')) ? 1 : 0;
     p.pub.raster_group = static_cast<int>(tiles_m < 8 ? (tiles_m > 0 ? tiles_m : 1) : 8);
     p.pub.smem_bytes = static_cast<size_t>(k->smem_bytes);
     // K-group promotion. The transposed small-M kernel owns all 512 TMEM
