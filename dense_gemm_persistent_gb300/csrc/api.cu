@@ -66,6 +66,17 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int pair_ctas(int pair) { return pair ? 2 : 1; }
 
+// Split-K for grids that do not fill the GPU: K segments per tile so that
+// tiles x segments <= units, each segment at least 8 K slices, at most 4 (the
+// last-arriving warp sums the others' partials with all loads in flight).
+int64_t underfill_split(int64_t tiles, int64_t units, int64_t k_blocks) {
+    if (tiles <= 0 || tiles >= units) return 1;
+    int64_t s = units / tiles;
+    if (s > k_blocks / 8) s = k_blocks / 8;
+    if (s > 4) s = 4;
+    return s < 1 ? 1 : s;
+}
+
 // Launch epochs for the tail-split arrival counters: 56-bit values, unique per
 // launch within a process and started from a per-process pseudo-random point,
 // so counter words left in a reused workspace (by any earlier call, or by other
@@ -122,6 +133,10 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     const bool swap = (oq == DGEMM_QUANT_NONE) && M <= 64;
     const char* pair_env = std::getenv("DGEMM_CTA_PAIR");  // "0" disables, "1" forces CTA pairs (tests, sweeps)
     const bool pairs_ok = max_pairs > 0 && !(pair_env && pair_env[0] == '0');
+    const char* split_env = std::getenv("DGEMM_TAIL_SPLIT");
+    const bool force_split = split_env && split_env[0] == 'f';
+    const bool split_ok = allow_split && !(split_env && split_env[0] == '0') && oq == DGEMM_QUANT_NONE;
+    const int64_t kb_all = (K + (128 / static_cast<int64_t>(esz)) - 1) / (128 / static_cast<int64_t>(esz));
     int bn;
     int pair = 0;
     if (swap) {
@@ -155,7 +170,10 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
             const int64_t units = c.pair ? max_pairs : num_sms;
             const int64_t tiles = ((M + tm - 1) / tm) * ((N + c.bn - 1) / c.bn);
             const int64_t waves = (tiles + units - 1) / units;
-            const double cost = static_cast<double>(waves) * (128.0 * c.bn) * c.penalty;
+            double cost = static_cast<double>(waves) * (128.0 * c.bn) * c.penalty;
+            // under one wave, split-K divides each unit's work (reduction ~15 % of a tile)
+            const int64_t sk = split_ok ? underfill_split(tiles, units, kb_all) : 1;
+            if (sk > 1) cost = (128.0 * c.bn) * c.penalty * (1.0 / static_cast<double>(sk) + 0.15);
             if (cost < best) {
                 best = cost;
                 bn = c.bn;
@@ -199,12 +217,49 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.cooperative = (p.mode == dg::MODE_ROWQ && !(coop_env && coop_env[0] == '0')) ? 1 : 0;
     p.pub.raster_group = static_cast<int>(tiles_m < 8 ? (tiles_m > 0 ? tiles_m : 1) : 8);
     p.pub.smem_bytes = static_cast<size_t>(k->smem_bytes);
+
+    // Tail splitting: when the tiles do not fill the last wave, run the full
+    // waves whole and split each leftover tile along K into as many segments
+    // as there are idle units (2), so the wave ends after half a tile instead
+    // of a whole one. Needs workspace for FP32 partials, bounded by one
+    // tile-sized partial per unit. The partials' round trip through L2 costs a
+    // few microseconds, so only long tiles (>= kMinTailSlices K slices) are
+    // split, and problems with no full wave are left alone.
+    // DGEMM_TAIL_SPLIT=0 disables splitting, =force drops the length rule.
+    const int64_t k_blocks = (K + p.bk - 1) / p.bk;
+    p.dp_tiles = p.pub.num_tiles;
+    p.split = 1;
+    p.tail_items = 0;
+    p.tail_count_bytes = 0;
+    auto use_split = [&](int dp_tiles, int split, int items) {
+        p.dp_tiles = dp_tiles;
+        p.split = split;
+        p.tail_items = items;
+        p.pub.grid = pair_ctas(pair) * (items > units ? units : (dp_tiles > 0 ? units : items));
+        p.tail_count_bytes = round_up(static_cast<size_t>(units) * pair_ctas(pair) * k->epi_warps * 8, 256);
+        p.pub.workspace_bytes =
+            p.tail_count_bytes + static_cast<size_t>(units) * pair_ctas(pair) * 128 * static_cast<size_t>(bn) * 4;
+    };
+    // Split-K when the tiles do not fill one wave (decode shapes, small M x N
+    // with long K): every tile is split into K segments run on the idle units.
+    const int64_t sk = (split_ok && k_blocks > 0) ? underfill_split(p.pub.num_tiles, units, k_blocks) : 1;
+    if (sk > 1 && (p.mode == dg::MODE_TILE || p.mode == dg::MODE_SWAP)) {
+        use_split(0, static_cast<int>(sk), p.pub.num_tiles * static_cast<int>(sk));
+    } else if (p.mode == dg::MODE_TILE && split_ok && k_blocks > 0) {
+        const int rem = p.pub.num_tiles % units;
+        if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks >= kMinTailSlices)) {
+            int64_t split64 = units / rem;
+            if (split64 > k_blocks / 8) split64 = k_blocks / 8;
+            if (split64 > 2) split64 = 2;   // a third or fourth partial costs more than it saves
+            const int split = static_cast<int>(split64);
+            if (split >= 2) use_split(p.pub.num_tiles - rem, split, rem * split);
+        }
+    }
     // K-group promotion. The transposed small-M kernel owns all 512 TMEM
     // columns but needs only BN per accumulator: it splits K into as many
     // groups as fit (two buffers of 256 columns when a CTA runs several tiles,
     // one of 512 when it runs one) and sums them in FP32, which cuts the
     // tensor core's round-toward-zero accumulation error by about that factor.
-    const int64_t k_blocks = (K + p.bk - 1) / p.bk;
     int groups = 1;
     p.acc_stride = bn;
     if (p.mode == dg::MODE_SWAP) {
@@ -214,38 +269,6 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         p.acc_stride = groups * bn;
     }
     p.pub.k_groups = groups;
-    // Tail splitting: when the tiles do not fill the last wave, run the full
-    // waves whole and split each leftover tile along K into as many segments
-    // as there are idle units (2), so the wave ends after half a tile instead
-    // of a whole one. Needs workspace for FP32 partials, bounded by one
-    // tile-sized partial per unit. The partials' round trip through L2 costs a
-    // few microseconds, so only long tiles (>= kMinTailSlices K slices) are
-    // split, and problems with no full wave are left alone.
-    // DGEMM_TAIL_SPLIT=0 disables splitting, =force drops the length rule.
-    p.dp_tiles = p.pub.num_tiles;
-    p.split = 1;
-    p.tail_items = 0;
-    p.tail_count_bytes = 0;
-    const char* split_env = std::getenv("DGEMM_TAIL_SPLIT");
-    const bool force_split = split_env && split_env[0] == 'f';
-    if (p.mode == dg::MODE_TILE && allow_split && !(split_env && split_env[0] == '0') && k_blocks > 0) {
-        const int rem = p.pub.num_tiles % units;
-        if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks >= kMinTailSlices)) {
-            int64_t split64 = units / rem;
-            if (split64 > k_blocks / 8) split64 = k_blocks / 8;
-            if (split64 > 2) split64 = 2;   // a third or fourth partial costs more than it saves
-            const int split = static_cast<int>(split64);
-            if (split >= 2) {
-                p.dp_tiles = p.pub.num_tiles - rem;
-                p.split = split;
-                p.tail_items = rem * split;
-                p.pub.grid = pair_ctas(pair) * units;   // every unit takes a tail segment
-                p.tail_count_bytes = round_up(static_cast<size_t>(units) * pair_ctas(pair) * k->epi_warps * 8, 256);
-                p.pub.workspace_bytes = p.tail_count_bytes + static_cast<size_t>(units) * pair_ctas(pair) * 128 *
-                                                                 static_cast<size_t>(bn) * 4;
-            }
-        }
-    }
     p.pub.tail_tiles = p.pub.num_tiles - p.dp_tiles;
     p.pub.tail_split = p.split;
     if (oq) p.pub.workspace_bytes = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;

@@ -84,7 +84,7 @@ struct Params {
     // tail_count; the last warp to arrive for a region sums the region's
     // partials and runs the epilogue on it.
     int dp_tiles, split, tail_items;
-    float* partials;         // [tail_items][CTAS][EPI_WARPS][units][8][32 lanes] float4
+    float* partials;         // [tail_items][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4
     unsigned long long* tail_count;  // [num_tiles - dp_tiles][CTAS][EPI_WARPS]: (epoch << 8) | arrivals
     unsigned long long epoch;        // unique per launch (56 bits): stale counters need no clearing
 };
@@ -501,12 +501,14 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t acc_base = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
-                // group g covers K slices [ceil(g*KB/G), ceil((g+1)*KB/G)) of
-                // the item's range (the small-M form, the only one with G > 1,
-                // never splits a tile, so there the range is the whole K)
+                // group g covers K slices [ceil(g*KB/G), ceil((g+1)*KB/G))
                 int group = 0;
-                int next_group_start = ngroups > 1 ? (kblocks + ngroups - 1) / ngroups : w.kb1;
-                uint32_t d_tmem = acc_base;
+                int next_group_start = w.kb1;
+                if (ngroups > 1) {   // a K segment may start inside the groups
+                    group = (w.kb0 * ngroups) / kblocks;
+                    next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
+                }
+                uint32_t d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
@@ -568,7 +570,12 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         const int q = warp & 3;                        // TMEM lane quarter this warp may access
         const int ew = warp - 2;                       // epilogue warp index
         const int cbase = (ew >> 2) * CF::EPI_COLS;    // first tile column this warp handles
-        uint8_t* stg = staging + ew * 4096;            // this warp's 4 KB staging box
+        uint8_t* stg = staging + ew * 4096;            // this warp's 4 KB staging box (tile modes)
+        constexpr int UNIT = CF::EPI_COLS < 32 ? CF::EPI_COLS : 32;
+        constexpr int NUNITS = CF::EPI_COLS / UNIT;
+        constexpr int UNIT_F4 = UNIT / 4;              // float4 per lane per unit in a partial
+        // partial layout: [item][cta][epilogue warp][unit][UNIT_F4][32 lanes] float4
+        constexpr int64_t ITEM_F4 = static_cast<int64_t>(CF::CTAS) * CF::EPI_WARPS * NUNITS * UNIT_F4 * 32;
         int stores = 0;
         int local = 0;
         bool ok = true;
@@ -587,25 +594,26 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             const int row = row_base + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * p.acc_stride);
-            const int groups = p.k_blocks > 0 ? p.acc_groups : 1;
+            // the K groups this item accumulated (a K segment touches only its own)
+            int g0 = 0, g1 = 1;
+            if (p.k_blocks > 0 && p.acc_groups > 1) {
+                g0 = (w.kb0 * p.acc_groups) / p.k_blocks;
+                g1 = ((w.kb1 - 1) * p.acc_groups) / p.k_blocks + 1;
+            }
             const float rs = (p.row_scale && row < p.M) ? p.row_scale[row] : 1.0f;
             float bias_row = 0.0f;
             if constexpr (CF::MODE == MODE_SWAP)
                 if (p.bias && row < p.M) bias_row = p.bias[row];
             float rowmax = 0.0f;
-            constexpr int UNIT = CF::EPI_COLS < 32 ? CF::EPI_COLS : 32;
-            constexpr int NUNITS = CF::EPI_COLS / UNIT;
-#pragma unroll 1
-            for (int u = 0; u < NUNITS; ++u) {
-                const int tcol = cbase + u * UNIT;            // column within the tile
-                const int col0 = nb * CF::BN + tcol;
-                float v[32];
+            const bool part = (CF::MODE != MODE_ROWQ) && w.item >= 0;   // a K segment of a split tile
+
+            // The accumulator of 32 (or 16) columns, FP32 sum of its K groups.
+            auto load_acc = [&](int u, float (&v)[32]) {
+                const int tcol = cbase + u * UNIT;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                // FP32 sum of the K-group partial accumulators (one group unless
-                // K-group promotion is on), added in group order.
 #pragma unroll 1
-                for (int g = 0; g < groups; ++g) {
+                for (int g = g0; g < g1; ++g) {
                     const uint32_t ta = taddr + static_cast<uint32_t>(g * CF::BN + tcol);
                     if constexpr (UNIT == 32) {
                         uint32_t r[32];
@@ -625,32 +633,11 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 }
-                if constexpr (CF::MODE == MODE_TILE) {
-                    if (w.item >= 0) {
-                        // tail segment: park the raw FP32 accumulator, laid out
-                        // so that each warp-wide store writes 512 contiguous bytes
-                        float4* dst = reinterpret_cast<float4*>(p.partials) +
-                                      (((static_cast<int64_t>(w.item) * CF::CTAS + rank) * CF::EPI_WARPS + ew) *
-                                           NUNITS + u) * 256 + lane;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-                    }
-                }
-                if (u == NUNITS - 1) {
-                    // Last read of this accumulator: hand it back to the MMA warp.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (CF::PAIR && rank != 0)
-                            mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
-                        else
-                            mbar_arrive(&acc_empty[buf]);
-                    }
-                }
-                if (CF::MODE == MODE_TILE && w.item >= 0) continue;   // finished by the last segment
+            };
+            // Epilogue arithmetic and output of finished values.
+            auto finish = [&](int u, float (&v)[32]) {
+                const int col0 = nb * CF::BN + cbase + u * UNIT;
                 epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row);
-
                 if constexpr (CF::MODE == MODE_SWAP) {
                     // MMA column = output row; MMA row = output column.
                     if (row < p.M) {
@@ -675,16 +662,44 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     }
                     tile_store_unit<CF>(v, p, u, col0, row_base, lane, stg, stores, &tmD);
                 }
+            };
+
+#pragma unroll 1
+            for (int u = 0; u < NUNITS; ++u) {
+                float v[32];
+                load_acc(u, v);
+                if (part) {
+                    // K segment: park the raw FP32 accumulator; each warp-wide
+                    // store writes 512 contiguous bytes
+                    float4* dst = reinterpret_cast<float4*>(p.partials) + w.item * ITEM_F4 +
+                                  ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) * (UNIT_F4 * 32) +
+                                  lane;
+#pragma unroll
+                    for (int j = 0; j < UNIT_F4; ++j)
+                        __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                }
+                if (u == NUNITS - 1) {
+                    // Last read of this accumulator: hand it back to the MMA warp.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (CF::PAIR && rank != 0)
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
+                        else
+                            mbar_arrive(&acc_empty[buf]);
+                    }
+                }
+                if (!part) finish(u, v);
             }
             if constexpr (CF::MODE == MODE_ROWQ) {
                 if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
             }
-            if constexpr (CF::MODE == MODE_TILE) {
-                if (w.item >= 0) {
+            if constexpr (CF::MODE != MODE_ROWQ) {
+                if (part) {
                     // This warp's region (32 rows x EPI_COLS columns) of the
                     // segment is in place: count it; the warp that brings the
-                    // count to `split` sums the region's partials and stores them.
-                    // Each warp counts and reduces on its own (no cross-warp wait).
+                    // count to `split` sums the region's partials and finishes
+                    // it. Each warp counts and reduces on its own (no waiting).
                     __syncwarp();
                     unsigned last = 0;
                     if (lane == 0) {
@@ -706,39 +721,39 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     }
                     last = __shfl_sync(0xffffffffu, last, 0);
                     if (last) {
+                        // Own segment from Tensor Memory (this is the unit's last
+                        // item, so its accumulator is never overwritten), the other
+                        // segments from the workspace, all their loads in flight
+                        // together (at most three others).
                         const int item0 = (w.tile - p.dp_tiles) * p.split;
-                        // item stride of the partial layout, in float4
-                        constexpr int64_t ITEM_F4 = static_cast<int64_t>(CF::CTAS) * CF::EPI_WARPS * NUNITS * 256;
+                        const int own = w.item - item0;
 #pragma unroll 1
                         for (int u = 0; u < NUNITS; ++u) {
-                            const int tcol = cbase + u * UNIT;
-                            const int col0 = nb * CF::BN + tcol;
                             float v[32];
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                            load_acc(u, v);
                             const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
-                                                ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) * 256 +
+                                                ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
+                                                    (UNIT_F4 * 32) +
                                                 lane;
-                            // two segments' loads in flight at a time
-#pragma unroll 1
-                            for (int sgi = 0; sgi < p.split; sgi += 2) {
-                                const bool two = sgi + 1 < p.split;
-                                float4 f0[8], f1[8];
+                            float4 f[3][UNIT_F4];
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    f0[j] = __ldcg(src + sgi * ITEM_F4 + 32 * j);
-                                    f1[j] = two ? __ldcg(src + (sgi + 1) * ITEM_F4 + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                                }
+                            for (int o = 0; o < 3; ++o) {
+                                const int sgi = o + (o >= own ? 1 : 0);
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    v[4 * j] += f0[j].x + f1[j].x;
-                                    v[4 * j + 1] += f0[j].y + f1[j].y;
-                                    v[4 * j + 2] += f0[j].z + f1[j].z;
-                                    v[4 * j + 3] += f0[j].w + f1[j].w;
-                                }
+                                for (int j = 0; j < UNIT_F4; ++j)
+                                    f[o][j] = sgi < p.split ? __ldcg(src + sgi * ITEM_F4 + 32 * j)
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
-                            epilogue_math<false>(v, p, row, col0, UNIT, rs, bias_row);
-                            tile_store_unit<CF>(v, p, u, col0, row_base, lane, stg, stores, &tmD);
+#pragma unroll
+                            for (int o = 0; o < 3; ++o)
+#pragma unroll
+                                for (int j = 0; j < UNIT_F4; ++j) {
+                                    v[4 * j] += f[o][j].x;
+                                    v[4 * j + 1] += f[o][j].y;
+                                    v[4 * j + 2] += f[o][j].z;
+                                    v[4 * j + 3] += f[o][j].w;
+                                }
+                            finish(u, v);
                         }
                     }
                 }

@@ -210,3 +210,36 @@ def test_tail_split_default_rule_on_long_tiles():
     got, ref = bf16_case(2304, 2816, 3072, "nk", seed=900, ws=True)
     assert dg.dgemm_plan(0, 2304, 2816, 3072, "nk", "f32")["tail_split"] == 2
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("shape,layout", [((1024, 1024, 4096), "nk"), ((1024, 1000, 2048), "kn"),
+                                          ((520, 776, 1600), "nk")])
+def test_split_k_underfilled_tile_exact(shape, layout):
+    """Grids that do not fill the GPU split every tile along K (up to 4
+    segments); the last-arriving warp adds its own accumulator from TMEM to the
+    others' partials."""
+    M, N, K = shape
+    plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
+    assert plan["tail_split"] >= 2 and plan["tail_tiles"] == plan["num_tiles"]
+    got, ref = bf16_case(M, N, K, layout, seed=1000 + K, ws=True)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("M,layout", [(1, "nk"), (16, "nk"), (5, "kn"), (40, "nk"), (64, "kn")])
+def test_split_k_small_m_exact(M, layout):
+    """Small-M (transposed) tiles split along K, with the K groups of each
+    segment inside the segment's range."""
+    N, K = 4096, 4096
+    plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
+    assert plan["swap_ab"] == 1 and plan["tail_split"] >= 2 and plan["k_groups"] > 1
+    got, ref = bf16_case(M, N, K, layout, seed=1100 + M, ws=True)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("M", [1, 48])
+def test_split_k_fp8_small_m_exact(M):
+    N, K = 2048, 8192
+    plan = dg.dgemm_plan(1, M, N, K, "nk", "f32")
+    assert plan["tail_split"] >= 2
+    got, ref = fp8_case(M, N, K, "nk", seed=1200 + M, ws=True)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
