@@ -400,6 +400,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
     }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above (barriers, TMEM, descriptor prefetch) may overlap the
+    // previous kernel in the stream; global memory is touched only from here.
+    grid_dependency_wait();
+    if (threadIdx.x == 0) grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

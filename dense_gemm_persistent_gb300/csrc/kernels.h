@@ -28,8 +28,15 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
     cfg.blockDim = dim3(CF::NUM_THREADS);
     cfg.dynamicSmemBytes = CF::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     unsigned n = 0;
+    if (!cooperative) {
+        // may start while the previous kernel in the stream finishes (the
+        // kernel waits on griddepcontrol before touching global memory)
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     if (CF::PAIR) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
         attr[n].val.clusterDim.x = 2;

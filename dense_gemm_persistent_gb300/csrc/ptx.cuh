@@ -218,6 +218,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this launch depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialization) have completed
+// and their memory operations are visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream (if launched with programmatic stream
+// serialization) begin launching; it still waits for this grid to complete
+// before reading memory.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- CTA pairs (cta_group::2)
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
