@@ -74,6 +74,8 @@ def _load():
             lib.orc_decode.argtypes = [vp, i32, i64, vp]
             lib.orc_dequant.restype = i32
             lib.orc_dequant.argtypes = [vp, i32, i64, i64, vp, i32, vp]
+            lib.orc_dequant_grouped.restype = i32
+            lib.orc_dequant_grouped.argtypes = [vp, i64, i64, vp, i32, i64, vp]
             lib.orc_gemm.restype = i32
             lib.orc_gemm.argtypes = [vp, vp, i32, vp, d, d, i64, i64, i64, i64, i64, vp, i32]
             lib.orc_epilogue.restype = i32
@@ -203,6 +205,22 @@ def dequant(codes: np.ndarray, scale: np.ndarray, axis: int) -> np.ndarray:
     return out
 
 
+def dequant_grouped(codes: np.ndarray, scale: np.ndarray, k_axis: int, group: int) -> np.ndarray:
+    """Decode E4M3 codes and multiply each by the scale of its K group ([W3] §3.2,
+    per-group granularity). ``k_axis`` is the index of ``codes`` that runs along K;
+    ``scale`` is [ceil(K / group), L], L the extent of the other index."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    rows, cols = codes.shape
+    K, L = (cols, rows) if k_axis == 1 else (rows, cols)
+    if scale.shape != (-(-K // group), L):
+        raise ValueError("scale shape")
+    out = np.empty((rows, cols), dtype=np.float64)
+    if _load().orc_dequant_grouped(_ptr(codes), rows, cols, _ptr(scale), int(k_axis), int(group), _ptr(out)) != 0:
+        raise ValueError("bad group or axis")
+    return out
+
+
 def epilogue(X: np.ndarray, bias: np.ndarray | None = None, act: str = "none") -> np.ndarray:
     """y = x + bias[n], then the activation ([W1] §6.1). Returns a new array."""
     X = np.array(X, dtype=np.float64, order="C", copy=True)
@@ -237,6 +255,15 @@ def _row_select(X, rows):
     return X[np.asarray(rows, dtype=np.int64)]
 
 
+def _rows_index(rows, n):
+    """The row indices a (row0, row1) range or an index array selects (None: all n)."""
+    if rows is None:
+        return np.arange(n)
+    if isinstance(rows, tuple):
+        return np.arange(rows[0], rows[1])
+    return np.asarray(rows, dtype=np.int64)
+
+
 def bf16_gemm_ref(A_bits, B_bits, b_layout, C=None, alpha=1.0, beta=0.0, rows=None,
                   nthreads=None) -> np.ndarray:
     """Reference for the BF16 form: inputs are the raw BF16 bit patterns (uint16) the
@@ -252,12 +279,22 @@ def bf16_gemm_ref(A_bits, B_bits, b_layout, C=None, alpha=1.0, beta=0.0, rows=No
 
 
 def fp8_gemm_ref(Aq, Bq, b_layout, a_scale, b_scale, C=None, alpha=1.0, beta=0.0,
-                 bias=None, act="none", rows=None, nthreads=None) -> np.ndarray:
+                 bias=None, act="none", rows=None, nthreads=None, k_group=0) -> np.ndarray:
     """Reference for the FP8 form: D = alpha * diag(sa) (Aq Bq) diag(sb) + beta*C,
-    then + bias and the activation, on the dequantised E4M3 values ([W3] §3.2)."""
-    Ad = dequant(_row_select(Aq, rows), _row_select(a_scale, rows), 0)
+    then + bias and the activation, on the dequantised E4M3 values ([W3] §3.2).
+    With k_group > 0 the scales are per K group: a_scale [G, M] and b_scale
+    [G, N] (G = ceil(K / k_group)), and each code is dequantised with its own
+    group's scale before the plain GEMM."""
+    if k_group:
+        if np.shape(a_scale) != (-(-Aq.shape[1] // k_group), Aq.shape[0]):
+            raise ValueError("a_scale shape")
+        Ad = dequant_grouped(_row_select(Aq, rows), np.asarray(a_scale)[:, _rows_index(rows, Aq.shape[0])],
+                             1, k_group)
+        Bd = dequant_grouped(Bq, b_scale, 1 if b_layout == "nk" else 0, k_group)
+    else:
+        Ad = dequant(_row_select(Aq, rows), _row_select(a_scale, rows), 0)
+        Bd = dequant(Bq, b_scale, 0 if b_layout == "nk" else 1)
     Cs = _row_select(C, rows)
-    Bd = dequant(Bq, b_scale, 0 if b_layout == "nk" else 1)
     Cd = None
     if beta != 0.0:
         Cd = decode_bf16(Cs) if Cs.dtype == np.uint16 else decode(np.asarray(Cs, np.float32), F32)

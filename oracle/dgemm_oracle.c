@@ -139,6 +139,32 @@ int orc_dequant(const void* codes, int type, int64_t rows, int64_t cols,
     return 0;
 }
 
+/* Per-group dequantisation: the scales change along K every `group` elements.
+ * codes is a rows x cols row-major matrix of E4M3 codes; k_axis says which of
+ * its two indices runs along K (1: the column index, as in A [M,K] or B stored
+ * [N,K]; 0: the row index, as in B stored [K,N]). The other index i (a token or
+ * an output channel) selects the scale within a group:
+ *     dst[r][c] = dec(codes[r][c]) * scale[(k / group) * L + i],
+ * with (k, i) = (c, r) when k_axis == 1 and (r, c) when k_axis == 0, and
+ * L = the extent of i. The scale table is group-major: for group j, the L
+ * scales of that K group are contiguous. This is the per-group scale
+ * granularity the FP8 page asks integrators to confirm ([W3] §3.2), as
+ * opposed to one scale per row or channel for the whole of K. */
+int orc_dequant_grouped(const uint8_t* codes, int64_t rows, int64_t cols, const float* scale,
+                        int k_axis, int64_t group, double* dst) {
+    int64_t r, c;
+    const int64_t L = k_axis ? rows : cols;
+    if (group <= 0 || (k_axis != 0 && k_axis != 1)) return -1;
+    if (orc_decode(codes, ORC_E4M3, rows * cols, dst) != 0) return -1;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c) {
+            const int64_t k = k_axis ? c : r;
+            const int64_t i = k_axis ? r : c;
+            dst[r * cols + c] *= (double)scale[(k / group) * L + i];
+        }
+    return 0;
+}
+
 /* out[(i - row0) * N + n] = alpha * sum_k a(i,k) * b(k,n) + beta * c(i,n)
  * for rows i in [row0, row1). [W1] §1.1: C = alpha*A*B + beta*C, A is MxK,
  * B is KxN. b(k,n) is B[k*N + n] when b_nk == 0 (B stored KxN) and B[n*K + k]

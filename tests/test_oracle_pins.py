@@ -256,3 +256,87 @@ def test_requant_rows_invariants():
     idx = np.searchsorted(grid, np.abs(x)).clip(1, 126)
     spacing = grid[idx] - grid[idx - 1]
     assert np.all(np.abs(np.abs(dq) - np.abs(x)) <= spacing / 2 + 1e-12)
+
+
+# ---------------------------------------------------------------- FP8 per-K-group scales
+
+def _int_codes(rng, shape):
+    """E4M3 codes of small integers in [-8, 8] (exact values, exact sums)."""
+    vals = rng.integers(-8, 9, size=shape).astype(np.float64)
+    return oracle.encode_e4m3(vals), vals
+
+
+@pytest.mark.parametrize("b_layout", ["nk", "kn"])
+def test_fp8_grouped_brute_force_ragged_k(b_layout):
+    """Tiny case, written out index by index: K = 7 in groups of 3 (the last group
+    is partial), power-of-two scales, so every product and sum is exact."""
+    rng = np.random.default_rng(21)
+    M, N, K, g = 3, 4, 7, 3
+    G = 3
+    Aq, Av = _int_codes(rng, (M, K))
+    Bq, Bv = _int_codes(rng, (N, K))
+    sa = (2.0 ** rng.integers(-3, 4, size=(G, M))).astype(np.float32)
+    sb = (2.0 ** rng.integers(-3, 4, size=(G, N))).astype(np.float32)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            for k in range(K):
+                want[m, n] += Av[m, k] * sa[k // g, m] * Bv[n, k] * sb[k // g, n]
+    B_in = Bq if b_layout == "nk" else np.ascontiguousarray(Bq.T)
+    got = oracle.fp8_gemm_ref(Aq, B_in, b_layout, sa, sb, k_group=g)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("b_layout", ["nk", "kn"])
+def test_fp8_grouped_is_sum_of_per_group_gemms(b_layout):
+    """Per-group scaling = the sum over K groups of per-row x per-channel scaled
+    GEMMs on that group's K slice (each already pinned above)."""
+    rng = np.random.default_rng(22)
+    M, N, K, g = 10, 12, 40, 16
+    G = 3
+    Aq, _ = _int_codes(rng, (M, K))
+    Bq, _ = _int_codes(rng, (N, K))
+    sa = (2.0 ** rng.integers(-4, 5, size=(G, M))).astype(np.float32)
+    sb = (2.0 ** rng.integers(-4, 5, size=(G, N))).astype(np.float32)
+    want = np.zeros((M, N))
+    for j in range(G):
+        ks = slice(j * g, min(K, (j + 1) * g))
+        want += oracle.fp8_gemm_ref(np.ascontiguousarray(Aq[:, ks]), np.ascontiguousarray(Bq[:, ks]), "nk",
+                                    sa[j], sb[j])
+    B_in = Bq if b_layout == "nk" else np.ascontiguousarray(Bq.T)
+    got = oracle.fp8_gemm_ref(Aq, B_in, b_layout, sa, sb, k_group=g)
+    assert np.array_equal(got, want)
+    # rows of the result are the GEMM on those rows of A (and of a_scale's columns)
+    part = oracle.fp8_gemm_ref(Aq, B_in, b_layout, sa, sb, k_group=g, rows=np.array([7, 2]))
+    assert np.array_equal(part, got[[7, 2]])
+
+
+def test_fp8_grouped_constant_scales_reduce_to_per_row():
+    """Scales equal across K groups give the per-row x per-channel result exactly;
+    a group size >= K is one group."""
+    rng = np.random.default_rng(23)
+    Aq, _ = _int_codes(rng, (5, 64))
+    Bq, _ = _int_codes(rng, (7, 64))
+    sa = rng.uniform(0.5, 2, size=5).astype(np.float32)
+    sb = rng.uniform(0.5, 2, size=7).astype(np.float32)
+    plain = oracle.fp8_gemm_ref(Aq, Bq, "nk", sa, sb)
+    grouped = oracle.fp8_gemm_ref(Aq, Bq, "nk", np.tile(sa, (4, 1)), np.tile(sb, (4, 1)), k_group=16)
+    assert np.allclose(grouped, plain, rtol=1e-14, atol=0)
+    one = oracle.fp8_gemm_ref(Aq, Bq, "nk", sa[None, :], sb[None, :], k_group=64)
+    assert np.array_equal(one, plain)
+    with pytest.raises(ValueError):   # a scale table of the wrong orientation
+        oracle.fp8_gemm_ref(Aq, Bq, "nk", np.tile(sa, (4, 1)).T.copy(), np.tile(sb, (4, 1)), k_group=16)
+
+
+def test_fp8_grouped_scale_layout_is_group_major():
+    """All-ones codes, scale (j, i) = distinct powers: entry (m, n) is
+    sum_j |group j| * sa[j, m] * sb[j, n], which a [L, G] table would not give."""
+    M, N, K, g = 2, 3, 10, 4
+    Aq = np.full((M, K), 0x38, np.uint8)   # 1.0
+    Bq = np.full((N, K), 0x38, np.uint8)
+    sa = np.array([[1, 2], [4, 8], [16, 32]], np.float32)          # [G=3, M=2]
+    sb = np.array([[1, 3, 5], [7, 9, 11], [13, 15, 17]], np.float32)   # [G=3, N=3]
+    sizes = np.array([4, 4, 2], np.float64)
+    want = np.einsum("j,jm,jn->mn", sizes, sa.astype(np.float64), sb.astype(np.float64))
+    assert np.array_equal(oracle.fp8_gemm_ref(Aq, Bq, "nk", sa, sb, k_group=g), want)
+    assert want[0, 0] == 4 * 1 * 1 + 4 * 4 * 7 + 2 * 16 * 13

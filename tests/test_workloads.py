@@ -51,3 +51,17 @@ def test_fp8_quantisation_recipe():
     # per-channel weight scales near 0.02 * (max |N(0,1)| over K) / 448
     sw = w.b_scale.numpy()
     assert np.all((sw > 0.02 * 2 / 448) & (sw < 0.02 * 6 / 448))
+
+
+def test_grouped_quantisation_scales_per_group():
+    w = wl.fp8_grouped(32, 24, 300, k_group=128, seed=3)
+    assert tuple(w.a_scale.shape) == (3, 32) and tuple(w.b_scale.shape) == (3, 24)
+    assert tuple(w.B.shape) == (24, 300) and w.k_group == 128
+    a = w.A.to(torch.float32).numpy()
+    # each (row, group) slice has its amax at the largest finite code, 448
+    for j, ks in enumerate((slice(0, 128), slice(128, 256), slice(256, 300))):
+        assert np.allclose(np.abs(a[:, ks]).max(axis=1), 448.0)
+    # the scales differ from group to group (the recipe's per-group magnitudes)
+    assert (w.a_scale[0] != w.a_scale[1]).any()
+    kn = wl.fp8_grouped(32, 24, 300, k_group=128, seed=3, b_layout="kn")
+    assert torch.equal(kn.B.view(torch.uint8), w.B.view(torch.uint8).t())

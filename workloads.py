@@ -50,6 +50,7 @@ class Workload:
     act: str = "none"
     d_dtype: str = "bf16"        # "f32" | "bf16" | "e4m3"
     out_quant: str = "none"      # "none" | "e4m3_row_amax"
+    k_group: int = 0             # FP8: 0 = one scale per row / channel; g > 0 = one per K group of g
     seed: int = 0
     extras: dict = field(default_factory=dict)
 
@@ -81,6 +82,24 @@ def quantize_e4m3_rows(X: np.ndarray):
     s[s == 0] = 1.0
     q = torch.from_numpy(X32 / s[:, None]).to(torch.float8_e4m3fn)
     return q, torch.from_numpy(s)
+
+
+def quantize_e4m3_groups(X: np.ndarray, group: int):
+    """E4M3 codes of X [rows, K] with one FP32 scale per (row, K group of
+    ``group`` columns), s = amax / 448 over that slice. Scales come back
+    group-major, [ceil(K / group), rows]."""
+    X32 = np.ascontiguousarray(X, dtype=np.float32)
+    rows, K = X32.shape
+    G = -(-K // group)
+    s = np.empty((G, rows), dtype=np.float32)
+    Y = np.empty_like(X32)
+    for j in range(G):
+        sl = X32[:, j * group:(j + 1) * group]
+        sj = (np.abs(sl).max(axis=1, initial=0.0) / np.float32(E4M3_MAX)).astype(np.float32)
+        sj[sj == 0] = 1.0
+        s[j] = sj
+        Y[:, j * group:(j + 1) * group] = sl / sj[:, None]
+    return torch.from_numpy(Y).to(torch.float8_e4m3fn), torch.from_numpy(s)
 
 
 def _log_uniform_rows(rng, M, lo=0.1, hi=10.0):
@@ -140,6 +159,28 @@ def config5(M=8192, N=8192, K=8192, seed=None) -> Workload:
     return Workload(5, f"fp8 {M}x{N}x{K} + bias -> SiLU -> E4M3 row requant", "fp8", M, N, K,
                     "nk", A=Xq, B=Wq, a_scale=sx, b_scale=sw, bias=bias, act="silu",
                     d_dtype="e4m3", out_quant="e4m3_row_amax", seed=seed)
+
+
+def fp8_grouped(M=4096, N=11008, K=4096, k_group=128, b_layout="nk", seed=None, d_dtype="bf16") -> Workload:
+    """FP8 GEMM with per-K-group scales: the workload 3 recipe, with an extra
+    log-uniform magnitude per (token, K group) in [0.1, 10] on the activations
+    and per (channel, K group) in [0.5, 2] on the weights, so neighbouring
+    groups get different scales. a_scale [G, M], b_scale [G, N]."""
+    seed = 1003 if seed is None else seed
+    rng = np.random.default_rng(seed)
+    G = -(-K // k_group)
+    tx = np.exp(rng.uniform(math.log(0.1), math.log(10.0), size=(M, G))).astype(np.float32)
+    tw = np.exp(rng.uniform(math.log(0.5), math.log(2.0), size=(N, G))).astype(np.float32)
+    cols = np.arange(K) // k_group
+    X = rng.standard_normal((M, K), dtype=np.float32) * _log_uniform_rows(rng, M) * tx[:, cols]
+    W = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02) * tw[:, cols]
+    Xq, sx = quantize_e4m3_groups(X, k_group)
+    Wq, sw = quantize_e4m3_groups(W, k_group)
+    if b_layout == "kn":
+        Wq = Wq.t().contiguous()
+    return Workload(3, f"fp8 {M}x{N}x{K} per-{k_group}-K-group scales -> {d_dtype}", "fp8", M, N, K,
+                    b_layout, A=Xq, B=Wq, a_scale=sx, b_scale=sw, d_dtype=d_dtype, k_group=k_group,
+                    seed=seed)
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
