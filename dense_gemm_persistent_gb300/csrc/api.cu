@@ -40,19 +40,21 @@ std::atomic<unsigned char> g_attr_set[64][kMaxDevices];
 std::once_flag g_kernels_once;
 
 void collect_kernels() {
-    int n1 = 0, n2 = 0;
+    int n1 = 0, n2 = 0, n3 = 0;
     const dg::KernelInfo* t1 = dg::kernels_bf16(&n1);
     const dg::KernelInfo* t2 = dg::kernels_fp8(&n2);
+    const dg::KernelInfo* t3 = dg::kernels_fp8_grouped(&n3);
     for (int i = 0; i < n1 && g_nk < 64; ++i) g_kernels[g_nk++] = &t1[i];
     for (int i = 0; i < n2 && g_nk < 64; ++i) g_kernels[g_nk++] = &t2[i];
+    for (int i = 0; i < n3 && g_nk < 64; ++i) g_kernels[g_nk++] = &t3[i];
 }
 
-int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode, int pair) {
+int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode, int pair, int gs) {
     std::call_once(g_kernels_once, collect_kernels);
     for (int i = 0; i < g_nk; ++i) {
         const dg::KernelInfo* k = g_kernels[i];
         if (k->bn == bn && k->fp8 == fp8 && k->a_mn == a_mn && k->b_mn == b_mn && k->mode == mode &&
-            k->pair == pair)
+            k->pair == pair && k->gs == gs)
             return i;
     }
     return -1;
@@ -104,6 +106,8 @@ struct Plan {
     int64_t Mm, Nm;    // problem in the MMA's orientation
     int bk;            // K elements per stage
     int acc_stride;    // TMEM columns between the two accumulator buffers
+    int gs;            // per-K-group scales (group_kb K slices per group)
+    int group_kb;
     int dp_tiles, split, tail_items;   // tail splitting (MODE_TILE)
     size_t tail_count_bytes;           // workspace: per-warp arrival counters
 };
@@ -111,8 +115,9 @@ struct Plan {
 // Validates the sizes, enums and epilogue; picks the kernel variant and grid.
 // Pure host logic: needs no GPU.
 dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t bl, dgemm_dtype_t d_dtype,
-                         const dgemm_epilogue_t* epi, int num_sms, int max_pairs, bool allow_split, Plan* out) {
-    if (M < 0 || N < 0 || K < 0 || num_sms <= 0) return DGEMM_ERR_INVALID_VALUE;
+                         const dgemm_epilogue_t* epi, int num_sms, int max_pairs, bool allow_split, Plan* out,
+                         int k_group = 0) {
+    if (M < 0 || N < 0 || K < 0 || num_sms <= 0 || k_group < 0) return DGEMM_ERR_INVALID_VALUE;
     if (bl != DGEMM_B_KN && bl != DGEMM_B_NK) return DGEMM_ERR_INVALID_VALUE;
     if (d_dtype != DGEMM_F32 && d_dtype != DGEMM_BF16 && d_dtype != DGEMM_E4M3) return DGEMM_ERR_INVALID_VALUE;
     const int act = epi ? epi->act : DGEMM_ACT_NONE;
@@ -128,8 +133,15 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     if (bl == DGEMM_B_KN && (static_cast<size_t>(N) * esz) % 16 != 0) return DGEMM_ERR_MISALIGNED;
     if ((static_cast<size_t>(N) * dtype_bytes(d_dtype)) % 16 != 0) return DGEMM_ERR_MISALIGNED;
 
+    // Per-K-group scales: groups of whole K slices (128 E4M3 values), no
+    // requantising epilogue.
+    const int gs = k_group > 0 ? 1 : 0;
+    if (gs && (!fp8 || k_group % 128 != 0 || oq != DGEMM_QUANT_NONE)) return DGEMM_ERR_NOT_SUPPORTED;
+
     Plan p{};
     p.bk = static_cast<int>(128 / esz);
+    p.gs = gs;
+    p.group_kb = gs ? k_group / p.bk : 0;
     const bool swap = (oq == DGEMM_QUANT_NONE) && M <= 64;
     const char* pair_env = std::getenv("DGEMM_CTA_PAIR");  // "0" disables, "1" forces CTA pairs (tests, sweeps)
     const bool pairs_ok = max_pairs > 0 && !(pair_env && pair_env[0] == '0');
@@ -185,16 +197,16 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     // exercise every variant in tests and for tuning sweeps).
     if (const char* f = std::getenv("DGEMM_TILE_N")) {
         const int v = std::atoi(f);
-        if (v != bn && find_kernel(v, fp8, p.a_mn, p.b_mn, p.mode, 0) >= 0) {
+        if (v != bn && find_kernel(v, fp8, p.a_mn, p.b_mn, p.mode, 0, gs) >= 0) {
             bn = v;
             pair = 0;
         }
     }
     // DGEMM_CTA_PAIR=1 forces the CTA-pair variant when one exists for this tile.
     if (pair_env && pair_env[0] == '1' && !swap && M > 128 && max_pairs > 0 &&
-        find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, 1) >= 0)
+        find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, 1, gs) >= 0)
         pair = 1;
-    p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair);
+    p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair, gs);
     if (p.kernel < 0) return DGEMM_ERR_NOT_SUPPORTED;
     const dg::KernelInfo* k = g_kernels[p.kernel];
     const int tile_m = pair ? 256 : 128;
@@ -262,7 +274,9 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     // tensor core's round-toward-zero accumulation error by about that factor.
     int groups = 1;
     p.acc_stride = bn;
-    if (p.mode == dg::MODE_SWAP) {
+    if (gs) {
+        groups = static_cast<int>((K + k_group - 1) / k_group);  // scale groups (two buffers alternate)
+    } else if (p.mode == dg::MODE_SWAP) {
         const bool one_tile = p.pub.num_tiles <= p.pub.grid;  // (no pairs in this mode)
         const int max_groups = (one_tile ? 512 : 256) / bn;
         groups = static_cast<int>(k_blocks < max_groups ? (k_blocks > 0 ? k_blocks : 1) : max_groups);
@@ -326,7 +340,15 @@ cudaError_t configure_kernel(int kernel, int devid) {
     std::atomic<unsigned char>& flag = g_attr_set[kernel][devid];
     if (flag.load(std::memory_order_acquire)) return cudaSuccess;
     const dg::KernelInfo* k = g_kernels[kernel];
-    const cudaError_t e = cudaFuncSetAttribute(k->func, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes);
+    cudaError_t e = cudaFuncSetAttribute(k->func, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes);
+    if (e == cudaSuccess && k->launch_regs > 0) {
+        // A kernel that moves registers between warpgroups must be launched
+        // with at least the registers its split adds up to, or the raising
+        // warpgroups would wait forever: refuse to launch it otherwise.
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, k->func);
+        if (e == cudaSuccess && fa.numRegs < k->launch_regs) e = cudaErrorInvalidConfiguration;
+    }
     if (e == cudaSuccess) flag.store(1, std::memory_order_release);
     return e;
 }
@@ -373,10 +395,10 @@ CUtensorMapDataType tm_type(dgemm_dtype_t t) {
 dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, const float* a_scale,
                    const float* b_scale, const void* C, dgemm_dtype_t c_dtype, void* D, dgemm_dtype_t d_dtype,
                    int64_t M, int64_t N, int64_t K, float alpha, float beta, const dgemm_epilogue_t* epi, void* ws,
-                   size_t ws_bytes, cudaStream_t stream) {
+                   size_t ws_bytes, cudaStream_t stream, int k_group = 0) {
     // ---- arguments that need no device
     Plan plan;
-    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, false, &plan);
+    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, false, &plan, k_group);
     if (st != DGEMM_OK) return st;
     if (M == 0 || N == 0) return DGEMM_OK;
     if (!D || (K > 0 && (!A || !B))) return DGEMM_ERR_INVALID_VALUE;
@@ -403,10 +425,10 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     st = device_state(&dev, &devid);
     if (st != DGEMM_OK) return st;
     const int pairs = max_pairs(dev, devid, fp8);
-    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, true, &plan);
+    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, true, &plan, k_group);
     if (st != DGEMM_OK) return st;
     if (plan.split > 1 && (!ws || ws_bytes < plan.pub.workspace_bytes)) {
-        st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, false, &plan);  // no room: whole tiles
+        st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, false, &plan, k_group);  // no room: whole tiles
         if (st != DGEMM_OK) return st;
     }
     const dg::KernelInfo* k = g_kernels[plan.kernel];
@@ -458,7 +480,7 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.num_tiles = plan.pub.num_tiles;
     p.k_blocks = static_cast<int>((K + plan.bk - 1) / plan.bk);
     p.group_m = plan.pub.raster_group;
-    p.acc_groups = plan.pub.k_groups;
+    p.acc_groups = plan.gs ? 1 : plan.pub.k_groups;
     p.acc_stride = plan.acc_stride;
     p.alpha = alpha;
     p.beta = beta;
@@ -468,8 +490,17 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.D = D;
     p.ldd = N;
     p.d_f32 = d_dtype == DGEMM_F32;
-    p.row_scale = plan.pub.swap_ab ? b_scale : a_scale;
-    p.col_scale = plan.pub.swap_ab ? a_scale : b_scale;
+    if (plan.gs) {
+        // group-major tables: a_scale [G][M], b_scale [G][N]
+        p.row_gscale = plan.pub.swap_ab ? b_scale : a_scale;
+        p.col_gscale = plan.pub.swap_ab ? a_scale : b_scale;
+        p.gs_ld_row = plan.Mm;
+        p.gs_ld_col = plan.Nm;
+        p.group_kb = plan.group_kb;
+    } else {
+        p.row_scale = plan.pub.swap_ab ? b_scale : a_scale;
+        p.col_scale = plan.pub.swap_ab ? a_scale : b_scale;
+    }
     p.bias = bias;
     p.act = epi ? epi->act : 0;
     p.status = dev->status;
@@ -510,9 +541,8 @@ dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t
                                 const float* b_scale, int k_group, const void* C, dgemm_dtype_t c_dtype, void* D,
                                 dgemm_dtype_t d_dtype, int64_t M, int64_t N, int64_t K, float alpha, float beta,
                                 const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes, dgemm_stream_t stream) {
-    if (k_group != 0) return k_group < 0 ? DGEMM_ERR_INVALID_VALUE : DGEMM_ERR_NOT_SUPPORTED;
     return run(1, Aq, Bq, b_layout, a_scale, b_scale, C, c_dtype, D, d_dtype, M, N, K, alpha, beta, epi, ws,
-               ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+               ws_bytes, reinterpret_cast<cudaStream_t>(stream), k_group);
 }
 
 size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,

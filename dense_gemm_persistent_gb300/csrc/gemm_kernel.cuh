@@ -68,6 +68,13 @@ struct Params {
     int d_f32;      // 1: D is FP32, 0: BF16 (MODE_TILE / MODE_SWAP)
     const float* row_scale;  // per MMA row, or null
     const float* col_scale;  // per MMA column, or null
+    // Per-K-group scales (GS kernels): in K group j (group_kb K slices), MMA
+    // row r and column c are scaled by row_gscale[j * gs_ld_row + r] *
+    // col_gscale[j * gs_ld_col + c] before the groups are summed.
+    const float* row_gscale;
+    const float* col_gscale;
+    int64_t gs_ld_row, gs_ld_col;
+    int group_kb;
     const float* bias;       // per output channel, or null
     int act;                 // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
     // MODE_ROWQ
@@ -117,7 +124,7 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
 
 
 
-template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false>
+template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false, bool GS_ = false>
 struct Cfg {
     static constexpr int BM = 128;                // accumulator rows per CTA
     static constexpr bool PAIR = PAIR_;
@@ -128,6 +135,9 @@ struct Cfg {
     static constexpr bool A_MN = A_MN_;
     static constexpr bool B_MN = B_MN_;
     static constexpr int MODE = MODE_;
+    // Per-K-group scales: each group's product goes to one of two TMEM
+    // buffers and the epilogue warps fold it, scaled, into FP32 registers.
+    static constexpr bool GS = GS_;
     static constexpr int ESZ = FP8 ? 1 : 2;       // operand bytes
     static constexpr int BK = 128 / ESZ;          // K elements per stage (128 bytes)
     static constexpr int UMMA_K = 32 / ESZ;       // K elements per MMA (32 bytes)
@@ -142,22 +152,41 @@ struct Cfg {
     static constexpr int EPI_WARPS = (MODE == MODE_SWAP || BN < 128) ? 4 : 8;
     static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);   // columns per epilogue warp
     static constexpr int STAGING_BYTES = (MODE == MODE_SWAP) ? 0 : EPI_WARPS * 4096;  // one 4 KB box each
+    // Per-K-group column scales, staged in shared memory two groups ahead:
+    // three buffers of EPI_COLS floats per epilogue warp (tile modes; the
+    // small-M form reads its few column scales directly).
+    static constexpr bool GS_SMEM = GS && MODE != MODE_SWAP;
+    static constexpr int GS_BUFS = 3;
+    static constexpr int GS_BYTES = GS_SMEM ? EPI_WARPS * GS_BUFS * EPI_COLS * 4 : 0;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_LIMIT = 232448;  // 227 KB opt-in maximum per CTA
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - STAGING_BYTES - GS_BYTES - BAR_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
-    static constexpr int TMEM_COLS = (MODE == MODE_SWAP) ? 512
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + GS_BYTES + BAR_BYTES;
+    static constexpr int TMEM_COLS = (MODE == MODE_SWAP && !GS) ? 512
                                    : (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr uint32_t IDESC = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, TILE_M, BN);
-    static constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+    // Per-K-group scales keep each epilogue thread's share of the running sum
+    // (EPI_COLS FP32 values) in registers. With 8 epilogue warps that needs more
+    // than the 168 registers a thread of a 10-warp block can have, so those
+    // kernels run 12 warps as three warpgroups -- producer, MMA issuer and two
+    // idle warps, then the 8 epilogue warps -- and move registers from the
+    // first warpgroup to the others (setmaxnreg).
+    static constexpr bool REG_SPLIT = GS && EPI_WARPS == 8;
+    static constexpr int EPI_WARP0 = REG_SPLIT ? 4 : 2;     // first epilogue warp
+    static constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+    static constexpr int LAUNCH_REGS = 168;   // per thread at launch (12 warps: 3 per SM sub-partition)
+    static constexpr int REGS_LOW = 56, REGS_HIGH = 224;
+    static_assert(!REG_SPLIT || 128 * REGS_LOW + 32 * EPI_WARPS * REGS_HIGH <= NUM_THREADS * LAUNCH_REGS,
+                  "register split exceeds the launch allocation");
 
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
     static_assert(!B_MN || BN_CTA % MN_ATOM == 0, "MN-major B needs whole 128-byte atoms");
     static_assert(!PAIR || (MODE != MODE_SWAP && !A_MN && BN == 256), "CTA pairs: 256 x 256 tiles");
     static_assert(MODE == MODE_SWAP || EPI_COLS % 64 == 0, "tile epilogue works in 64-column boxes");
     static_assert(STAGES >= 2, "pipeline depth");
+    static_assert(!GS || (FP8 && MODE != MODE_ROWQ), "per-K-group scales: FP8, tile or small-M form");
     static_assert(BN < 32 || BN % 32 == 0, "epilogue reads 32-column units");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
 };
@@ -213,6 +242,39 @@ __device__ __forceinline__ float4 ld_bcast4(const float* base, int idx, int n) {
     r.z = idx + 2 < n ? __ldg(base + idx + 2) : 0.0f;
     r.w = 0.0f;
     return r;
+}
+
+// Per-K-group scales: sum[c] += P[c] * rs * s[c] for the UNIT columns of one
+// Tensor Memory load, in packed FP32 pairs.
+__device__ __forceinline__ void gs_fold4(float* sum, const uint32_t* r, float rs, float4 s) {
+    float w0, w1, w2, w3;
+    fmul2(w0, w1, s.x, s.y, rs, rs);
+    fmul2(w2, w3, s.z, s.w, rs, rs);
+    ffma2(sum[0], sum[1], __uint_as_float(r[0]), __uint_as_float(r[1]), w0, w1);
+    ffma2(sum[2], sum[3], __uint_as_float(r[2]), __uint_as_float(r[3]), w2, w3);
+}
+
+// Column scales from a shared-memory copy of this warp's columns (broadcast reads).
+template <int UNIT>
+__device__ __forceinline__ void gs_fold_smem(float* sum, const uint32_t (&r)[UNIT], float rs, const float* cs) {
+#pragma unroll
+    for (int c = 0; c < UNIT; c += 4) gs_fold4(sum + c, r + c, rs, *reinterpret_cast<const float4*>(cs + c));
+}
+
+// Column scales read from global memory one by one (the small-M form, whose
+// column scale table has any row length); columns at or beyond ncols get 0.
+template <int UNIT>
+__device__ __forceinline__ void gs_fold(float* sum, const uint32_t (&r)[UNIT], float rs, const float* cs, int col,
+                                        int ncols) {
+#pragma unroll
+    for (int c = 0; c < UNIT; c += 4) {
+        float4 s;
+        s.x = col + c < ncols ? __ldg(cs + col + c) : 0.0f;
+        s.y = col + c + 1 < ncols ? __ldg(cs + col + c + 1) : 0.0f;
+        s.z = col + c + 2 < ncols ? __ldg(cs + col + c + 2) : 0.0f;
+        s.w = col + c + 3 < ncols ? __ldg(cs + col + c + 3) : 0.0f;
+        gs_fold4(sum + c, r + c, rs, s);
+    }
 }
 
 // The FP32 epilogue arithmetic shared by all modes for 32 consecutive columns
@@ -342,7 +404,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     uint8_t* staging = smem + S * CF::STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + CF::STAGING_BYTES);
+    float* gs_cols = reinterpret_cast<float*>(staging + CF::STAGING_BYTES);   // GS column-scale buffers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + CF::STAGING_BYTES + CF::GS_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
     uint64_t* acc_full = bars + 2 * S;
@@ -405,132 +468,109 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
     grid_dependency_wait();
     if (threadIdx.x == 0) grid_launch_dependents();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_last();
-            uint32_t stage = 0, phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            Work w;
-            for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it) {
-                int mb, nb;
-                tile_coords(w.tile, p, mb, nb);
-                const int row0 = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM;   // this CTA's A rows
-                const int col0 = nb * CF::BN + static_cast<int>(rank) * CF::BN_CTA;  // this CTA's B rows
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sa = stages + stage * CF::STAGE_BYTES;
-                    uint8_t* sb = sa + CF::A_BYTES;
-                    const int k0 = kb * CF::BK;
-                    if constexpr (CF::PAIR) {
-                        // both CTAs' copies complete on the leader's full barrier
-                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], CF::CTAS * CF::STAGE_BYTES);
-                        const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-                        tma_load_2d_pair(sa, &tmA, fb, k0, row0, pol);
-                        if constexpr (CF::B_MN) {
-#pragma unroll
-                            for (int i = 0; i < CF::BN_CTA / CF::MN_ATOM; ++i)
-                                tma_load_2d_pair(sb + i * CF::BK * 128, &tmB, fb, col0 + i * CF::MN_ATOM, k0, pol);
-                        } else {
-                            tma_load_2d_pair(sb, &tmB, fb, k0, col0, pol);
+    if (warp < CF::EPI_WARP0) {
+        // Register reallocation happens once per warpgroup, at one point in
+        // each role's branch (the code after it is compiled to that count).
+        if constexpr (CF::REG_SPLIT) regs_dec<CF::REGS_LOW>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                const uint64_t pol = policy_evict_last();
+                uint32_t stage = 0, phase = 0;
+                int64_t issued = 0;
+                bool ok = true;
+                Work w;
+                for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it) {
+                    int mb, nb;
+                    tile_coords(w.tile, p, mb, nb);
+                    const int row0 = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM;   // this CTA's A rows
+                    const int col0 = nb * CF::BN + static_cast<int>(rank) * CF::BN_CTA;  // this CTA's B rows
+                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
                         }
-                    } else {
-                        mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
-                        if constexpr (CF::A_MN) {
-#pragma unroll
-                            for (int i = 0; i < CF::BM / CF::MN_ATOM; ++i)
-                                tma_load_2d(sa + i * CF::BK * 128, &tmA, &full[stage], row0 + i * CF::MN_ATOM, k0,
-                                            pol);
+                        uint8_t* sa = stages + stage * CF::STAGE_BYTES;
+                        uint8_t* sb = sa + CF::A_BYTES;
+                        const int k0 = kb * CF::BK;
+                        if constexpr (CF::PAIR) {
+                            // both CTAs' copies complete on the leader's full barrier
+                            if (rank == 0) mbar_arrive_expect_tx(&full[stage], CF::CTAS * CF::STAGE_BYTES);
+                            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+                            tma_load_2d_pair(sa, &tmA, fb, k0, row0, pol);
+                            if constexpr (CF::B_MN) {
+    #pragma unroll
+                                for (int i = 0; i < CF::BN_CTA / CF::MN_ATOM; ++i)
+                                    tma_load_2d_pair(sb + i * CF::BK * 128, &tmB, fb, col0 + i * CF::MN_ATOM, k0, pol);
+                            } else {
+                                tma_load_2d_pair(sb, &tmB, fb, k0, col0, pol);
+                            }
                         } else {
-                            tma_load_2d(sa, &tmA, &full[stage], k0, row0, pol);
+                            mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
+                            if constexpr (CF::A_MN) {
+    #pragma unroll
+                                for (int i = 0; i < CF::BM / CF::MN_ATOM; ++i)
+                                    tma_load_2d(sa + i * CF::BK * 128, &tmA, &full[stage], row0 + i * CF::MN_ATOM, k0,
+                                                pol);
+                            } else {
+                                tma_load_2d(sa, &tmA, &full[stage], k0, row0, pol);
+                            }
+                            if constexpr (CF::B_MN) {
+    #pragma unroll
+                                for (int i = 0; i < CF::BN_CTA / CF::MN_ATOM; ++i)
+                                    tma_load_2d(sb + i * CF::BK * 128, &tmB, &full[stage], col0 + i * CF::MN_ATOM, k0,
+                                                pol);
+                            } else {
+                                tma_load_2d(sb, &tmB, &full[stage], k0, col0, pol);
+                            }
                         }
-                        if constexpr (CF::B_MN) {
-#pragma unroll
-                            for (int i = 0; i < CF::BN_CTA / CF::MN_ATOM; ++i)
-                                tma_load_2d(sb + i * CF::BK * 128, &tmB, &full[stage], col0 + i * CF::MN_ATOM, k0,
-                                            pol);
-                        } else {
-                            tma_load_2d(sb, &tmB, &full[stage], k0, col0, pol);
+                        ++issued;
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1;
                         }
                     }
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
+                }
+                if (!ok) raise_error(p, ERR_TIMEOUT_PRODUCER, abort_flag);
+                // Drain: every copy this thread issued must have landed before the
+                // CTA can exit (normally these waits return at once). The peer of a
+                // pair signals the leader's full barriers, so it waits instead for
+                // the MMA's release of its last use of each stage.
+                for (int s = 0; s < S; ++s) {
+                    const int64_t cnt = issued > s ? (issued - s + S - 1) / S : 0;
+                    uint64_t* bar = (CF::PAIR && rank != 0) ? &empty[s] : &full[s];
+                    if (cnt > 0 && !mbar_wait(bar, static_cast<uint32_t>((cnt - 1) & 1), nullptr))
+                        raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
                 }
             }
-            if (!ok) raise_error(p, ERR_TIMEOUT_PRODUCER, abort_flag);
-            // Drain: every copy this thread issued must have landed before the
-            // CTA can exit (normally these waits return at once). The peer of a
-            // pair signals the leader's full barriers, so it waits instead for
-            // the MMA's release of its last use of each stage.
-            for (int s = 0; s < S; ++s) {
-                const int64_t cnt = issued > s ? (issued - s + S - 1) / S : 0;
-                uint64_t* bar = (CF::PAIR && rank != 0) ? &empty[s] : &full[s];
-                if (cnt > 0 && !mbar_wait(bar, static_cast<uint32_t>((cnt - 1) & 1), nullptr))
-                    raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && rank == 0) {
-            // The tensor core's instruction queue is shallow (issue time equals
-            // execution time), so this loop must spend almost nothing between
-            // MMAs: descriptors are built once and advanced by additions, and
-            // K-group boundaries are tracked incrementally (a division per K
-            // slice here measurably starves the tensor pipe).
-            const uint32_t s0 = smem_u32(stages);
-            const uint64_t a_desc0 = smem_desc_sw128(s0, CF::A_MN ? CF::BK * 128 : 16, 1024);
-            const uint64_t b_desc0 = smem_desc_sw128(s0 + CF::A_BYTES, CF::B_MN ? CF::BK * 128 : 16, 1024);
-            constexpr uint32_t A_KSTEP = (CF::A_MN ? CF::UMMA_K * 128 : 32) >> 4;
-            constexpr uint32_t B_KSTEP = (CF::B_MN ? CF::UMMA_K * 128 : 32) >> 4;
-            constexpr uint32_t STAGE_STEP = CF::STAGE_BYTES >> 4;
-            const int kblocks = p.k_blocks, ngroups = p.acc_groups;
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            int local = 0;
-            Work w;
-            for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it, ++local) {
-                const int buf = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
-                if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t acc_base = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
-                // group g covers K slices [ceil(g*KB/G), ceil((g+1)*KB/G))
-                int group = 0;
-                int next_group_start = w.kb1;
-                if (ngroups > 1) {   // a K segment may start inside the groups
-                    group = (w.kb0 * ngroups) / kblocks;
-                    next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
-                }
-                uint32_t d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    bool first_in_group = (kb == w.kb0);
-                    if (kb == next_group_start) {
-                        ++group;
-                        first_in_group = true;
-                        next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
-                        d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
-                    }
-                    const uint64_t ad = a_desc0 + stage * STAGE_STEP;
-                    const uint64_t bd = b_desc0 + stage * STAGE_STEP;
-#pragma unroll
+            __syncwarp();
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0 && rank == 0) {
+                // The tensor core's instruction queue is shallow (issue time equals
+                // execution time), so this loop must spend almost nothing between
+                // MMAs: descriptors are built once and advanced by additions, and
+                // K-group boundaries are tracked incrementally (a division per K
+                // slice here measurably starves the tensor pipe).
+                const uint32_t s0 = smem_u32(stages);
+                const uint64_t a_desc0 = smem_desc_sw128(s0, CF::A_MN ? CF::BK * 128 : 16, 1024);
+                const uint64_t b_desc0 = smem_desc_sw128(s0 + CF::A_BYTES, CF::B_MN ? CF::BK * 128 : 16, 1024);
+                constexpr uint32_t A_KSTEP = (CF::A_MN ? CF::UMMA_K * 128 : 32) >> 4;
+                constexpr uint32_t B_KSTEP = (CF::B_MN ? CF::UMMA_K * 128 : 32) >> 4;
+                constexpr uint32_t STAGE_STEP = CF::STAGE_BYTES >> 4;
+                const int kblocks = p.k_blocks, ngroups = p.acc_groups;
+                uint32_t stage = 0, phase = 0;
+                bool ok = true;
+                int local = 0;
+                Work w;
+                // The MMAs of one K slice (a pipeline stage) into accumulator d_tmem;
+                // `first` starts a fresh accumulation.
+                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first) {
+                    const uint64_t ad = a_desc0 + st * STAGE_STEP;
+                    const uint64_t bd = b_desc0 + st * STAGE_STEP;
+    #pragma unroll
                     for (int k = 0; k < CF::BK / CF::UMMA_K; ++k) {
-                        const uint32_t acc = (!first_in_group || k > 0) ? 1u : 0u;
+                        const uint32_t acc = (!first || k > 0) ? 1u : 0u;
                         if constexpr (CF::PAIR) {
                             if constexpr (CF::FP8)
                                 mma_f8_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
@@ -545,34 +585,111 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     }
                     // the stage is free (in both CTAs of a pair) once these MMAs have read it
                     if constexpr (CF::PAIR)
-                        mma_commit_pair(&empty[stage], 3);
+                        mma_commit_pair(&empty[st], 3);
                     else
-                        mma_commit(&empty[stage]);
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1;
+                        mma_commit(&empty[st]);
+                };
+                if constexpr (CF::GS) {
+                    // Per-K-group scales: every scale group of every work item gets
+                    // its own accumulator, alternating between the two TMEM buffers
+                    // (gcount counts groups over the whole loop, so the epilogue can
+                    // fold one group while the next is computed).
+                    int gcount = 0;
+                    for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it) {
+                        int kin = w.kb1 > w.kb0 ? w.kb0 % p.group_kb : 0;   // position inside the group
+                        uint32_t d_tmem = tmem_base;
+                        int gb = 0;
+                        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                            const bool first = (kb == w.kb0) || kin == 0;
+                            if (first) {
+                                gb = gcount & 1;
+                                if (!mbar_wait(&acc_empty[gb], ((gcount >> 1) & 1) ^ 1, abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                d_tmem = tmem_base + static_cast<uint32_t>(gb * p.acc_stride);
+                            }
+                            if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_stage(d_tmem, stage, first);
+                            if (++stage == S) {
+                                stage = 0;
+                                phase ^= 1;
+                            }
+                            if (++kin == p.group_kb || kb + 1 == w.kb1) {
+                                // the group's product is ready for the epilogue
+                                if constexpr (CF::PAIR)
+                                    mma_commit_pair(&acc_full[gb], 3);
+                                else
+                                    mma_commit(&acc_full[gb]);
+                                ++gcount;
+                                kin = 0;
+                            }
+                        }
                     }
+                } else
+                for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it, ++local) {
+                    const int buf = local & 1;
+                    const uint32_t acc_phase = (local >> 1) & 1;
+                    if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t acc_base = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
+                    // group g covers K slices [ceil(g*KB/G), ceil((g+1)*KB/G))
+                    int group = 0;
+                    int next_group_start = w.kb1;
+                    if (ngroups > 1) {   // a K segment may start inside the groups
+                        group = (w.kb0 * ngroups) / kblocks;
+                        next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
+                    }
+                    uint32_t d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
+                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        bool first_in_group = (kb == w.kb0);
+                        if (kb == next_group_start) {
+                            ++group;
+                            first_in_group = true;
+                            next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
+                            d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
+                        }
+                        issue_stage(d_tmem, stage, first_in_group);
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    // accumulator ready for the epilogue (of both CTAs of a pair)
+                    if constexpr (CF::PAIR)
+                        mma_commit_pair(&acc_full[buf], 3);
+                    else
+                        mma_commit(&acc_full[buf]);
                 }
-                if (!ok) break;
-                // accumulator ready for the epilogue (of both CTAs of a pair)
+                if (!ok) raise_error(p, ERR_TIMEOUT_MMA, abort_flag);
+                // Drain: all issued MMAs complete before TMEM is released.
                 if constexpr (CF::PAIR)
-                    mma_commit_pair(&acc_full[buf], 3);
+                    mma_commit_pair(drain, 1);
                 else
-                    mma_commit(&acc_full[buf]);
+                    mma_commit(drain);
+                if (!mbar_wait(drain, 0, nullptr)) raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
             }
-            if (!ok) raise_error(p, ERR_TIMEOUT_MMA, abort_flag);
-            // Drain: all issued MMAs complete before TMEM is released.
-            if constexpr (CF::PAIR)
-                mma_commit_pair(drain, 1);
-            else
-                mma_commit(drain);
-            if (!mbar_wait(drain, 0, nullptr)) raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        if constexpr (CF::REG_SPLIT) regs_inc<CF::REGS_HIGH>();
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                        // TMEM lane quarter this warp may access
-        const int ew = warp - 2;                       // epilogue warp index
+        const int ew = warp - CF::EPI_WARP0;           // epilogue warp index
         const int cbase = (ew >> 2) * CF::EPI_COLS;    // first tile column this warp handles
         uint8_t* stg = staging + ew * 4096;            // this warp's 4 KB staging box (tile modes)
         constexpr int UNIT = CF::EPI_COLS < 32 ? CF::EPI_COLS : 32;
@@ -580,20 +697,25 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         constexpr int UNIT_F4 = UNIT / 4;              // float4 per lane per unit in a partial
         // partial layout: [item][cta][epilogue warp][unit][UNIT_F4][32 lanes] float4
         constexpr int64_t ITEM_F4 = static_cast<int64_t>(CF::CTAS) * CF::EPI_WARPS * NUNITS * UNIT_F4 * 32;
+        // GS: the u loops index the register-resident group sum, so they unroll
+        constexpr int U_UNROLL = CF::GS ? NUNITS : 1;
         int stores = 0;
         int local = 0;
+        int gcount = 0;   // GS: scale groups folded so far (both buffers alternate)
         bool ok = true;
         Work w;
         for (int it = 0; next_work(p, unit0, units, it, w); ++it, ++local) {
             int mb, nb;
             tile_coords(w.tile, p, mb, nb);
             const int buf = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
-            if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) {
-                ok = false;
-                break;
+            if constexpr (!CF::GS) {
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
             }
-            tc_fence_after();
             const int row_base = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM + q * 32;
             const int row = row_base + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -611,8 +733,100 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             float rowmax = 0.0f;
             const bool part = (CF::MODE != MODE_ROWQ) && w.item >= 0;   // a K segment of a split tile
 
+            // Per-K-group scales: fold each scale group's product into gsum as
+            // soon as the MMA warp has finished it, then hand its buffer back.
+            float gsum[CF::GS ? CF::EPI_COLS : 1];
+            if constexpr (CF::GS) {
+#pragma unroll
+                for (int c = 0; c < CF::EPI_COLS; ++c) gsum[c] = 0.0f;
+                if (w.kb1 > w.kb0) {
+                    const int j0 = w.kb0 / p.group_kb, j1 = (w.kb1 - 1) / p.group_kb + 1;
+                    const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(cbase);
+                    const int colw = nb * CF::BN + cbase;   // this warp's first MMA column
+                    float* cs_buf = gs_cols + ew * CF::GS_BUFS * CF::EPI_COLS;
+                    // Group j's scales are fetched two groups ahead, right after
+                    // the previous group's buffer is handed back: that arrive
+                    // has release semantics and would otherwise wait for them.
+                    // Column scales (tile modes): EPI_COLS floats into this warp's
+                    // shared buffer j % 3, 16 bytes per lane, zero past column N
+                    // (N % 4 == 0). Row scales: one per lane, into a register.
+                    auto stage_cols = [&](int j) {
+                        if constexpr (CF::GS_SMEM) {
+                            if (j < j1 && lane * 4 < CF::EPI_COLS) {
+                                const int c = colw + lane * 4;
+                                const float* src = p.col_gscale + j * p.gs_ld_col + (c < p.N ? c : 0);
+                                cp_async_16(cs_buf + (j % CF::GS_BUFS) * CF::EPI_COLS + lane * 4, src,
+                                            c < p.N ? 16u : 0u);
+                            }
+                            cp_async_commit();   // (an empty group past the last)
+                        }
+                    };
+                    auto load_rs = [&](int j) {
+                        return (j < j1 && row < p.M) ? __ldg(p.row_gscale + j * p.gs_ld_row + row) : 0.0f;
+                    };
+                    stage_cols(j0);
+                    stage_cols(j0 + 1);
+                    float rs_cur = load_rs(j0), rs_nxt = load_rs(j0 + 1);
+                    for (int j = j0; j < j1; ++j, ++gcount) {
+                        const int gb = gcount & 1;
+                        if constexpr (CF::GS_SMEM) cp_async_wait<1>();   // group j's copy (j + 1's may fly)
+                        __syncwarp();   // ... and visible to the whole warp
+                        const float* csj = CF::GS_SMEM ? cs_buf + (j % CF::GS_BUFS) * CF::EPI_COLS
+                                                       : p.col_gscale + j * p.gs_ld_col;
+                        const float rsj = rs_cur;
+                        if (!mbar_wait(&acc_full[gb], (gcount >> 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // two Tensor Memory loads in flight per wait
+#pragma unroll
+                        for (int u = 0; u < NUNITS; u += 2) {
+                            constexpr int PAIRED = NUNITS >= 2 ? 2 : 1;
+                            uint32_t r[PAIRED][UNIT];
+#pragma unroll
+                            for (int h = 0; h < PAIRED; ++h) {
+                                const uint32_t ta = tq + static_cast<uint32_t>(gb * p.acc_stride + (u + h) * UNIT);
+                                if constexpr (UNIT == 32)
+                                    tmem_ld32(ta, r[h]);
+                                else
+                                    tmem_ld16(ta, r[h]);
+                            }
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int h = 0; h < PAIRED; ++h) {
+                                if constexpr (CF::GS_SMEM)
+                                    gs_fold_smem<UNIT>(gsum + (u + h) * UNIT, r[h], rsj, csj + (u + h) * UNIT);
+                                else
+                                    gs_fold<UNIT>(gsum + (u + h) * UNIT, r[h], rsj, csj, colw + (u + h) * UNIT, p.N);
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();   // every lane is done with TMEM buffer gb and scale buffer j % 3
+                        // The buffer's reads have completed (tcgen05.wait::ld), so the
+                        // hand-back needs no memory ordering: a relaxed arrive, which
+                        // does not wait for the scale prefetches still in flight.
+                        if (lane == 0) {
+                            if (CF::PAIR && rank != 0)
+                                mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&acc_empty[gb]), 0));
+                            else
+                                mbar_arrive_relaxed(&acc_empty[gb]);
+                        }
+                        stage_cols(j + 2);   // into the buffer just read
+                        rs_cur = rs_nxt;
+                        rs_nxt = load_rs(j + 2);
+                    }
+                    if constexpr (CF::GS_SMEM) cp_async_wait<0>();   // nothing in flight past the item
+                }
+                if (!ok) break;
+            }
+
             // The accumulator of 32 (or 16) columns, FP32 sum of its K groups.
             auto load_acc = [&](int u, float (&v)[32]) {
+                if constexpr (CF::GS) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = j < UNIT ? gsum[u * UNIT + j] : 0.0f;
+                } else {
                 const int tcol = cbase + u * UNIT;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
@@ -636,6 +850,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 if (p.k_blocks == 0) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                }
                 }
             };
             // Epilogue arithmetic and output of finished values.
@@ -668,7 +883,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
             };
 
-#pragma unroll 1
+#pragma unroll U_UNROLL
             for (int u = 0; u < NUNITS; ++u) {
                 float v[32];
                 load_acc(u, v);
@@ -682,7 +897,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     for (int j = 0; j < UNIT_F4; ++j)
                         __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                 }
-                if (u == NUNITS - 1) {
+                if (!CF::GS && u == NUNITS - 1) {
                     // Last read of this accumulator: hand it back to the MMA warp.
                     tc_fence_before();
                     __syncwarp();
@@ -731,7 +946,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         // together (at most three others).
                         const int item0 = (w.tile - p.dp_tiles) * p.split;
                         const int own = w.item - item0;
-#pragma unroll 1
+#pragma unroll U_UNROLL
                         for (int u = 0; u < NUNITS; ++u) {
                             float v[32];
                             load_acc(u, v);

@@ -14,8 +14,9 @@ using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, con
                                  const Params& p, int grid, cudaStream_t s, bool cooperative);
 
 struct KernelInfo {
-    int bn, fp8, a_mn, b_mn, mode, pair;
+    int bn, fp8, a_mn, b_mn, mode, pair, gs;
     int stages, smem_bytes, tmem_cols, threads, epi_warps;
+    int launch_regs;   // register split (setmaxnreg): registers per thread the split assumes at launch; 0 = none
     const void* func;  // host stub of the __global__ function (for attributes)
     LaunchFn launch;
 };
@@ -57,12 +58,14 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
 template <class CF>
 KernelInfo make_info() {
     return KernelInfo{CF::BN,     CF::FP8,    CF::A_MN,       CF::B_MN,      CF::MODE,
-                      CF::PAIR ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS, CF::EPI_WARPS,
+                      CF::PAIR ? 1 : 0, CF::GS ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
+                      CF::EPI_WARPS, CF::REG_SPLIT ? CF::LAUNCH_REGS : 0,
                       reinterpret_cast<const void*>(&gemm_persistent<CF>), &launch_variant<CF>};
 }
 
 // Each instantiation unit exports its table.
 const KernelInfo* kernels_bf16(int* count);
 const KernelInfo* kernels_fp8(int* count);
+const KernelInfo* kernels_fp8_grouped(int* count);
 
 }  // namespace dg

@@ -148,10 +148,21 @@ dgemm_status_t dgemm_bf16(const void* A, const void* B, dgemm_b_layout_t b_layou
 /* FP8 E4M3 scaled GEMM:
  *   D = epi(alpha * diag(a_scale) . (Aq . op(Bq)) . diag(b_scale) + beta * C)
  *   Aq       [M,K] E4M3 codes (1 byte each).   Bq [K,N] or [N,K] E4M3 codes.
- *   a_scale  [M] FP32, one per row of A (per token), stride 1.
- *   b_scale  [N] FP32, one per output channel n, stride 1.
- *   k_group  0: the scales are constant along K and are applied once to the
- *            FP32 accumulator (exact); other values: DGEMM_ERR_NOT_SUPPORTED.
+ *   k_group  0: one scale per row and per channel, constant along K, applied
+ *            once to the FP32 accumulator (exact):
+ *              a_scale [M] FP32, one per row of A (per token), stride 1;
+ *              b_scale [N] FP32, one per output channel n, stride 1.
+ *            g > 0, a multiple of 128: per-K-group scales ([W3] §3.2 asks to
+ *            confirm per-GEMM or per-group granularity). K is cut into
+ *            G = ceil(K / g) groups of g (the last may be shorter) and
+ *              D = epi(alpha * sum_j diag(a_scale[j]) (Aq_j . op(Bq_j)) diag(b_scale[j]) + beta * C)
+ *            with Aq_j, Bq_j the group's K slice. Tables are group-major:
+ *              a_scale [G][M] (a_scale[j*M + m]), b_scale [G][N] (b_scale[j*N + n]).
+ *            Each group's product is accumulated by the tensor core and folded
+ *            into the FP32 sum, scaled, by the epilogue warps (2 FP32 operations
+ *            per output element per group, so small groups cost throughput).
+ *            Not combinable with DGEMM_QUANT_E4M3_ROW_AMAX; g not a multiple of
+ *            128: DGEMM_ERR_NOT_SUPPORTED; g < 0: DGEMM_ERR_INVALID_VALUE.
  *   C, D, epi, ws as for dgemm_bf16.
  * [W3] §1.2, §3.2, §5.1. */
 dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t b_layout,

@@ -74,9 +74,14 @@ def test_argument_errors_return_before_any_device_call(lib):
     assert call_bf16(lib, epi=ctypes.byref(epi)) == 1           # bad activation
     # empty problems are a no-op and need no device
     assert call_bf16(lib, M=0) == 0 and call_bf16(lib, N=0) == 0
-    # fp8 per-group scales are not built
-    assert lib.dgemm_fp8_scaled(16, 16, 1, 16, 16, 128, None, 0, 16, 1, 128, 128, 128, 1.0, 0.0, None,
-                                None, 0, None) == 2
+    # fp8 per-K-group scales: groups of whole 128-element K slices, no requantisation
+    def fp8(k_group, epi=None, d_dt=1):
+        return lib.dgemm_fp8_scaled(16, 16, 1, 16, 16, k_group, None, 0, 16, d_dt, 128, 128, 256, 1.0, 0.0, epi,
+                                    None, 0, None)
+    assert fp8(-1) == 1
+    assert fp8(64) == 2 and fp8(200) == 2
+    epi = _lib.Epilogue(None, 0, 1, 16)
+    assert fp8(128, ctypes.byref(epi), d_dt=2) == 2
 
 
 def test_workspace_sizes(lib, monkeypatch):

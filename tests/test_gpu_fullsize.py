@@ -63,3 +63,12 @@ def test_workload5_full_size_sampled_rows():
     qa = q.numpy() & 0x7F
     assert np.all(s.numpy() > 0)
     assert np.all(qa.max(axis=1) == 0x7E)
+
+
+def test_fp8_grouped_scales_full_size_sampled_rows():
+    """The FFN projection of workload 3 with one scale per 128-element K group."""
+    w = wl.fp8_grouped(4096, 11008, 4096, k_group=128)
+    D, _ = run_workload(w)
+    rows = sample_rows(w.M, 24, seed=6)
+    ok, msg = bf16_ulp_ok(to_f64(D)[rows], ref_of(w, rows=rows))
+    assert ok, msg
