@@ -152,13 +152,15 @@ struct Cfg {
     static constexpr int EPI_WARPS = (MODE == MODE_SWAP || BN < 128) ? 4 : 8;
     static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);   // columns per epilogue warp
     static constexpr int STAGING_BYTES = (MODE == MODE_SWAP) ? 0 : EPI_WARPS * 4096;  // one 4 KB box each
-    // Per-K-group column scales, staged in shared memory two groups ahead:
-    // three buffers of EPI_COLS floats per epilogue warp (tile modes; the
-    // small-M form reads its few column scales directly).
+    // Per-K-group scales (tile modes): a scale-producer warp copies each
+    // group's BN column scales and this CTA's 128 row scales into a ring of
+    // SC_SLOTS shared-memory slots ahead of the epilogue (the small-M form
+    // reads its few scales directly).
     static constexpr bool GS_SMEM = GS && MODE != MODE_SWAP;
-    static constexpr int GS_BUFS = 3;
-    static constexpr int GS_BYTES = GS_SMEM ? EPI_WARPS * GS_BUFS * EPI_COLS * 4 : 0;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int SC_SLOTS = GS_SMEM ? 4 : 0;
+    static constexpr int SLOT_FLOATS = BN + BM;
+    static constexpr int GS_BYTES = SC_SLOTS * SLOT_FLOATS * 4;
+    static constexpr int BAR_BYTES = GS_SMEM ? 384 : 256;
     static constexpr int SMEM_LIMIT = 232448;  // 227 KB opt-in maximum per CTA
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - STAGING_BYTES - GS_BYTES - BAR_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
@@ -174,7 +176,9 @@ struct Cfg {
     // idle warps, then the 8 epilogue warps -- and move registers from the
     // first warpgroup to the others (setmaxnreg).
     static constexpr bool REG_SPLIT = GS && EPI_WARPS == 8;
-    static constexpr int EPI_WARP0 = REG_SPLIT ? 4 : 2;     // first epilogue warp
+    // first epilogue warp: the per-group tile kernels use warp 2 as the scale
+    // producer (warp 3 idles), the split kernels need whole warpgroups
+    static constexpr int EPI_WARP0 = (REG_SPLIT || GS_SMEM) ? 4 : 2;
     static constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     static constexpr int LAUNCH_REGS = 168;   // per thread at launch (12 warps: 3 per SM sub-partition)
     static constexpr int REGS_LOW = 56, REGS_HIGH = 224;
@@ -404,14 +408,16 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     uint8_t* staging = smem + S * CF::STAGE_BYTES;
-    float* gs_cols = reinterpret_cast<float*>(staging + CF::STAGING_BYTES);   // GS column-scale buffers
+    float* gs_area = reinterpret_cast<float*>(staging + CF::STAGING_BYTES);   // GS scale slots
     uint64_t* bars = reinterpret_cast<uint64_t*>(staging + CF::STAGING_BYTES + CF::GS_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
     uint64_t* acc_full = bars + 2 * S;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sc_full = drain + 1;                 // GS scale slots: filled / free
+    uint64_t* sc_empty = sc_full + CF::SC_SLOTS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sc_empty + CF::SC_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -432,6 +438,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             mbar_init(&acc_empty[b], CF::EPI_WARPS * CF::CTAS);  // every epilogue warp of the pair
         }
         mbar_init(drain, 1);
+        for (int sl = 0; sl < CF::SC_SLOTS; ++sl) {
+            mbar_init(&sc_full[sl], 32);               // every lane of the scale producer
+            mbar_init(&sc_empty[sl], CF::EPI_WARPS);   // every epilogue warp of this CTA
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -684,6 +694,48 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 if (!mbar_wait(drain, 0, nullptr)) raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
             }
             __syncwarp();
+        } else if (CF::GS_SMEM && warp == 2) {
+            // ------------------------------------------------------------ scale producer
+            // For every scale group of every work item, in the epilogue's order:
+            // the tile's BN column scales (16 bytes per copy; N % 4 == 0) and this
+            // CTA's 128 row scales (4 bytes per copy; any M) into the next slot,
+            // zero past the edges; each lane's copies arrive on the slot's full
+            // barrier when they land.
+            int gcount = 0;
+            bool ok = true;
+            Work w;
+            for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it) {
+                if (w.kb1 <= w.kb0) continue;
+                int mb, nb;
+                tile_coords(w.tile, p, mb, nb);
+                const int row0 = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM;
+                const int col0 = nb * CF::BN;
+                const int j0 = w.kb0 / p.group_kb, j1 = (w.kb1 - 1) / p.group_kb + 1;
+                for (int j = j0; j < j1; ++j, ++gcount) {
+                    const int slot = gcount % (CF::SC_SLOTS > 0 ? CF::SC_SLOTS : 1);
+                    const uint32_t ph = static_cast<uint32_t>(gcount / (CF::SC_SLOTS > 0 ? CF::SC_SLOTS : 1)) & 1u;
+                    if (!mbar_wait(&sc_empty[slot], ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    float* dst = gs_area + slot * CF::SLOT_FLOATS;
+                    const float* cs = p.col_gscale + j * p.gs_ld_col;
+                    const float* rs = p.row_gscale + j * p.gs_ld_row;
+#pragma unroll
+                    for (int c = lane * 4; c < CF::BN; c += 128) {
+                        const int n = col0 + c;
+                        cp_async_16(dst + c, cs + (n < p.N ? n : 0), n < p.N ? 16u : 0u);
+                    }
+#pragma unroll
+                    for (int r = lane; r < CF::BM; r += 32) {
+                        const int m = row0 + r;
+                        cp_async_4(dst + CF::BN + r, rs + (m < p.M ? m : 0), m < p.M ? 4u : 0u);
+                    }
+                    cp_async_mbar_arrive(&sc_full[slot]);
+                }
+            }
+            if (!ok) raise_error(p, ERR_TIMEOUT_PRODUCER, abort_flag);
+            cp_async_wait<0>();   // no copy into this CTA's shared memory outlives it
         }
     } else {
         if constexpr (CF::REG_SPLIT) regs_inc<CF::REGS_HIGH>();
@@ -743,37 +795,36 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     const int j0 = w.kb0 / p.group_kb, j1 = (w.kb1 - 1) / p.group_kb + 1;
                     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(cbase);
                     const int colw = nb * CF::BN + cbase;   // this warp's first MMA column
-                    float* cs_buf = gs_cols + ew * CF::GS_BUFS * CF::EPI_COLS;
-                    // Group j's scales are fetched two groups ahead, right after
-                    // the previous group's buffer is handed back: that arrive
-                    // has release semantics and would otherwise wait for them.
-                    // Column scales (tile modes): EPI_COLS floats into this warp's
-                    // shared buffer j % 3, 16 bytes per lane, zero past column N
-                    // (N % 4 == 0). Row scales: one per lane, into a register.
-                    auto stage_cols = [&](int j) {
-                        if constexpr (CF::GS_SMEM) {
-                            if (j < j1 && lane * 4 < CF::EPI_COLS) {
-                                const int c = colw + lane * 4;
-                                const float* src = p.col_gscale + j * p.gs_ld_col + (c < p.N ? c : 0);
-                                cp_async_16(cs_buf + (j % CF::GS_BUFS) * CF::EPI_COLS + lane * 4, src,
-                                            c < p.N ? 16u : 0u);
-                            }
-                            cp_async_commit();   // (an empty group past the last)
-                        }
-                    };
+                    // Tile modes: scales from the scale producer's slot gcount % SC_SLOTS.
+                    // Small-M form: row scale one per lane into a register, fetched
+                    // two groups ahead (after the hand-back arrive, which is relaxed
+                    // so it does not wait for them); column scales read directly.
                     auto load_rs = [&](int j) {
                         return (j < j1 && row < p.M) ? __ldg(p.row_gscale + j * p.gs_ld_row + row) : 0.0f;
                     };
-                    stage_cols(j0);
-                    stage_cols(j0 + 1);
-                    float rs_cur = load_rs(j0), rs_nxt = load_rs(j0 + 1);
+                    float rs_cur = 0.0f, rs_nxt = 0.0f;
+                    if constexpr (!CF::GS_SMEM) {
+                        rs_cur = load_rs(j0);
+                        rs_nxt = load_rs(j0 + 1);
+                    }
                     for (int j = j0; j < j1; ++j, ++gcount) {
                         const int gb = gcount & 1;
-                        if constexpr (CF::GS_SMEM) cp_async_wait<1>();   // group j's copy (j + 1's may fly)
-                        __syncwarp();   // ... and visible to the whole warp
-                        const float* csj = CF::GS_SMEM ? cs_buf + (j % CF::GS_BUFS) * CF::EPI_COLS
-                                                       : p.col_gscale + j * p.gs_ld_col;
-                        const float rsj = rs_cur;
+                        const int slot = gcount % (CF::SC_SLOTS > 0 ? CF::SC_SLOTS : 1);
+                        const float* csj;
+                        float rsj;
+                        if constexpr (CF::GS_SMEM) {
+                            const uint32_t ph = static_cast<uint32_t>(gcount / CF::SC_SLOTS) & 1u;
+                            if (!mbar_wait(&sc_full[slot], ph, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            const float* sl = gs_area + slot * CF::SLOT_FLOATS;
+                            csj = sl + cbase;
+                            rsj = sl[CF::BN + q * 32 + lane];
+                        } else {
+                            csj = p.col_gscale + j * p.gs_ld_col;
+                            rsj = rs_cur;
+                        }
                         if (!mbar_wait(&acc_full[gb], (gcount >> 1) & 1, abort_flag)) {
                             ok = false;
                             break;
@@ -802,21 +853,22 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             }
                         }
                         tc_fence_before();
-                        __syncwarp();   // every lane is done with TMEM buffer gb and scale buffer j % 3
-                        // The buffer's reads have completed (tcgen05.wait::ld), so the
-                        // hand-back needs no memory ordering: a relaxed arrive, which
-                        // does not wait for the scale prefetches still in flight.
+                        __syncwarp();   // every lane is done with TMEM buffer gb and scale slot
+                        // The buffer's and slot's reads have completed (tcgen05.wait::ld;
+                        // shared loads consumed), so the hand-backs need no memory
+                        // ordering: relaxed arrives, which do not wait for loads in flight.
                         if (lane == 0) {
                             if (CF::PAIR && rank != 0)
                                 mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&acc_empty[gb]), 0));
                             else
                                 mbar_arrive_relaxed(&acc_empty[gb]);
+                            if constexpr (CF::GS_SMEM) mbar_arrive_relaxed(&sc_empty[slot]);
                         }
-                        stage_cols(j + 2);   // into the buffer just read
-                        rs_cur = rs_nxt;
-                        rs_nxt = load_rs(j + 2);
+                        if constexpr (!CF::GS_SMEM) {
+                            rs_cur = rs_nxt;
+                            rs_nxt = load_rs(j + 2);
+                        }
                     }
-                    if constexpr (CF::GS_SMEM) cp_async_wait<0>();   // nothing in flight past the item
                 }
                 if (!ok) break;
             }

@@ -266,6 +266,17 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// 4-byte asynchronous copy global -> shared (cp.async, through L1); with
+// src_bytes = 0 the destination is zero-filled and nothing is read.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// Arrives on an mbarrier once all of this thread's earlier cp.async copies have
+// landed (the arrival is one of the barrier's expected count: .noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Waits until at most N of this thread's committed copy groups are pending.
 template <int N>
