@@ -79,7 +79,7 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: int):
+def recorded_traffic(workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
     current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -148,6 +148,29 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def make_workload(args):
+    """The workload a run times: one of the five, or with --k-group, workload 3's
+    shape and recipe with per-K-group scales."""
+    import workloads as wl
+    if getattr(args, "k_group", 0):
+        if args.config != 3:
+            raise SystemExit("--k-group applies to workload 3 (FP8 E4M3 4096 x 11008 x 4096)")
+        return wl.fp8_grouped(k_group=args.k_group)
+    return wl.make(args.config)
+
+
+def workload_key(args) -> str:
+    return f"{args.config}g{args.k_group}" if getattr(args, "k_group", 0) else str(args.config)
+
+
+def describe(args) -> str:
+    d = DESCRIPTIONS[args.config]
+    if getattr(args, "k_group", 0):
+        d = d.replace("per-token x per-channel scales",
+                      f"per-(token, {args.k_group}-element K group) x per-(channel, K group) scales")
+    return d
+
+
 def oracle_sample(w, seconds: float):
     """Time the oracle on whole rows of the workload until `seconds` have passed
     (at least one row); returns (flops, elapsed, rows, threads)."""
@@ -167,7 +190,7 @@ def oracle_sample(w, seconds: float):
         else:
             y = oracle.fp8_gemm_ref(A, B, w.b_layout, w.a_scale.numpy(), w.b_scale.numpy(), C, w.alpha, w.beta,
                                     None if w.bias is None else w.bias.numpy(), w.act, rows=rows,
-                                    nthreads=threads)
+                                    nthreads=threads, k_group=w.k_group)
             if w.out_quant != "none":
                 oracle.requant_rows(y)
         done = rows[1]
@@ -191,7 +214,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dg.load()
-    w = wl.make(args.config)
+    w = make_workload(args)
     peaks, peak_kind = measured_peaks()
 
     # ---- rotating input sets (each timed call finds its operands out of L2)
@@ -217,7 +240,7 @@ def run_ours(args, rank, world, local):
         if w.form == "bf16":
             dg.dgemm_bf16(g.A, g.B, D, **kw)
         else:
-            dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, **kw)
+            dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, **kw)
 
     dist = world > 1
     if dist:
@@ -305,7 +328,7 @@ def run_ours(args, rank, world, local):
         base = peaks["bf16_tflops"]
         peak = base if w.form == "bf16" else 2.0 * base   # FP8:BF16 dense ratio 2
         unit, bound = "TFLOP/s", "tensor"
-    traffic = recorded_traffic(args.config)
+    traffic = recorded_traffic(workload_key(args))
     roof = {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": f"{peak_kind}" + ("" if w.form == "bf16" or skinny else " bf16 x 2 (FP8:BF16 ratio)"),
@@ -318,8 +341,8 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.form == "bf16" else "e4m3", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.config], "number": args.config, "M": w.M, "N": w.N, "K": w.K,
-                   "b_layout": w.b_layout, "parallelism": f"replicas x{world}",
+        "config": {"workload": describe(args), "number": args.config, "M": w.M, "N": w.N, "K": w.K,
+                   "b_layout": w.b_layout, "k_group": w.k_group, "parallelism": f"replicas x{world}",
                    "l2": f"rotating {nsets} input sets of {set_bytes / 2**20:.0f} MiB (> L2 129 MiB)",
                    "plan": {k: plan[k] for k in ("swap_ab", "tile_m", "tile_n", "stages", "num_tiles", "grid",
                                                  "cooperative")}},
@@ -344,6 +367,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU time spent on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--k-group", type=int, default=0,
+                    help="workload 3 with per-K-group FP8 scales of this group size (multiple of 128)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="wall time the reference arm spends on warm-up + steps")
     args = ap.parse_args()
@@ -383,7 +408,7 @@ def run_reference(args, world):
     sample (whole rows) of the same workload, sized so warm-up + steps take about
     two minutes."""
     import workloads as wl
-    w = wl.make(args.config)
+    w = make_workload(args)
     budget = args.ref_seconds / (args.steps + args.warmup)
     # calibrate rows per step on one row
     fl, el, rows, threads = oracle_sample(w, 0.0)
@@ -402,7 +427,7 @@ def run_reference(args, world):
         else:
             y = oracle.fp8_gemm_ref(A, B, w.b_layout, w.a_scale.numpy(), w.b_scale.numpy(), C, w.alpha, w.beta,
                                     None if w.bias is None else w.bias.numpy(), w.act, rows=rows,
-                                    nthreads=threads)
+                                    nthreads=threads, k_group=w.k_group)
             if w.out_quant != "none":
                 oracle.requant_rows(y)
         return rows[1] - rows[0]
@@ -420,8 +445,8 @@ def run_reference(args, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.config], "number": args.config, "M": w.M, "N": w.N, "K": w.K,
-                   "b_layout": w.b_layout},
+        "config": {"workload": describe(args), "number": args.config, "M": w.M, "N": w.N, "K": w.K,
+                   "b_layout": w.b_layout, "k_group": w.k_group},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} rows of {w.M} per step of the same workload, float64 "
                                    f"oracle, OpenMP"},
