@@ -109,14 +109,16 @@ struct Plan {
     int gs;            // per-K-group scales (group_kb K slices per group)
     int group_kb;
     int dp_tiles, split, tail_items;   // tail splitting (MODE_TILE)
+    int cluster_split;                 // split K segments of a tile form a cluster of `split` CTAs
     size_t tail_count_bytes;           // workspace: per-warp arrival counters
 };
 
 // Validates the sizes, enums and epilogue; picks the kernel variant and grid.
 // Pure host logic: needs no GPU.
+// max_pairs: co-resident 2-CTA clusters; max_quads: co-resident 4-CTA clusters.
 dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t bl, dgemm_dtype_t d_dtype,
-                         const dgemm_epilogue_t* epi, int num_sms, int max_pairs, bool allow_split, Plan* out,
-                         int k_group = 0) {
+                         const dgemm_epilogue_t* epi, int num_sms, int max_pairs, int max_quads, bool allow_split,
+                         Plan* out, int k_group = 0) {
     if (M < 0 || N < 0 || K < 0 || num_sms <= 0 || k_group < 0) return DGEMM_ERR_INVALID_VALUE;
     if (bl != DGEMM_B_KN && bl != DGEMM_B_NK) return DGEMM_ERR_INVALID_VALUE;
     if (d_dtype != DGEMM_F32 && d_dtype != DGEMM_BF16 && d_dtype != DGEMM_E4M3) return DGEMM_ERR_INVALID_VALUE;
@@ -148,6 +150,9 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     const char* split_env = std::getenv("DGEMM_TAIL_SPLIT");
     const bool force_split = split_env && split_env[0] == 'f';
     const bool split_ok = allow_split && !(split_env && split_env[0] == '0') && oq == DGEMM_QUANT_NONE;
+    const char* cl_env = std::getenv("DGEMM_CLUSTER_SPLIT");   // "0": split-K through the workspace only
+    if (cl_env && cl_env[0] == '0') max_quads = 0;
+    const bool cluster_ok = !(cl_env && cl_env[0] == '0');
     const int64_t kb_all = (K + (128 / static_cast<int64_t>(esz)) - 1) / (128 / static_cast<int64_t>(esz));
     int bn;
     int pair = 0;
@@ -184,8 +189,11 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
             const int64_t waves = (tiles + units - 1) / units;
             double cost = static_cast<double>(waves) * (128.0 * c.bn) * c.penalty;
             // under one wave, split-K divides each unit's work (reduction ~15 % of a tile)
+            // (the reduction ~15 % of a tile through the workspace, ~5 % when the
+            // segments of a single-CTA tile share a cluster)
             const int64_t sk = split_ok ? underfill_split(tiles, units, kb_all) : 1;
-            if (sk > 1) cost = (128.0 * c.bn) * c.penalty * (1.0 / static_cast<double>(sk) + 0.15);
+            const bool cl = cluster_ok && !c.pair && (sk == 2 || sk == 4) && tiles <= (sk == 2 ? max_pairs : max_quads);
+            if (sk > 1) cost = (128.0 * c.bn) * c.penalty * (1.0 / static_cast<double>(sk) + (cl ? 0.05 : 0.15));
             if (cost < best) {
                 best = cost;
                 bn = c.bn;
@@ -254,9 +262,23 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     };
     // Split-K when the tiles do not fill one wave (decode shapes, small M x N
     // with long K): every tile is split into K segments run on the idle units.
+    // When the segments can form clusters (single-CTA kernels, 2 or 4
+    // segments, every cluster resident at once) they are summed through
+    // distributed shared memory instead, and no workspace is needed.
     const int64_t sk = (split_ok && k_blocks > 0) ? underfill_split(p.pub.num_tiles, units, k_blocks) : 1;
+    p.cluster_split = 0;
     if (sk > 1 && (p.mode == dg::MODE_TILE || p.mode == dg::MODE_SWAP)) {
-        use_split(0, static_cast<int>(sk), p.pub.num_tiles * static_cast<int>(sk));
+        if (cluster_ok && !pair && (sk == 2 || sk == 4) && p.pub.num_tiles <= (sk == 2 ? max_pairs : max_quads)) {
+            p.cluster_split = 1;
+            p.dp_tiles = 0;
+            p.split = static_cast<int>(sk);
+            p.tail_items = p.pub.num_tiles * static_cast<int>(sk);
+            p.pub.grid = p.tail_items;
+            p.tail_count_bytes = 0;
+            p.pub.workspace_bytes = 0;
+        } else {
+            use_split(0, static_cast<int>(sk), p.pub.num_tiles * static_cast<int>(sk));
+        }
     } else if (p.mode == dg::MODE_TILE && split_ok && k_blocks > 0) {
         const int rem = p.pub.num_tiles % units;
         if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks >= kMinTailSlices)) {
@@ -285,6 +307,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.k_groups = groups;
     p.pub.tail_tiles = p.pub.num_tiles - p.dp_tiles;
     p.pub.tail_split = p.split;
+    p.pub.cluster_split = p.cluster_split;
     if (oq) p.pub.workspace_bytes = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
     *out = p;
     return DGEMM_OK;
@@ -353,26 +376,29 @@ cudaError_t configure_kernel(int kernel, int devid) {
     return e;
 }
 
-// How many CTA pairs (2-CTA clusters) of the pair kernels fit on the device at
-// once, measured once per device with the occupancy API (0: no pairs).
-int g_max_pairs[kMaxDevices][2];
-std::once_flag g_pairs_once[kMaxDevices][2];
+// How many clusters of `size` CTAs (2: the CTA-pair kernels; 4: single-CTA
+// kernels whose split K segments share a cluster) fit on the device at once,
+// measured once per device with the occupancy API on a representative kernel
+// (every variant runs one CTA per SM). 0: none.
+int g_max_clusters[kMaxDevices][2][2];
+std::once_flag g_clusters_once[kMaxDevices][2][2];
 
-int max_pairs(DeviceState* dev, int devid, int fp8) {
-    std::call_once(g_pairs_once[devid][fp8], [&]() {
+int max_clusters(DeviceState* dev, int devid, int fp8, int size) {
+    const int si = size == 2 ? 0 : 1;
+    std::call_once(g_clusters_once[devid][fp8][si], [&]() {
         int best = 0;
         std::call_once(g_kernels_once, collect_kernels);
         for (int i = 0; i < g_nk; ++i) {
             const dg::KernelInfo* k = g_kernels[i];
-            if (!k->pair || k->fp8 != fp8 || k->mode != dg::MODE_TILE) continue;
+            if (k->pair != (size == 2 ? 1 : 0) || k->fp8 != fp8 || k->mode != dg::MODE_TILE || k->gs) continue;
             if (configure_kernel(i, devid) != cudaSuccess) continue;
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2 * static_cast<unsigned>(dev->num_sms));
+            cfg.gridDim = dim3(static_cast<unsigned>(size * dev->num_sms));
             cfg.blockDim = dim3(static_cast<unsigned>(k->threads));
             cfg.dynamicSmemBytes = static_cast<size_t>(k->smem_bytes);
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(size);
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
@@ -382,10 +408,16 @@ int max_pairs(DeviceState* dev, int devid, int fp8) {
             else (void)cudaGetLastError();
             break;
         }
-        g_max_pairs[devid][fp8] = best > dev->num_sms / 2 ? dev->num_sms / 2 : best;
+        g_max_clusters[devid][fp8][si] = best > dev->num_sms / size ? dev->num_sms / size : best;
     });
-    return g_max_pairs[devid][fp8];
+    return g_max_clusters[devid][fp8][si];
 }
+
+int max_pairs(DeviceState* dev, int devid, int fp8) { return max_clusters(dev, devid, fp8, 2); }
+int max_quads(DeviceState* dev, int devid, int fp8) { return max_clusters(dev, devid, fp8, 4); }
+
+// Without a device: a GB300's measured 36 four-CTA clusters on 152 SMs, scaled.
+int quads_estimate(int num_sms) { return num_sms * 36 / 152; }
 
 CUtensorMapDataType tm_type(dgemm_dtype_t t) {
     return t == DGEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -398,7 +430,7 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
                    size_t ws_bytes, cudaStream_t stream, int k_group = 0) {
     // ---- arguments that need no device
     Plan plan;
-    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, false, &plan, k_group);
+    dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, 0, false, &plan, k_group);
     if (st != DGEMM_OK) return st;
     if (M == 0 || N == 0) return DGEMM_OK;
     if (!D || (K > 0 && (!A || !B))) return DGEMM_ERR_INVALID_VALUE;
@@ -425,10 +457,12 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     st = device_state(&dev, &devid);
     if (st != DGEMM_OK) return st;
     const int pairs = max_pairs(dev, devid, fp8);
-    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, true, &plan, k_group);
+    const int quads = max_quads(dev, devid, fp8);
+    st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, quads, true, &plan, k_group);
     if (st != DGEMM_OK) return st;
     if (plan.split > 1 && (!ws || ws_bytes < plan.pub.workspace_bytes)) {
-        st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, false, &plan, k_group);  // no room: whole tiles
+        st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, quads, false, &plan,
+                       k_group);  // no room: whole tiles
         if (st != DGEMM_OK) return st;
     }
     const dg::KernelInfo* k = g_kernels[plan.kernel];
@@ -520,7 +554,9 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
         p.out_row_scale = epi->out_row_scale;
         if (cudaMemsetAsync(ws, 0, kWsHeader + amax_bytes, stream) != cudaSuccess) return DGEMM_ERR_CUDA;
     }
-    if (k->launch(tmA, tmB, tmD, p, plan.pub.grid, stream, plan.pub.cooperative != 0) != cudaSuccess)
+    p.cluster_split = plan.cluster_split;
+    if (k->launch(tmA, tmB, tmD, p, plan.pub.grid, stream, plan.pub.cooperative != 0,
+                  plan.cluster_split ? plan.split : 1) != cudaSuccess)
         return DGEMM_ERR_CUDA;
     return DGEMM_OK;
 }
@@ -548,7 +584,7 @@ dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t
 size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,
                             const dgemm_epilogue_t* epi) {
     // SM count of the current device if there is one, else a GB300's 152.
-    int sms = 152, pairs = 76;
+    int sms = 152, pairs = 76, quads = quads_estimate(152);
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
         DeviceState* ds = nullptr;
@@ -556,15 +592,17 @@ size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b
         if (device_state(&ds, &devid) == DGEMM_OK) {
             sms = ds->num_sms;
             pairs = max_pairs(ds, devid, is_fp8 ? 1 : 0);
+            quads = max_quads(ds, devid, is_fp8 ? 1 : 0);
         }
     } else {
         (void)cudaGetLastError();
     }
     Plan plan;
     const dgemm_dtype_t d = (epi && epi->out_quant) ? DGEMM_E4M3 : DGEMM_BF16;
-    if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d, epi, sms, pairs, true, &plan) != DGEMM_OK) {
+    if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d, epi, sms, pairs, quads, true, &plan) != DGEMM_OK) {
         // the output dtype is not an argument here: retry with FP32 output
-        if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, DGEMM_F32, epi, sms, pairs, true, &plan) != DGEMM_OK)
+        if (make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, DGEMM_F32, epi, sms, pairs, quads, true, &plan) !=
+            DGEMM_OK)
             return 0;
     }
     return plan.pub.workspace_bytes;
@@ -573,18 +611,19 @@ size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b
 dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,
                           dgemm_dtype_t d_dtype, const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan) {
     if (!plan) return DGEMM_ERR_INVALID_VALUE;
-    int pairs = num_sms / 2;
-    if (num_sms <= 0) {  // the current device: its SM count and measured CTA-pair occupancy
+    int pairs = num_sms / 2, quads = quads_estimate(num_sms);
+    if (num_sms <= 0) {  // the current device: its SM count and measured cluster occupancy
         DeviceState* ds = nullptr;
         int devid = 0;
         const dgemm_status_t dst = device_state(&ds, &devid);
         if (dst != DGEMM_OK) return dst;
         num_sms = ds->num_sms;
         pairs = max_pairs(ds, devid, is_fp8 ? 1 : 0);
+        quads = max_quads(ds, devid, is_fp8 ? 1 : 0);
     }
     Plan p;
     const dgemm_status_t st =
-        make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, pairs, true, &p);
+        make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, pairs, quads, true, &p);
     if (st == DGEMM_OK) *plan = p.pub;
     return st;
 }

@@ -92,6 +92,11 @@ struct Params {
     // partials and runs the epilogue on it.
     int dp_tiles, split, tail_items;
     float* partials;         // [tail_items][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4
+    // Split-K through distributed shared memory (single-CTA kernels, under-
+    // filled grids): the split K segments of a tile are the CTAs of one
+    // cluster of `split` CTAs (rank = segment); partials go through the idle
+    // pipeline buffers and the peers' shared memory instead of the workspace.
+    int cluster_split;
     unsigned long long* tail_count;  // [num_tiles - dp_tiles][CTAS][EPI_WARPS]: (epoch << 8) | arrivals
     unsigned long long epoch;        // unique per launch (56 bits): stale counters need no clearing
 };
@@ -193,6 +198,8 @@ struct Cfg {
     static_assert(!GS || (FP8 && MODE != MODE_ROWQ), "per-K-group scales: FP8, tile or small-M form");
     static_assert(BN < 32 || BN % 32 == 0, "epilogue reads 32-column units");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
+    // split-K through the cluster parks a whole accumulator in the pipeline buffers
+    static_assert(EPI_WARPS * BN / (EPI_WARPS / 4) * 32 * 4 <= STAGES * STAGE_BYTES, "parked partials fit");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
@@ -737,6 +744,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             if (!ok) raise_error(p, ERR_TIMEOUT_PRODUCER, abort_flag);
             cp_async_wait<0>();   // no copy into this CTA's shared memory outlives it
         }
+        if (!CF::PAIR && p.cluster_split) {   // the split-K cluster barrier, once per thread
+            __syncwarp();
+            cluster_sync();
+        }
     } else {
         if constexpr (CF::REG_SPLIT) regs_inc<CF::REGS_HIGH>();
         // ------------------------------------------------------------ epilogue
@@ -754,6 +765,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         int stores = 0;
         int local = 0;
         int gcount = 0;   // GS: scale groups folded so far (both buffers alternate)
+        bool cluster_done = false;   // passed the split-K cluster barrier
         bool ok = true;
         Work w;
         for (int it = 0; next_work(p, unit0, units, it, w); ++it, ++local) {
@@ -905,10 +917,39 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
                 }
             };
-            // Epilogue arithmetic and output of finished values.
-            auto finish = [&](int u, float (&v)[32]) {
+            // Epilogue arithmetic and output of finished values. `direct`: store
+            // this unit with plain global stores instead of a TMA box (the K
+            // segments of a split tile each finish single units).
+            auto finish = [&](int u, float (&v)[32], bool direct) {
                 const int col0 = nb * CF::BN + cbase + u * UNIT;
                 epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row);
+                if constexpr (CF::MODE == MODE_TILE) {
+                    if (direct) {
+                        // row-major D, this thread's row: 16-byte chunks, each wholly
+                        // inside or outside N (N is a multiple of 8 for BF16, 4 for FP32)
+                        if (row < p.M) {
+                            if (p.d_f32) {
+                                float* d = static_cast<float*>(p.D) + static_cast<int64_t>(row) * p.ldd + col0;
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    if (col0 + 4 * c < p.N)
+                                        *reinterpret_cast<float4*>(d + 4 * c) =
+                                            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                            } else {
+                                uint16_t* d = static_cast<uint16_t*>(p.D) + static_cast<int64_t>(row) * p.ldd + col0;
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    if (col0 + 8 * c < p.N)
+                                        *reinterpret_cast<uint4*>(d + 8 * c) =
+                                            make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                                                       pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                                       pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                                       pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+                            }
+                        }
+                        return;
+                    }
+                }
                 if constexpr (CF::MODE == MODE_SWAP) {
                     // MMA column = output row; MMA row = output column.
                     if (row < p.M) {
@@ -935,19 +976,41 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
             };
 
+            // A split tile is finished by all of its K segments together: unit u
+            // (32 columns) of this warp's region belongs to segment u % split.
+            // Each segment parks the units other segments own as FP32 partials,
+            // counts its arrival, waits until every segment has arrived, then
+            // adds the others' partials of its own units to its accumulator and
+            // stores them directly: about one round trip through L2 per segment
+            // instead of a single warp reading every partial unit by unit.
+            const int item0 = part ? (w.tile - p.dp_tiles) * p.split : 0;
+            const int seg = part ? w.item - item0 : 0;
+            auto owner = [&](int u) { return u % p.split; };
+            // generic writes to buffers the TMA (async proxy) filled
+            if (part && p.cluster_split) fence_proxy_async_smem();
 #pragma unroll U_UNROLL
             for (int u = 0; u < NUNITS; ++u) {
                 float v[32];
                 load_acc(u, v);
-                if (part) {
-                    // K segment: park the raw FP32 accumulator; each warp-wide
-                    // store writes 512 contiguous bytes
-                    float4* dst = reinterpret_cast<float4*>(p.partials) + w.item * ITEM_F4 +
-                                  ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) * (UNIT_F4 * 32) +
-                                  lane;
+                if (part && owner(u) != seg) {
+                    // a unit another segment finishes: park the raw FP32
+                    // accumulator; each warp-wide store writes 512 contiguous bytes
+                    if (p.cluster_split) {
+                        // into this CTA's idle pipeline buffers (every stage has been
+                        // consumed: this is the unit's last item), for the peers
+                        float4* dst = reinterpret_cast<float4*>(stages) + (ew * NUNITS + u) * (UNIT_F4 * 32) + lane;
 #pragma unroll
-                    for (int j = 0; j < UNIT_F4; ++j)
-                        __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                        for (int j = 0; j < UNIT_F4; ++j)
+                            dst[32 * j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(p.partials) + w.item * ITEM_F4 +
+                                      ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
+                                          (UNIT_F4 * 32) +
+                                      lane;
+#pragma unroll
+                        for (int j = 0; j < UNIT_F4; ++j)
+                            __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                    }
                 }
                 if (!CF::GS && u == NUNITS - 1) {
                     // Last read of this accumulator: hand it back to the MMA warp.
@@ -960,60 +1023,36 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             mbar_arrive(&acc_empty[buf]);
                     }
                 }
-                if (!part) finish(u, v);
+                if (!part) finish(u, v, false);
             }
             if constexpr (CF::MODE == MODE_ROWQ) {
                 if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
             }
-            if constexpr (CF::MODE != MODE_ROWQ) {
-                if (part) {
-                    // This warp's region (32 rows x EPI_COLS columns) of the
-                    // segment is in place: count it; the warp that brings the
-                    // count to `split` sums the region's partials and finishes
-                    // it. Each warp counts and reduces on its own (no waiting).
+            if constexpr (CF::MODE != MODE_ROWQ && !CF::PAIR) {
+                if (part && p.cluster_split) {
+                    // Every segment of the tile is a CTA of this cluster (rank =
+                    // segment). One cluster barrier publishes the parked units;
+                    // each thread of each CTA arrives at it exactly once.
                     __syncwarp();
-                    unsigned last = 0;
-                    if (lane == 0) {
-                        // The counter word holds (launch epoch << 8) | arrivals; a
-                        // word left by any earlier launch counts as zero arrivals.
-                        unsigned long long* cnt =
-                            p.tail_count + ((w.tile - p.dp_tiles) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
-                        __threadfence();
-                        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), next = 0;
-                        for (int tries = 0; tries < 4096; ++tries) {
-                            next = ((old >> 8) == p.epoch) ? old + 1 : ((p.epoch << 8) | 1ull);
-                            const unsigned long long seen = atomicCAS(cnt, old, next);
-                            if (seen == old) break;
-                            old = seen;
-                        }
-                        last = ((next >> 8) == p.epoch && (next & 0xFFull) == static_cast<unsigned long long>(p.split))
-                                   ? 1u : 0u;
-                        __threadfence();
-                    }
-                    last = __shfl_sync(0xffffffffu, last, 0);
-                    if (last) {
-                        // Own segment from Tensor Memory (this is the unit's last
-                        // item, so its accumulator is never overwritten), the other
-                        // segments from the workspace, all their loads in flight
-                        // together (at most three others).
-                        const int item0 = (w.tile - p.dp_tiles) * p.split;
-                        const int own = w.item - item0;
+                    cluster_sync();
+                    cluster_done = true;
+                    if (seg < NUNITS) {
 #pragma unroll U_UNROLL
                         for (int u = 0; u < NUNITS; ++u) {
+                            if (owner(u) != seg) continue;
                             float v[32];
                             load_acc(u, v);
-                            const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
-                                                ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
-                                                    (UNIT_F4 * 32) +
-                                                lane;
+                            const uint32_t mine =
+                                smem_u32(reinterpret_cast<float4*>(stages) + (ew * NUNITS + u) * (UNIT_F4 * 32) + lane);
                             float4 f[3][UNIT_F4];
 #pragma unroll
                             for (int o = 0; o < 3; ++o) {
-                                const int sgi = o + (o >= own ? 1 : 0);
+                                const int peer = o + (o >= seg ? 1 : 0);
+                                const uint32_t base = peer < p.split ? mapa_shared(mine, static_cast<uint32_t>(peer)) : 0u;
 #pragma unroll
                                 for (int j = 0; j < UNIT_F4; ++j)
-                                    f[o][j] = sgi < p.split ? __ldcg(src + sgi * ITEM_F4 + 32 * j)
-                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    f[o][j] = peer < p.split ? ld_shared_cluster_f4(base + 16u * 32u * j)
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
 #pragma unroll
                             for (int o = 0; o < 3; ++o)
@@ -1024,13 +1063,97 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                     v[4 * j + 2] += f[o][j].z;
                                     v[4 * j + 3] += f[o][j].w;
                                 }
-                            finish(u, v);
+                            finish(u, v, true);
                         }
                     }
                 }
             }
+            if constexpr (CF::MODE != MODE_ROWQ) {
+                if (part && !p.cluster_split) {
+                    // Count this warp's region of the segment in, then (if this
+                    // segment owns boxes of the region) wait for all segments.
+                    // The counter word holds (launch epoch << 8) | arrivals; a word
+                    // left by any earlier launch counts as zero arrivals. Every
+                    // segment of a tile runs at once (each unit takes at most one
+                    // split item, as its last, and the grid is resident), and the
+                    // wait is bounded regardless.
+                    __threadfence();   // this lane's partial stores before the count
+                    __syncwarp();
+                    const bool owns = seg < NUNITS;
+                    unsigned ready = 0;
+                    if (lane == 0) {
+                        unsigned long long* cnt =
+                            p.tail_count + ((w.tile - p.dp_tiles) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
+                        __threadfence();
+                        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), next = 0;
+                        for (int tries = 0; tries < 4096; ++tries) {
+                            next = ((old >> 8) == p.epoch) ? old + 1 : ((p.epoch << 8) | 1ull);
+                            const unsigned long long seen = atomicCAS(cnt, old, next);
+                            if (seen == old) break;
+                            old = seen;
+                        }
+                        if (owns) {
+                            const unsigned long long want = (p.epoch << 8) | static_cast<unsigned long long>(p.split);
+                            unsigned long long seen = next;
+                            const uint64_t t0 = globaltimer();
+                            while (seen != want) {
+                                if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) break;
+                                __nanosleep(32);
+                                asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(seen) : "l"(cnt) : "memory");
+                            }
+                            ready = seen == want ? 1u : 0u;
+                            __threadfence();
+                        }
+                    }
+                    if (owns) {
+                        ready = __shfl_sync(0xffffffffu, ready, 0);
+                        __threadfence();   // the other segments' partials after their count
+                        if (!ready) {
+                            ok = false;
+                        } else {
+                            // Own segment from Tensor Memory (the unit's last item, so
+                            // its accumulator is never overwritten), the others from
+                            // the workspace, all their loads in flight together.
+#pragma unroll U_UNROLL
+                            for (int u = 0; u < NUNITS; ++u) {
+                                if (owner(u) != seg) continue;
+                                float v[32];
+                                load_acc(u, v);
+                                const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
+                                                    ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
+                                                        (UNIT_F4 * 32) +
+                                                    lane;
+                                float4 f[3][UNIT_F4];
+#pragma unroll
+                                for (int o = 0; o < 3; ++o) {
+                                    const int sgi = o + (o >= seg ? 1 : 0);
+#pragma unroll
+                                    for (int j = 0; j < UNIT_F4; ++j)
+                                        f[o][j] = sgi < p.split ? __ldcg(src + sgi * ITEM_F4 + 32 * j)
+                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                                }
+#pragma unroll
+                                for (int o = 0; o < 3; ++o)
+#pragma unroll
+                                    for (int j = 0; j < UNIT_F4; ++j) {
+                                        v[4 * j] += f[o][j].x;
+                                        v[4 * j + 1] += f[o][j].y;
+                                        v[4 * j + 2] += f[o][j].z;
+                                        v[4 * j + 3] += f[o][j].w;
+                                    }
+                                finish(u, v, true);
+                            }
+                        }
+                    }
+                }
+            }
+            if (!ok) break;
         }
         if (!ok) raise_error(p, ERR_TIMEOUT_EPILOGUE, abort_flag);
+        if (!CF::PAIR && p.cluster_split && !cluster_done) {   // the split-K barrier, once per thread
+            __syncwarp();
+            cluster_sync();
+        }
         if (lane == 0) {
             bulk_wait_all();
             if constexpr (CF::MODE == MODE_ROWQ) {
@@ -1051,6 +1174,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             tmem_dealloc_pair(tmem_base, CF::TMEM_COLS);
         }
     } else {
+        // with split-K through the cluster, no CTA leaves while a peer may
+        // still read its parked partials
+        if (p.cluster_split) cluster_sync();
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem_base, CF::TMEM_COLS);

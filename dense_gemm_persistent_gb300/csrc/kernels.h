@@ -10,8 +10,9 @@
 namespace dg {
 
 struct KernelInfo;
+// cluster: CTAs per cluster for kernels that are not CTA pairs (1 = none).
 using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                                 const Params& p, int grid, cudaStream_t s, bool cooperative);
+                                 const Params& p, int grid, cudaStream_t s, bool cooperative, int cluster);
 
 struct KernelInfo {
     int bn, fp8, a_mn, b_mn, mode, pair, gs;
@@ -23,7 +24,7 @@ struct KernelInfo {
 
 template <class CF>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const Params& p,
-                           int grid, cudaStream_t s, bool cooperative) {
+                           int grid, cudaStream_t s, bool cooperative, int cluster) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(CF::NUM_THREADS);
@@ -38,9 +39,9 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
     }
-    if (CF::PAIR) {
+    if (CF::PAIR || cluster > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.x = CF::PAIR ? 2u : static_cast<unsigned>(cluster);
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
         ++n;

@@ -123,6 +123,9 @@ typedef struct {
     int tail_tiles;        /* tiles of the last, partial wave that are split
                               along K so the wave finishes sooner (0 = none)    */
     int tail_split;        /* K segments per tail tile (1 = no splitting)       */
+    int cluster_split;     /* 1: the K segments of each split tile run as one
+                              thread-block cluster and are summed through
+                              distributed shared memory (no workspace needed) */
     size_t smem_bytes;     /* dynamic shared memory per CTA                     */
     size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
 } dgemm_plan_t;

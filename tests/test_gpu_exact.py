@@ -212,34 +212,44 @@ def test_tail_split_default_rule_on_long_tiles():
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
+@pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("shape,layout", [((1024, 1024, 4096), "nk"), ((1024, 1000, 2048), "kn"),
                                           ((520, 776, 1600), "nk")])
-def test_split_k_underfilled_tile_exact(shape, layout):
+def test_split_k_underfilled_tile_exact(shape, layout, cluster, monkeypatch):
     """Grids that do not fill the GPU split every tile along K (up to 4
-    segments); the last-arriving warp adds its own accumulator from TMEM to the
-    others' partials."""
+    segments). Each segment finishes its share of the tile's 32-column units,
+    adding the other segments' partials to its own accumulator from TMEM: read
+    from the peers' shared memory when the segments form a cluster, else from
+    the workspace."""
+    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
     M, N, K = shape
     plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
     assert plan["tail_split"] >= 2 and plan["tail_tiles"] == plan["num_tiles"]
+    assert plan["cluster_split"] == int(cluster)
     got, ref = bf16_case(M, N, K, layout, seed=1000 + K, ws=True)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
+@pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("M,layout", [(1, "nk"), (16, "nk"), (5, "kn"), (40, "nk"), (64, "kn")])
-def test_split_k_small_m_exact(M, layout):
+def test_split_k_small_m_exact(M, layout, cluster, monkeypatch):
     """Small-M (transposed) tiles split along K, with the K groups of each
     segment inside the segment's range."""
+    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
     N, K = 4096, 4096
     plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
     assert plan["swap_ab"] == 1 and plan["tail_split"] >= 2 and plan["k_groups"] > 1
+    assert plan["cluster_split"] == int(cluster)
     got, ref = bf16_case(M, N, K, layout, seed=1100 + M, ws=True)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
-@pytest.mark.parametrize("M", [1, 48])
-def test_split_k_fp8_small_m_exact(M):
-    N, K = 2048, 8192
+@pytest.mark.parametrize("cluster", ["1", "0"])
+@pytest.mark.parametrize("M", [1, 48, 256])
+def test_split_k_fp8_exact(M, cluster, monkeypatch):
+    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
+    N, K = 2048 if M < 256 else 512, 8192
     plan = dg.dgemm_plan(1, M, N, K, "nk", "f32")
-    assert plan["tail_split"] >= 2
+    assert plan["tail_split"] >= 2 and plan["cluster_split"] == int(cluster)
     got, ref = fp8_case(M, N, K, "nk", seed=1200 + M, ws=True)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"

@@ -63,12 +63,14 @@ def test_grouped_small_m_exact(layout, M, g):
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
+@pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 4096), (16, 1024, 4096)])
-def test_grouped_split_k_segments_inside_groups_exact(M, N, K):
+def test_grouped_split_k_segments_inside_groups_exact(M, N, K, cluster, monkeypatch):
     """Under-filled grids split every tile into K segments of 8 slices; with
     groups of 3 slices (384 elements) most segments start inside a group."""
+    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
     plan = dg.dgemm_plan(1, M, N, K, "nk", "f32", num_sms=0)
-    assert plan["tail_split"] > 1
+    assert plan["tail_split"] > 1 and plan["cluster_split"] == int(cluster)
     got, ref = grouped_int_case(M, N, K, 384, "nk", seed=K + M)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
