@@ -460,7 +460,7 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     const int quads = max_quads(dev, devid, fp8);
     st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, quads, true, &plan, k_group);
     if (st != DGEMM_OK) return st;
-    if (plan.split > 1 && (!ws || ws_bytes < plan.pub.workspace_bytes)) {
+    if (plan.split > 1 && plan.pub.workspace_bytes > 0 && (!ws || ws_bytes < plan.pub.workspace_bytes)) {
         st = make_plan(fp8, M, N, K, bl, d_dtype, epi, dev->num_sms, pairs, quads, false, &plan,
                        k_group);  // no room: whole tiles
         if (st != DGEMM_OK) return st;
