@@ -894,22 +894,38 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 const int tcol = cbase + u * UNIT;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                // K groups (the small-M form only): GB loads in flight per wait
+                // (64 registers), then the rest
+                constexpr int GB = CF::MODE == MODE_SWAP ? (UNIT == 32 ? 2 : 4) : 1;
+                int g = g0;
 #pragma unroll 1
-                for (int g = g0; g < g1; ++g) {
-                    const uint32_t ta = taddr + static_cast<uint32_t>(g * CF::BN + tcol);
-                    if constexpr (UNIT == 32) {
-                        uint32_t r[32];
-                        tmem_ld32(ta, r);
-                        tmem_ld_wait();
+                for (; GB > 1 && g + GB <= g1; g += GB) {
+                    uint32_t r[GB][UNIT];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(r[j]);
-                    } else {
-                        uint32_t r[16];
-                        tmem_ld16(ta, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+                    for (int h = 0; h < GB; ++h) {
+                        const uint32_t ta = taddr + static_cast<uint32_t>((g + h) * CF::BN + tcol);
+                        if constexpr (UNIT == 32)
+                            tmem_ld32(ta, r[h]);
+                        else
+                            tmem_ld16(ta, r[h]);
                     }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < GB; ++h)
+#pragma unroll
+                        for (int j = 0; j < UNIT; ++j) v[j] += __uint_as_float(r[h][j]);
+                }
+#pragma unroll 1
+                for (; g < g1; ++g) {
+                    const uint32_t ta = taddr + static_cast<uint32_t>(g * CF::BN + tcol);
+                    uint32_t r[UNIT];
+                    if constexpr (UNIT == 32)
+                        tmem_ld32(ta, r);
+                    else
+                        tmem_ld16(ta, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < UNIT; ++j) v[j] += __uint_as_float(r[j]);
                 }
                 if (p.k_blocks == 0) {
 #pragma unroll
