@@ -328,11 +328,19 @@ def run_ours(args, rank, world, local):
         base = peaks["bf16_tflops"]
         peak = base if w.form == "bf16" else 2.0 * base   # FP8:BF16 dense ratio 2
         unit, bound = "TFLOP/s", "tensor"
+    # The tensor core's rate at the SM clock seen during the timed region:
+    # SMs x dense FLOP per clock per SM (128 x 256 x 16 BF16 or x 32 E4M3 MACs
+    # per 128 cycles, measured at that rate) x the median sampled clock.
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    flop_per_clk = 8192 if w.form == "bf16" else 16384
+    theo = (n_sm * flop_per_clk * clocks["sm_mhz"] * 1e6 / 1e12) if clocks.get("sm_mhz") else None
     traffic = recorded_traffic(workload_key(args))
     roof = {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": f"{peak_kind}" + ("" if w.form == "bf16" or skinny else " bf16 x 2 (FP8:BF16 ratio)"),
             "compulsory_bytes": int(comp),
+            "tensor_peak_at_clock_tflops": None if theo is None else round(theo, 1),
+            "frac_of_peak_at_clock": None if (theo is None or skinny) else round(flops / (ms_step * 1e-3) / 1e12 / theo, 4),
             "tiled_traffic_bytes_no_l2": int(roofline.tiled_read_elements(w.M, w.N, w.K, plan["tile_m"],
                                                                           plan["tile_n"]) * esz
                                              + w.M * w.N * (dsz + c_in))}
