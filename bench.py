@@ -57,6 +57,46 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's);
+    the value itself when no process group is initialised."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (weak scaling: each rank runs the full workload)."""
+    return world * units_per_rank / seconds
+
+
+def parse_clock_rows(text: str) -> dict:
+    """Median SM clock, max clock and power, and the throttle reasons seen in
+    nvidia-smi rows of ClockSampler.FIELDS (csv, noheader, nounits)."""
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        r = [x.strip() for x in line.split(",")]
+        if len(r) < 9:
+            continue
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+            power.append(float(r[3]))
+        except ValueError:
+            continue
+        for name, val in zip(names, r[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -126,26 +166,10 @@ class ClockSampler:
             self.proc.kill()
         self.out.flush()
         self.out.seek(0)
-        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        text = self.out.read()
         self.out.close()
         os.unlink(self.out.name)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                power.append(float(r[3]))
-            except ValueError:
-                continue
-            for name, val in zip(names, r[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_rows(text)
 
 
 def make_workload(args):
@@ -268,16 +292,12 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier()
-    ms_total = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
     if dg.dgemm_query_device_status(stream) != 0:
         raise RuntimeError("device status after the timed region")
     ms_step = ms_total / args.steps
     flops = w.flops
-    tflops = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+    tflops = job_rate(flops * args.steps, world, ms_total * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs -> device, call, result -> host
     host = {k: t.pin_memory() for k, t in w.tensors().items()}
@@ -306,11 +326,7 @@ def run_ours(args, rank, world, local):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = f0.elapsed_time(f1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
 
     # ---- roofline of the kernel (one launch per step)
     plan = dg.dgemm_plan(w.form == "fp8", w.M, w.N, w.K, w.b_layout, w.d_dtype, out_quant=w.out_quant,
@@ -355,7 +371,7 @@ def run_ours(args, rank, world, local):
                    "plan": {k: plan[k] for k in ("swap_ab", "tile_m", "tile_n", "stages", "num_tiles", "grid",
                                                  "cooperative")}},
         "clocks": clocks,
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOPS",
+        "e2e": {"value": round(job_rate(flops, world, e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": args.steps,
         "roofline": roof,

@@ -1,0 +1,90 @@
+"""Host-side logic of bench.py on the CPU: the cross-rank timing of the N-GPU
+(replica) runs over a 2-rank gloo group, the whole-job rate, the clock-sample
+parser, workload selection and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as tdist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    tdist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = [3.0, 5.0][rank]            # rank 1 is the slower one
+        slowest = bench.max_over_ranks(local_ms)
+        rate = bench.job_rate(100.0, world, slowest * 1e-3)
+        tdist.barrier()
+        q.put((rank, slowest, rate))
+    finally:
+        tdist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_rate_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 1000)
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, slowest, rate in got:
+        assert slowest == 5.0                    # every rank sees the slowest rank's time
+        assert rate == pytest.approx(2 * 100.0 / 5e-3)   # units of both ranks over that time
+
+
+def test_max_over_ranks_without_a_group_is_identity():
+    assert bench.max_over_ranks(7.5) == 7.5
+    assert bench.job_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_parse_clock_rows():
+    rows = "\n".join([
+        "0, 1900, 2070, 1200.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1800, 2070, 1350.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2000, 2070, 900.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ])
+    c = bench.parse_clock_rows(rows)
+    assert c["sm_mhz"] == 1900 and c["sm_max_mhz"] == 2070 and c["samples"] == 3
+    assert c["reasons"] == ["sw_power_cap"] and c["power_w_max"] == 1350.0
+    hot = bench.parse_clock_rows("0, 1500, 2070, 1000, 0x40, Active, Active, Not Active, Not Active")
+    assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_workload_selection():
+    class A:
+        config, k_group = 3, 128
+    assert bench.workload_key(A) == "3g128" and "K group" in bench.describe(A)
+    A.k_group = 0
+    assert bench.workload_key(A) == "3"
+    A.config, A.k_group = 2, 128
+    with pytest.raises(SystemExit):
+        bench.make_workload(A)
+
+
+def test_reference_arm_json_line():
+    """--impl reference times the oracle on the host: one JSON line with the
+    contract's keys, the oracle as its cpu_baseline and no host<->device bytes."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "1",
+                        "--steps", "3", "--warmup", "3", "--ref-seconds", "2"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 3
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
