@@ -200,6 +200,10 @@ struct Cfg {
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     // split-K through the cluster parks a whole accumulator in the pipeline buffers
     static_assert(EPI_WARPS * BN / (EPI_WARPS / 4) * 32 * 4 <= STAGES * STAGE_BYTES, "parked partials fit");
+    // the requantisation pass double-buffers 8 KB stash chunks per warp in the
+    // pipeline buffers and keeps its barriers in the staging area
+    static_assert(MODE != MODE_ROWQ || 2 * (NUM_THREADS / 32) * 8192 <= STAGES * STAGE_BYTES, "requant slots fit");
+    static_assert(MODE != MODE_ROWQ || 2 * (NUM_THREADS / 32) * 8 <= STAGING_BYTES, "requant barriers fit");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
@@ -1221,50 +1225,85 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         if (*abort_flag) return;
         // ---------------------------------------------------------- requantise
         // s[m] = amax[m] / 448; q = RN_E4M3(y * (1 / s[m])), saturating.
-        // One warp per output row at a time: lane l converts the 16-element
-        // groups l, l + 32, ... of the row, RQ_UNROLL of them with their loads in
-        // flight together, so the pass runs at memory bandwidth. The row scale
-        // s[m] = amax[m] / 448 is written once per row.
-        constexpr int RQ_UNROLL = 8;
-        const int warps_per_cta = static_cast<int>(blockDim.x) >> 5;
-        const int warps_total = static_cast<int>(gridDim.x) * warps_per_cta;
-        const int groups_per_row = p.N / 16;
-        for (int m = static_cast<int>(blockIdx.x) * warps_per_cta + warp; m < p.M; m += warps_total) {
+        // The stash is streamed through the idle pipeline buffers by bulk
+        // asynchronous copies: it is cut into chunks of up to RQ_CHUNK values of
+        // one row, dealt round-robin to the CTAs and then to their warps; each
+        // warp double-buffers its chunks (two 8 KB slots, one mbarrier each), so
+        // an SM keeps up to 2 x warps x 8 KB of the stash in flight. Lane l
+        // converts 16 values at a time and writes their 16 codes; the row scale
+        // is written by the warp that converts the row's first chunk.
+        constexpr int RQ_CHUNK = 4096;
+        const int nwarps = static_cast<int>(blockDim.x) >> 5;
+        const int64_t cpr = (p.N + RQ_CHUNK - 1) / RQ_CHUNK;   // chunks per row
+        const int64_t nchunks = static_cast<int64_t>(p.M) * cpr;
+        uint8_t* slot0 = stages + static_cast<size_t>(2 * warp) * RQ_CHUNK * 2;
+        uint64_t* rq_bar = reinterpret_cast<uint64_t*>(staging) + 2 * warp;   // epilogue staging is idle too
+        if (lane == 0) {
+            mbar_init(&rq_bar[0], 1);
+            mbar_init(&rq_bar[1], 1);
+            fence_mbarrier_init();
+        }
+        __syncwarp();
+        auto chunk_of = [&](int64_t t) {
+            return static_cast<int64_t>(blockIdx.x) +
+                   static_cast<int64_t>(gridDim.x) * (static_cast<int64_t>(warp) + static_cast<int64_t>(nwarps) * t);
+        };
+        int64_t issued = 0;   // (lane 0) chunks whose copy has been started
+        auto issue = [&](int64_t t) {
+            const int64_t j = chunk_of(t);
+            if (j >= nchunks) return;
+            const int64_t m = j / cpr;
+            const int c0 = static_cast<int>(j % cpr) * RQ_CHUNK;
+            const uint32_t bytes = static_cast<uint32_t>(min(RQ_CHUNK, p.N - c0)) * 2u;
+            fence_proxy_async_smem();   // the slot's earlier reads before the copy rewrites it
+            mbar_arrive_expect_tx(&rq_bar[t & 1], bytes);
+            bulk_load_1d(slot0 + (t & 1) * RQ_CHUNK * 2, p.stash + m * p.N + c0, bytes, &rq_bar[t & 1]);
+            issued = t + 1;
+        };
+        if (lane == 0) {
+            issue(0);
+            issue(1);
+        }
+        bool rq_ok = true;
+        int64_t t = 0;
+        for (; chunk_of(t) < nchunks; ++t) {
+            const int64_t j = chunk_of(t);
+            const int64_t m = j / cpr;
+            const int c0 = static_cast<int>(j % cpr) * RQ_CHUNK;
+            const int len = min(RQ_CHUNK, p.N - c0);   // a multiple of 16 (N is)
             const float amax = __uint_as_float(__ldcg(p.amax + m));
             const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
             const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
-            if (lane == 0) p.out_row_scale[m] = s;
-            const uint4* src = reinterpret_cast<const uint4*>(p.stash + static_cast<int64_t>(m) * p.N);
-            uint4* dst = reinterpret_cast<uint4*>(p.q_out + static_cast<int64_t>(m) * p.N);
-            for (int g0 = lane; g0 < groups_per_row; g0 += 32 * RQ_UNROLL) {
-                uint4 y0[RQ_UNROLL], y1[RQ_UNROLL];
-#pragma unroll
-                for (int u = 0; u < RQ_UNROLL; ++u) {
-                    const int g = g0 + 32 * u;
-                    if (g < groups_per_row) {
-                        y0[u] = __ldcg(src + 2 * g);
-                        y1[u] = __ldcg(src + 2 * g + 1);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < RQ_UNROLL; ++u) {
-                    const int g = g0 + 32 * u;
-                    if (g < groups_per_row) {
-                        const uint32_t w[8] = {y0[u].x, y0[u].y, y0[u].z, y0[u].w,
-                                               y1[u].x, y1[u].y, y1[u].z, y1[u].w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
-                            const uint32_t hi =
-                                pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
-                            o[h] = lo | (hi << 16);
-                        }
-                        dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                }
+            if (lane == 0 && c0 == 0) p.out_row_scale[m] = s;
+            if (!mbar_wait(&rq_bar[t & 1], static_cast<uint32_t>(t >> 1) & 1u, abort_flag)) {
+                rq_ok = false;
+                break;
             }
+            const uint4* src = reinterpret_cast<const uint4*>(slot0 + (t & 1) * RQ_CHUNK * 2);
+            uint4* dst = reinterpret_cast<uint4*>(p.q_out + m * p.N + c0);
+            for (int g = lane; g < len / 16; g += 32) {
+                const uint4 y0 = src[2 * g], y1 = src[2 * g + 1];
+                const uint32_t w[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
+                    const uint32_t hi = pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
+                    o[h] = lo | (hi << 16);
+                }
+                dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            __syncwarp();   // every lane is done with this slot
+            if (lane == 0) issue(t + 2);
         }
+        if (lane == 0) {
+            if (!rq_ok) raise_error(p, ERR_TIMEOUT_EPILOGUE, abort_flag);
+            // no copy into this CTA's shared memory may outlive it
+            for (int64_t u = t + (rq_ok ? 0 : 1); u < issued; ++u)
+                if (!mbar_wait(&rq_bar[u & 1], static_cast<uint32_t>(u >> 1) & 1u, nullptr))
+                    raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
+        }
+        __syncwarp();
     }
 }
 

@@ -260,6 +260,16 @@ __device__ __forceinline__ void fmul2(float& r0, float& r1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Bulk (non-tensor) asynchronous copy global -> shared of `bytes` bytes, its
+// completion counted on `bar` in bytes. Addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared through L2 (cp.async); with
 // src_bytes = 0 the destination is zero-filled and nothing is read.
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
