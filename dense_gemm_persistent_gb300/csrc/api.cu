@@ -110,6 +110,7 @@ struct Plan {
     int group_kb;
     int dp_tiles, split, tail_items;   // tail splitting (MODE_TILE)
     int cluster_split;                 // split K segments of a tile form a cluster of `split` CTAs
+    size_t split_offset;               // workspace offset of the split area (after the requant stash)
     size_t tail_count_bytes;           // workspace: per-warp arrival counters
 };
 
@@ -149,7 +150,8 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     const bool pairs_ok = max_pairs > 0 && !(pair_env && pair_env[0] == '0');
     const char* split_env = std::getenv("DGEMM_TAIL_SPLIT");
     const bool force_split = split_env && split_env[0] == 'f';
-    const bool split_ok = allow_split && !(split_env && split_env[0] == '0') && oq == DGEMM_QUANT_NONE;
+    // (the requantising epilogue takes the tail split, not split-K of under-filled grids)
+    const bool split_ok = allow_split && !(split_env && split_env[0] == '0');
     const char* cl_env = std::getenv("DGEMM_CLUSTER_SPLIT");   // "0": split-K through the workspace only
     if (cl_env && cl_env[0] == '0') max_quads = 0;
     const bool cluster_ok = !(cl_env && cl_env[0] == '0');
@@ -191,7 +193,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
             // under one wave, split-K divides each unit's work (reduction ~15 % of a tile)
             // (the reduction ~15 % of a tile through the workspace, ~5 % when the
             // segments of a single-CTA tile share a cluster)
-            const int64_t sk = split_ok ? underfill_split(tiles, units, kb_all) : 1;
+            const int64_t sk = (split_ok && !oq) ? underfill_split(tiles, units, kb_all) : 1;
             const bool cl = cluster_ok && !c.pair && (sk == 2 || sk == 4) && tiles <= (sk == 2 ? max_pairs : max_quads);
             if (sk > 1) cost = (128.0 * c.bn) * c.penalty * (1.0 / static_cast<double>(sk) + (cl ? 0.05 : 0.15));
             if (cost < best) {
@@ -279,7 +281,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         } else {
             use_split(0, static_cast<int>(sk), p.pub.num_tiles * static_cast<int>(sk));
         }
-    } else if (p.mode == dg::MODE_TILE && split_ok && k_blocks > 0) {
+    } else if ((p.mode == dg::MODE_TILE || p.mode == dg::MODE_ROWQ) && split_ok && k_blocks > 0) {
         const int rem = p.pub.num_tiles % units;
         if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks >= kMinTailSlices)) {
             int64_t split64 = units / rem;
@@ -308,7 +310,18 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.tail_tiles = p.pub.num_tiles - p.dp_tiles;
     p.pub.tail_split = p.split;
     p.pub.cluster_split = p.cluster_split;
-    if (oq) p.pub.workspace_bytes = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
+    // Requantisation: barrier header, row maxima, BF16 stash, then (tail split)
+    // the split area.
+    p.split_offset = 0;
+    if (oq) {
+        const size_t base = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
+        if (p.split > 1) {
+            p.split_offset = round_up(base, 256);
+            p.pub.workspace_bytes += p.split_offset;
+        } else {
+            p.pub.workspace_bytes = base;
+        }
+    }
     *out = p;
     return DGEMM_OK;
 }
@@ -542,8 +555,8 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.split = plan.split;
     p.tail_items = plan.tail_items;
     if (plan.split > 1) {
-        p.tail_count = reinterpret_cast<unsigned long long*>(wsb);
-        p.partials = reinterpret_cast<float*>(wsb + plan.tail_count_bytes);
+        p.tail_count = reinterpret_cast<unsigned long long*>(wsb + plan.split_offset);
+        p.partials = reinterpret_cast<float*>(wsb + plan.split_offset + plan.tail_count_bytes);
         p.epoch = next_epoch();
     }
     if (plan.mode == dg::MODE_ROWQ) {
@@ -685,7 +698,10 @@ extern "C" dgemm_status_t dgemm_fp8_rowquant_noalloc(const void* Aq, const void*
                                                      const dgemm_epilogue_t* epi, dgemm_stream_t stream) {
     if (!epi || epi->out_quant != DGEMM_QUANT_E4M3_ROW_AMAX) return DGEMM_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0) return DGEMM_ERR_INVALID_VALUE;
-    if (dgemm_workspace_size(1, M, N, K, b_layout, epi) > DGEMM_NOALLOC_SCRATCH_BYTES)
+    // the requantising scratch without a split area (with too little room for
+    // one, run() keeps whole tiles)
+    const size_t need = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || need > DGEMM_NOALLOC_SCRATCH_BYTES)
         return DGEMM_ERR_WORKSPACE_TOO_SMALL;
     DeviceState* dev = nullptr;
     int devid = 0;

@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             if constexpr (CF::MODE == MODE_SWAP)
                 if (p.bias && row < p.M) bias_row = p.bias[row];
             float rowmax = 0.0f;
-            const bool part = (CF::MODE != MODE_ROWQ) && w.item >= 0;   // a K segment of a split tile
+            const bool part = w.item >= 0;   // a K segment of a split tile
 
             // Per-K-group scales: fold each scale group's product into gsum as
             // soon as the MMA warp has finished it, then hand its buffer back.
@@ -943,12 +943,20 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             auto finish = [&](int u, float (&v)[32], bool direct) {
                 const int col0 = nb * CF::BN + cbase + u * UNIT;
                 epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row);
-                if constexpr (CF::MODE == MODE_TILE) {
+                if constexpr (CF::MODE == MODE_ROWQ) {
+                    if (row < p.M) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) rowmax = fmaxf(rowmax, fabsf(v[j]));
+                    }
+                }
+                if constexpr (CF::MODE == MODE_TILE || CF::MODE == MODE_ROWQ) {
                     if (direct) {
-                        // row-major D, this thread's row: 16-byte chunks, each wholly
-                        // inside or outside N (N is a multiple of 8 for BF16, 4 for FP32)
+                        // row-major D (the BF16 stash for requantisation), this
+                        // thread's row: 16-byte chunks, each wholly inside or outside
+                        // N (N is a multiple of 8 for BF16, 4 for FP32)
                         if (row < p.M) {
-                            if (p.d_f32) {
+                            if (CF::MODE == MODE_TILE && p.d_f32) {
                                 float* d = static_cast<float*>(p.D) + static_cast<int64_t>(row) * p.ldd + col0;
 #pragma unroll
                                 for (int c = 0; c < 8; ++c)
@@ -956,7 +964,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                         *reinterpret_cast<float4*>(d + 4 * c) =
                                             make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
                             } else {
-                                uint16_t* d = static_cast<uint16_t*>(p.D) + static_cast<int64_t>(row) * p.ldd + col0;
+                                uint16_t* d = (CF::MODE == MODE_ROWQ ? const_cast<uint16_t*>(p.stash)
+                                                                     : static_cast<uint16_t*>(p.D)) +
+                                              static_cast<int64_t>(row) * p.ldd + col0;
 #pragma unroll
                                 for (int c = 0; c < 4; ++c)
                                     if (col0 + 8 * c < p.N)
@@ -985,13 +995,6 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             }
                     }
                 } else {
-                    if constexpr (CF::MODE == MODE_ROWQ) {
-                        if (row < p.M) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (col0 + j < p.N) rowmax = fmaxf(rowmax, fabsf(v[j]));
-                        }
-                    }
                     tile_store_unit<CF>(v, p, u, col0, row_base, lane, stg, stores, &tmD);
                 }
             };
@@ -1088,7 +1091,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     }
                 }
             }
-            if constexpr (CF::MODE != MODE_ROWQ) {
+            {
                 if (part && !p.cluster_split) {
                     // Count this warp's region of the segment in, then (if this
                     // segment owns boxes of the region) wait for all segments.
@@ -1163,6 +1166,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                     }
                                 finish(u, v, true);
                             }
+                            if constexpr (CF::MODE == MODE_ROWQ) {   // the row maxima of the units finished here
+                                if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
+                            }
                         }
                     }
                 }
@@ -1170,6 +1176,12 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             if (!ok) break;
         }
         if (!ok) raise_error(p, ERR_TIMEOUT_EPILOGUE, abort_flag);
+        if constexpr (CF::MODE == MODE_ROWQ) {
+            // stash rows written with plain stores (split tiles) are read by the
+            // requantisation pass's bulk copies (async proxy)
+            fence_proxy_async_global();
+            __threadfence();
+        }
         if (!CF::PAIR && p.cluster_split && !cluster_done) {   // the split-K barrier, once per thread
             __syncwarp();
             cluster_sync();

@@ -85,8 +85,12 @@ def test_argument_errors_return_before_any_device_call(lib):
 
 
 def test_workspace_sizes(lib, monkeypatch):
+    # requantisation: barrier header, row maxima, BF16 stash; 1024 tiles on 76
+    # pairs leave 36 for the last wave, split in halves: plus counters and one
+    # 256 x 256 FP32 partial per unit
+    base = 256 + 8192 * 4 + 8192 * 8192 * 2
     ws = dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax")
-    assert ws == 256 + 8192 * 4 + 8192 * 8192 * 2
+    assert ws == base + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
     # tail splitting: 256 tiles on 76 pairs leave 28 tiles for the last wave; the
     # workspace bounds one 256 x 256 FP32 partial per unit plus the counters
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
@@ -96,6 +100,7 @@ def test_workspace_sizes(lib, monkeypatch):
     assert dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)["tail_split"] == 1
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "0")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)["workspace_bytes"] == 0
+    assert dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax") == base
 
 
 def test_plans_for_the_five_workloads(lib):

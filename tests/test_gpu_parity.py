@@ -140,6 +140,23 @@ def test_fp8_with_c_bias_and_f32_output(M):
     assert ok, msg
 
 
+def test_requant_tail_split(monkeypatch):
+    """The requantising epilogue with the last partial wave split along K: the
+    split tiles' segments finish their units with plain stores into the stash
+    and fold their row maxima in before the grid barrier. 90 tiles of 256 x 256
+    on 76 pairs: the last 14 (rows 2048-2559 in the banded raster) are split."""
+    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
+    w = wl.make(5, M=2560, N=2304, K=2048)
+    plan = dg.dgemm_plan(1, w.M, w.N, w.K, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=0)
+    if plan["cta_group"] != 2 or plan["grid"] != 152:
+        pytest.skip("needs 76 resident CTA pairs")
+    assert plan["tail_tiles"] == 14 and plan["tail_split"] == 2
+    q, s = run_workload(w)
+    rows = np.array(sorted(set(range(2048, 2560, 23)) | {0, 1000, 2047, 2559}), dtype=np.int64)
+    ok, msg = requant_ok(q.numpy()[rows], s.numpy()[rows], ref_of(w, rows=rows))
+    assert ok, msg
+
+
 def test_requant_from_bf16_form():
     w = wl.make(2, M=300, N=512, K=640)
     w.bias = torch.from_numpy(np.random.default_rng(6).standard_normal(512).astype(np.float32) * 0.01)
