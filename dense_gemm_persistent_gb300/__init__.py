@@ -36,15 +36,16 @@ def _dtype_code(t) -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # plain ints: ctypes converts them for the c_void_p parameters
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     if stream is None:
-        return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+        return _torch().cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 def _dims(A, B, b_layout):

@@ -63,6 +63,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     """The loaded libdgemm.so. Raises RuntimeError if it is not built (unless
     build_if_missing, which runs nvcc)."""
     global _lib
+    lib = _lib
+    if lib is not None:   # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
