@@ -172,10 +172,26 @@ class ClockSampler:
         return parse_clock_rows(text)
 
 
+def parse_shape(text: str):
+    m, n, k = (int(x) for x in text.replace("x", ",").split(","))
+    if min(m, n, k) <= 0:
+        raise SystemExit("--shape wants positive M,N,K")
+    return m, n, k
+
+
 def make_workload(args):
-    """The workload a run times: one of the five, or with --k-group, workload 3's
-    shape and recipe with per-K-group scales."""
+    """The workload a run times: one of the five; with --k-group, workload 3's
+    shape and recipe with per-K-group scales; with --shape M,N,K, workload 2's
+    BF16 recipe at that size with B stored N x K (the weight layout)."""
     import workloads as wl
+    if getattr(args, "shape", None):
+        if args.config != 2 or getattr(args, "k_group", 0):
+            raise SystemExit("--shape applies to workload 2's BF16 recipe")
+        M, N, K = parse_shape(args.shape)
+        w = wl.make(2, M=M, N=N, K=K)
+        w.B = w.B.t().contiguous()
+        w.b_layout = "nk"
+        return w
     if getattr(args, "k_group", 0):
         if args.config != 3:
             raise SystemExit("--k-group applies to workload 3 (FP8 E4M3 4096 x 11008 x 4096)")
@@ -184,11 +200,16 @@ def make_workload(args):
 
 
 def workload_key(args) -> str:
+    if getattr(args, "shape", None):
+        return "2s" + "x".join(str(v) for v in parse_shape(args.shape))
     return f"{args.config}g{args.k_group}" if getattr(args, "k_group", 0) else str(args.config)
 
 
 def describe(args) -> str:
     d = DESCRIPTIONS[args.config]
+    if getattr(args, "shape", None):
+        M, N, K = parse_shape(args.shape)
+        return f"BF16 GEMM M={M} N={N} K={K}, entries N(0,1)/sqrt(K), B stored N x K -> BF16 D"
     if getattr(args, "k_group", 0):
         d = d.replace("per-token x per-channel scales",
                       f"per-(token, {args.k_group}-element K group) x per-(channel, K group) scales")
@@ -331,11 +352,13 @@ def run_ours(args, rank, world, local):
     # ---- roofline of the kernel (one launch per step)
     plan = dg.dgemm_plan(w.form == "fp8", w.M, w.N, w.K, w.b_layout, w.d_dtype, out_quant=w.out_quant,
                          act=w.act, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
-    skinny = args.config == 4
     dsz = {"f32": 4, "bf16": 2, "e4m3": 1}[w.d_dtype]
     esz = 2 if w.form == "bf16" else 1
     c_in = 4 if (w.C is not None and w.beta != 0) else 0
     comp = roofline.compulsory_bytes(w.M, w.N, w.K, esz, esz, c_in, dsz)
+    # HBM-bound: workload 4, or a --shape whose intensity is below the ridge point
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    skinny = args.config == 4 or (bool(args.shape) and flops / comp < ridge)
     if skinny:
         achieved = comp / (ms_step * 1e-3) / 1e9
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
@@ -391,13 +414,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU time spent on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K: workload 2's BF16 recipe at this size, B stored N x K (e.g. 1024,1024,4096)")
     ap.add_argument("--k-group", type=int, default=0,
                     help="workload 3 with per-K-group FP8 scales of this group size (multiple of 128)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="wall time the reference arm spends on warm-up + steps")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = DEFAULT_STEPS[args.config]
+        args.steps = 2000 if args.shape else DEFAULT_STEPS[args.config]
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()
 

@@ -88,3 +88,14 @@ def test_reference_arm_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_shape_option():
+    class A:
+        config, k_group, shape = 2, 0, "64,256,128"
+    w = bench.make_workload(A)
+    assert (w.M, w.N, w.K, w.b_layout) == (64, 256, 128, "nk") and tuple(w.B.shape) == (256, 128)
+    assert bench.workload_key(A) == "2s64x256x128" and "M=64 N=256 K=128" in bench.describe(A)
+    A.config = 3
+    with pytest.raises(SystemExit):
+        bench.make_workload(A)
