@@ -292,18 +292,34 @@ __device__ __forceinline__ void gs_fold(float* sum, const uint32_t (&r)[UNIT], f
     }
 }
 
+// Column j of a warp's columns from the per-lane float4 vectors that hold
+// them (lane l holds columns 4l .. 4l + 3): a warp shuffle, no memory access.
+__device__ __forceinline__ float4 lane_f4(const float4& x, int src_lane) {
+    return make_float4(__shfl_sync(0xffffffffu, x.x, src_lane), __shfl_sync(0xffffffffu, x.y, src_lane),
+                       __shfl_sync(0xffffffffu, x.z, src_lane), __shfl_sync(0xffffffffu, x.w, src_lane));
+}
+
 // The FP32 epilogue arithmetic shared by all modes for 32 consecutive columns
 // of one row: v = alpha * (rs * cs[j] * acc) + beta * c[j] + bias[j], then act.
+// Tile modes take the column scales and bias from per-lane float4 vectors
+// loaded before the accumulator was ready (cs_l, bias_l: lane l holds the
+// warp's columns 4l .. 4l + 3; this unit starts at lane lane0); the
+// transposed small-M form reads its column scales directly.
 template <bool SWAP>
 __device__ __forceinline__ void epilogue_math(float (&v)[32], const Params& p, int row, int col0,
-                                              int ncols, float rs, float bias_row) {
+                                              int ncols, float rs, float bias_row, const float4& cs_l,
+                                              const float4& bias_l, int lane0) {
     const bool row_ok = row < p.M;
     // column-indexed scale (per MMA column)
     if (p.col_scale) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            if (j < ncols && col0 + j < p.N) {
-                const float4 s = ld_bcast4(p.col_scale, col0 + j, p.N);
+            if (j < ncols) {
+                float4 s;
+                if constexpr (SWAP)
+                    s = col0 + j < p.N ? ld_bcast4(p.col_scale, col0 + j, p.N) : make_float4(0.f, 0.f, 0.f, 0.f);
+                else
+                    s = lane_f4(cs_l, lane0 + j / 4);
                 v[j] *= s.x; v[j + 1] *= s.y; v[j + 2] *= s.z; v[j + 3] *= s.w;
             }
         }
@@ -359,8 +375,8 @@ __device__ __forceinline__ void epilogue_math(float (&v)[32], const Params& p, i
         if (p.bias) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
-                if (j < ncols && col0 + j < p.N) {
-                    const float4 b = ld_bcast4(p.bias, col0 + j, p.N);
+                if (j < ncols) {
+                    const float4 b = lane_f4(bias_l, lane0 + j / 4);
                     v[j] += b.x; v[j + 1] += b.y; v[j + 2] += b.z; v[j + 3] += b.w;
                 }
         }
@@ -776,6 +792,26 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             int mb, nb;
             tile_coords(w.tile, p, mb, nb);
             const int buf = local & 1;
+            const int row_base = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM + q * 32;
+            const int row = row_base + lane;
+            // The item's scales and bias do not depend on the MMA: fetch them
+            // before waiting for the accumulator. Tile modes: lane l takes the
+            // warp's columns 4l .. 4l + 3 (0 past N), shared by shuffles later.
+            const float rs = (p.row_scale && row < p.M) ? p.row_scale[row] : 1.0f;
+            float bias_row = 0.0f;
+            if constexpr (CF::MODE == MODE_SWAP)
+                if (p.bias && row < p.M) bias_row = p.bias[row];
+            float4 cs_l = make_float4(1.f, 1.f, 1.f, 1.f), bias_l = make_float4(0.f, 0.f, 0.f, 0.f);
+            // (per-K-group-scale kernels have no column scale here, and fetch
+            // their bias after the group loop, whose running sum fills the registers)
+            auto load_cols = [&]() {
+                const int cl = nb * CF::BN + cbase + 4 * lane;
+                if (4 * lane < CF::EPI_COLS && cl < p.N) {
+                    if (!CF::GS && p.col_scale) cs_l = ld_bcast4(p.col_scale, cl, p.N);
+                    if (p.bias) bias_l = ld_bcast4(p.bias, cl, p.N);
+                }
+            };
+            if constexpr (CF::MODE != MODE_SWAP && !CF::GS) load_cols();
             if constexpr (!CF::GS) {
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) {
@@ -784,8 +820,6 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
                 tc_fence_after();
             }
-            const int row_base = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM + q * 32;
-            const int row = row_base + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * p.acc_stride);
             // the K groups this item accumulated (a K segment touches only its own)
@@ -794,10 +828,6 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 g0 = (w.kb0 * p.acc_groups) / p.k_blocks;
                 g1 = ((w.kb1 - 1) * p.acc_groups) / p.k_blocks + 1;
             }
-            const float rs = (p.row_scale && row < p.M) ? p.row_scale[row] : 1.0f;
-            float bias_row = 0.0f;
-            if constexpr (CF::MODE == MODE_SWAP)
-                if (p.bias && row < p.M) bias_row = p.bias[row];
             float rowmax = 0.0f;
             const bool part = w.item >= 0;   // a K segment of a split tile
 
@@ -889,6 +919,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 if (!ok) break;
             }
 
+            if constexpr (CF::MODE != MODE_SWAP && CF::GS) load_cols();
+
             // The accumulator of 32 (or 16) columns, FP32 sum of its K groups.
             auto load_acc = [&](int u, float (&v)[32]) {
                 if constexpr (CF::GS) {
@@ -942,7 +974,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // segments of a split tile each finish single units).
             auto finish = [&](int u, float (&v)[32], bool direct) {
                 const int col0 = nb * CF::BN + cbase + u * UNIT;
-                epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row);
+                epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row, cs_l, bias_l,
+                                                     u * UNIT / 4);
                 if constexpr (CF::MODE == MODE_ROWQ) {
                     if (row < p.M) {
 #pragma unroll
