@@ -242,11 +242,11 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
 
     // Tail splitting: when the tiles do not fill the last wave, run the full
     // waves whole and split each leftover tile along K into as many segments
-    // as there are idle units (2), so the wave ends after half a tile instead
-    // of a whole one. Needs workspace for FP32 partials, bounded by one
-    // tile-sized partial per unit. The partials' round trip through L2 costs a
-    // few microseconds, so only long tiles (>= kMinTailSlices K slices) are
-    // split, and problems with no full wave are left alone.
+    // as there are idle units (at most 2), so the wave ends after half a tile
+    // instead of a whole one. Needs workspace for FP32 partials, bounded by
+    // one tile-sized partial per unit. The partials' round trip through L2
+    // costs a few microseconds, so only long tiles (>= kMinTailSlices K
+    // slices) are split, and problems with no full wave are left alone.
     // DGEMM_TAIL_SPLIT=0 disables splitting, =force drops the length rule.
     const int64_t k_blocks = (K + p.bk - 1) / p.bk;
     p.dp_tiles = p.pub.num_tiles;

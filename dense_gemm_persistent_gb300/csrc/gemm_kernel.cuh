@@ -5,20 +5,31 @@
 // its own 128 rows of A and half of the B tile, the even CTA issues
 // tcgen05.mma.cta_group::2 over both, and each CTA's Tensor Memory holds its
 // 128 rows of the accumulator. Per SM this halves the B traffic from L2 and
-// leaves room for more pipeline stages. Each CTA's six warps split the work:
+// leaves room for more pipeline stages. The warps of a CTA split the work:
 //   warp 0     TMA producer: streams 128-byte-wide K slices of A and B into an
 //              S-stage shared-memory ring (128B swizzle), one mbarrier pair
 //              (full / empty) per stage.
 //   warp 1     MMA issuer: one thread issues tcgen05.mma for each K slice into
 //              one of two FP32 accumulators in Tensor Memory and commits the
 //              stage back to the producer; owns the TMEM allocation.
-//   warps 2-9  epilogue (2-5 for the small-M form): read the finished
-//              accumulator with tcgen05.ld (each warp a 32-lane quarter and half
-//              of the columns, one output row per thread), apply
+//   epilogue   warps 2-9 (2-5 for the small-M form and 64-wide tiles): read the
+//              finished accumulator with tcgen05.ld (each warp a 32-lane quarter
+//              and part of the columns, one output row per thread), apply
 //              scales, alpha/beta, bias and activation in FP32, convert once,
 //              and write through swizzled shared memory with TMA stores (or,
 //              for the transposed small-M form, with coalesced direct stores),
 //              while the MMA warp fills the other accumulator.
+// Per-K-group-scale tile kernels (GS) use warp 2 as a scale producer, leave
+// warp 3 idle and run the epilogue on warps 4-11; their epilogue folds every
+// group's product into an FP32 running sum in registers.
+//
+// Work items are whole tiles or K segments of split tiles (the last partial
+// wave, or every tile of a grid that does not fill the GPU); each segment
+// finishes its share of the tile's 32-column units, reading the other
+// segments' partials from the workspace or, when the segments form one
+// cluster, from the peers' shared memory. The requantising form (MODE_ROWQ)
+// ends with a grid barrier and a pass that turns the BF16 stash into E4M3
+// codes with per-row scales.
 //
 // The method is the one the pages describe -- tiles of C per block, K walked in
 // slices through a multi-buffered shared-memory pipeline, FP32 accumulation,
@@ -84,12 +95,13 @@ struct Params {
     uint8_t* q_out;          // [M,N] E4M3 codes
     float* out_row_scale;    // [M]
     unsigned* status;        // sticky device error word
-    // Tail splitting (MODE_TILE): tiles [0, dp_tiles) run whole; each of the
+    // Split tiles (all modes): tiles [0, dp_tiles) run whole; each of the
     // remaining tiles is split along K into `split` segments (tail_items in
-    // all), every unit taking at most one. Each epilogue warp writes its region
-    // of a segment's FP32 accumulator to `partials` and counts it in
-    // tail_count; the last warp to arrive for a region sums the region's
-    // partials and runs the epilogue on it.
+    // all), every unit taking at most one, as its last item. 32-column unit u
+    // of each epilogue warp's region belongs to segment u % split: a segment
+    // parks the units others own as FP32 partials in `partials`, counts its
+    // arrival in tail_count, waits (bounded) for every segment of the region,
+    // and finishes its own units from its accumulator plus the others' partials.
     int dp_tiles, split, tail_items;
     float* partials;         // [tail_items][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4
     // Split-K through distributed shared memory (single-CTA kernels, under-

@@ -135,11 +135,16 @@ typedef struct {
  *   C        [M,N] of c_dtype (F32 or BF16); read only when beta != 0.
  *   D        [M,N] of d_dtype: F32 or BF16, or E4M3 with
  *            epi->out_quant == DGEMM_QUANT_E4M3_ROW_AMAX.
- *   ws       device workspace of ws_bytes bytes. Required (at least
- *            dgemm_workspace_size(0, ...)) with the requantising epilogue.
- *            Otherwise optional: when it is at least that size, the last
- *            partial wave of tiles is split along K across the idle SMs (FP32
- *            partials in the workspace); with less, tiles are never split.
+ *   ws       device workspace of ws_bytes bytes, its contents arbitrary on
+ *            entry. With the requantising epilogue it is required: at least
+ *            256 + 4 * ceil(M / 64) * 64 + 2 * M * N bytes (barrier header, row
+ *            maxima, BF16 stash); dgemm_workspace_size(...) also counts room
+ *            for splitting the last partial wave of tiles along K. Otherwise
+ *            optional: with at least dgemm_workspace_size(...) bytes, tiles may
+ *            be split along K (the last partial wave, or every tile when the
+ *            tiles do not fill the GPU) with FP32 partials in the workspace;
+ *            with less, only splits that need no workspace are made (the K
+ *            segments of a tile running as one thread-block cluster).
  * [W1] §1.1, §3.1, §6. */
 dgemm_status_t dgemm_bf16(const void* A, const void* B, dgemm_b_layout_t b_layout,
                           const void* C, dgemm_dtype_t c_dtype,
