@@ -33,6 +33,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("swap_ab", _i32), ("tile_m", _i32), ("tile_n", _i32), ("cta_group", _i32), ("stages", _i32),
                 ("num_tiles", _i32), ("grid", _i32), ("cooperative", _i32), ("raster_group", _i32), ("k_groups", _i32),
                 ("tail_tiles", _i32), ("tail_split", _i32), ("cluster_split", _i32),
+                ("tail_halves", _i32),
                 ("smem_bytes", _sz), ("workspace_bytes", _sz)]
 
 

@@ -110,6 +110,7 @@ struct Plan {
     int group_kb;
     int dp_tiles, split, tail_items;   // tail splitting (MODE_TILE)
     int cluster_split;                 // split K segments of a tile form a cluster of `split` CTAs
+    int tail_halves;                   // tail tiles run as two N halves (tail_items = 2 x tail tiles)
     size_t split_offset;               // workspace offset of the split area (after the requant stash)
     size_t tail_count_bytes;           // workspace: per-warp arrival counters
 };
@@ -290,6 +291,22 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
             const int split = static_cast<int>(split64);
             if (split >= 2) use_split(p.pub.num_tiles - rem, split, rem * split);
         }
+        // N halves (CTA-pair 256-wide kernels) where the K split does not
+        // apply: when twice the leftover tiles fit in the last wave, each runs
+        // as two 256 x 128 halves over the whole K range, with no partials,
+        // reduction or workspace. A half does half the MMA work but reads
+        // three quarters of the tile's operand bytes, so on long tiles the K
+        // split (half of both) finishes the wave sooner despite its reduction:
+        // 4096^3 BF16 ran at 1654 TFLOP/s split along K, 1590 in halves;
+        // FP8 4096 x 11008 x 4096 (too short to split) at 3197 in halves,
+        // 3165 with whole tiles. DGEMM_TAIL_HALVES=0 disables it.
+        const char* halves_env = std::getenv("DGEMM_TAIL_HALVES");
+        if (p.split == 1 && rem > 0 && k->halves && 2 * rem <= units && !(halves_env && halves_env[0] == '0')) {
+            p.tail_halves = 1;
+            p.dp_tiles = p.pub.num_tiles - rem;
+            p.tail_items = 2 * rem;
+            p.pub.grid = pair_ctas(pair) * (p.dp_tiles > 0 ? units : p.tail_items);
+        }
     }
     // K-group promotion. The transposed small-M kernel owns all 512 TMEM
     // columns but needs only BN per accumulator: it splits K into as many
@@ -310,6 +327,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.tail_tiles = p.pub.num_tiles - p.dp_tiles;
     p.pub.tail_split = p.split;
     p.pub.cluster_split = p.cluster_split;
+    p.pub.tail_halves = p.tail_halves;
     // Requantisation: barrier header, row maxima, BF16 stash, then (tail split)
     // the split area.
     p.split_offset = 0;
@@ -485,9 +503,10 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     const dgemm_dtype_t in_t = fp8 ? DGEMM_E4M3 : DGEMM_BF16;
     const size_t esz = fp8 ? 1 : 2;
     const int mn_atom = static_cast<int>(128 / esz);
-    alignas(64) CUtensorMap tmA, tmB, tmD;
+    alignas(64) CUtensorMap tmA, tmB, tmBh, tmD;
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);
+    std::memset(&tmBh, 0, sizeof tmBh);
     std::memset(&tmD, 0, sizeof tmD);
     // The MMA's operands: X (rows of the MMA's M) and Y (rows of its N).
     const void* X = plan.pub.swap_ab ? B : A;
@@ -505,6 +524,12 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
             ok = encode_2d(&tmB, tm_type(in_t), Y, K, plan.Nm, K * esz, plan.bk,
                            static_cast<uint32_t>(plan.pub.tile_n / plan.pub.cta_group));
         if (!ok) return DGEMM_ERR_CUDA;
+        // a tail half's B rows: half the box of K-major B (MN-major B loads
+        // whole atoms through tmB)
+        if (plan.tail_halves && !plan.b_mn &&
+            !encode_2d(&tmBh, tm_type(in_t), Y, K, plan.Nm, K * esz, plan.bk,
+                       static_cast<uint32_t>(plan.pub.tile_n / plan.pub.cta_group / 2)))
+            return DGEMM_ERR_CUDA;
     }
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     const size_t amax_bytes = round_up(static_cast<size_t>(M) * 4, 256);
@@ -568,7 +593,9 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
         if (cudaMemsetAsync(ws, 0, kWsHeader + amax_bytes, stream) != cudaSuccess) return DGEMM_ERR_CUDA;
     }
     p.cluster_split = plan.cluster_split;
-    if (k->launch(tmA, tmB, tmD, p, plan.pub.grid, stream, plan.pub.cooperative != 0,
+    p.tail_halves = plan.tail_halves;
+    if (plan.tail_halves && !k->halves) return DGEMM_ERR_NOT_SUPPORTED;
+    if (k->launch(tmA, tmB, tmBh, tmD, p, plan.pub.grid, stream, plan.pub.cooperative != 0,
                   plan.cluster_split ? plan.split : 1) != cudaSuccess)
         return DGEMM_ERR_CUDA;
     return DGEMM_OK;

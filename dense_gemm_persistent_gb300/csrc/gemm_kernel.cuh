@@ -109,6 +109,10 @@ struct Params {
     // cluster of `split` CTAs (rank = segment); partials go through the idle
     // pipeline buffers and the peers' shared memory instead of the workspace.
     int cluster_split;
+    // Tail tiles split along N instead (CTA-pair 256-wide kernels): each of
+    // the tiles from dp_tiles on is run as two 256 x 128 halves (tail_items =
+    // 2 x those tiles), each a whole K range with an N = 128 MMA; no partials.
+    int tail_halves;
     unsigned long long* tail_count;  // [num_tiles - dp_tiles][CTAS][EPI_WARPS]: (epoch << 8) | arrivals
     unsigned long long epoch;        // unique per launch (56 bits): stale counters need no clearing
 };
@@ -116,12 +120,14 @@ struct Params {
 // One unit of work: a whole tile (item < 0) or one K segment of a split tile.
 struct Work {
     int tile, kb0, kb1, item;
+    int half;   // -1: the whole tile; 0 / 1: that 128-column half (tail_halves)
 };
 
 // The iter-th work item of a unit (a CTA, or a CTA pair): first its whole
 // tiles unit, unit + units, ... below dp_tiles, then tail items likewise.
 __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, int iter, Work& w) {
     const int dp_count = p.dp_tiles > unit ? (p.dp_tiles - unit + units - 1) / units : 0;
+    w.half = -1;
     if (iter < dp_count) {
         w.tile = unit + iter * units;
         w.kb0 = 0;
@@ -131,6 +137,14 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
     }
     const int j = unit + (iter - dp_count) * units;
     if (j >= p.tail_items) return false;
+    if (p.tail_halves) {
+        w.tile = p.dp_tiles + j / 2;
+        w.half = j % 2;
+        w.kb0 = 0;
+        w.kb1 = p.k_blocks;
+        w.item = -1;
+        return true;
+    }
     const int seg = j % p.split;
     w.tile = p.dp_tiles + j / p.split;
     w.kb0 = (seg * p.k_blocks) / p.split;
@@ -186,6 +200,12 @@ struct Cfg {
                                    : (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr uint32_t IDESC = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, TILE_M, BN);
+    // tail halves (PAIR, BN = 256): N = 128 per pair, 64 B rows per CTA
+    // Tail tiles as two N halves: each CTA loads 64 rows of B (K-major), or
+    // whole 128-byte atoms of it (MN-major; one for BF16, none fits for E4M3).
+    static constexpr bool HALVES = PAIR && BN == 256 && !GS && (!B_MN || (BN_CTA / 2) % MN_ATOM == 0);
+    static constexpr uint32_t IDESC_HALF = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, TILE_M, BN / 2);
+    static constexpr int B_BYTES_HALF = BN_CTA / 2 * 128;
     // Per-K-group scales keep each epilogue thread's share of the running sum
     // (EPI_COLS FP32 values) in registers. With 8 epilogue warps that needs more
     // than the 168 registers a thread of a 10-warp block can have, so those
@@ -441,6 +461,7 @@ __device__ __forceinline__ void tile_store_unit(const float (&v)[32], const Para
 template <class CF>
 __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmBh,
                     const __grid_constant__ CUtensorMap tmD, const Params p) {
     constexpr int S = CF::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -533,7 +554,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     int mb, nb;
                     tile_coords(w.tile, p, mb, nb);
                     const int row0 = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM;   // this CTA's A rows
-                    const int col0 = nb * CF::BN + static_cast<int>(rank) * CF::BN_CTA;  // this CTA's B rows
+                    // this CTA's B rows (of a tail half: its 64 of the half's 128)
+                    const bool half = CF::HALVES && w.half >= 0;
+                    const int col0 = half ? nb * CF::BN + w.half * (CF::BN / 2) + static_cast<int>(rank) * (CF::BN_CTA / 2)
+                                          : nb * CF::BN + static_cast<int>(rank) * CF::BN_CTA;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                             ok = false;
@@ -544,15 +568,20 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         const int k0 = kb * CF::BK;
                         if constexpr (CF::PAIR) {
                             // both CTAs' copies complete on the leader's full barrier
-                            if (rank == 0) mbar_arrive_expect_tx(&full[stage], CF::CTAS * CF::STAGE_BYTES);
+                            if (rank == 0)
+                                mbar_arrive_expect_tx(&full[stage],
+                                                      CF::CTAS * (half ? CF::A_BYTES + CF::B_BYTES_HALF : CF::STAGE_BYTES));
                             const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
                             tma_load_2d_pair(sa, &tmA, fb, k0, row0, pol);
                             if constexpr (CF::B_MN) {
+                                // 128-byte atoms of MN_ATOM columns each (a half loads the first ones only)
+                                const int atoms = (half ? CF::BN_CTA / 2 : CF::BN_CTA) / CF::MN_ATOM;
     #pragma unroll
                                 for (int i = 0; i < CF::BN_CTA / CF::MN_ATOM; ++i)
-                                    tma_load_2d_pair(sb + i * CF::BK * 128, &tmB, fb, col0 + i * CF::MN_ATOM, k0, pol);
+                                    if (i < atoms)
+                                        tma_load_2d_pair(sb + i * CF::BK * 128, &tmB, fb, col0 + i * CF::MN_ATOM, k0, pol);
                             } else {
-                                tma_load_2d_pair(sb, &tmB, fb, k0, col0, pol);
+                                tma_load_2d_pair(sb, half ? &tmBh : &tmB, fb, k0, col0, pol);
                             }
                         } else {
                             mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
@@ -614,7 +643,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 Work w;
                 // The MMAs of one K slice (a pipeline stage) into accumulator d_tmem;
                 // `first` starts a fresh accumulation.
-                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first) {
+                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc) {
                     const uint64_t ad = a_desc0 + st * STAGE_STEP;
                     const uint64_t bd = b_desc0 + st * STAGE_STEP;
     #pragma unroll
@@ -622,14 +651,14 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         const uint32_t acc = (!first || k > 0) ? 1u : 0u;
                         if constexpr (CF::PAIR) {
                             if constexpr (CF::FP8)
-                                mma_f8_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                                mma_f8_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
                             else
-                                mma_bf16_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                                mma_bf16_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
                         } else {
                             if constexpr (CF::FP8)
-                                mma_f8(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                                mma_f8(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
                             else
-                                mma_bf16(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, CF::IDESC, acc);
+                                mma_bf16(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
                         }
                     }
                     // the stage is free (in both CTAs of a pair) once these MMAs have read it
@@ -664,7 +693,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                 break;
                             }
                             tc_fence_after();
-                            issue_stage(d_tmem, stage, first);
+                            issue_stage(d_tmem, stage, first, CF::IDESC);
                             if (++stage == S) {
                                 stage = 0;
                                 phase ^= 1;
@@ -698,6 +727,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
                     }
                     uint32_t d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
+                    // a tail half is one MMA of half the width
+                    const uint32_t idesc_item = (CF::HALVES && w.half >= 0) ? CF::IDESC_HALF : CF::IDESC;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!mbar_wait(&full[stage], phase, abort_flag)) {
                             ok = false;
@@ -711,7 +742,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
                             d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                         }
-                        issue_stage(d_tmem, stage, first_in_group);
+                        issue_stage(d_tmem, stage, first_in_group, idesc_item);
                         if (++stage == S) {
                             stage = 0;
                             phase ^= 1;
@@ -806,6 +837,11 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             const int buf = local & 1;
             const int row_base = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM + q * 32;
             const int row = row_base + lane;
+            // A tail half has 128 accumulator columns, 64 per warp.
+            const bool hw = CF::HALVES && w.half >= 0;
+            const int cb = hw ? cbase / 2 : cbase;   // this warp's first accumulator column
+            const int ocol = nb * CF::BN + (hw ? w.half * (CF::BN / 2) : 0) + cb;   // ... and its output column
+            const int nunits = hw ? NUNITS / 2 : NUNITS;
             // The item's scales and bias do not depend on the MMA: fetch them
             // before waiting for the accumulator. Tile modes: lane l takes the
             // warp's columns 4l .. 4l + 3 (0 past N), shared by shuffles later.
@@ -817,8 +853,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // (per-K-group-scale kernels have no column scale here, and fetch
             // their bias after the group loop, whose running sum fills the registers)
             auto load_cols = [&]() {
-                const int cl = nb * CF::BN + cbase + 4 * lane;
-                if (4 * lane < CF::EPI_COLS && cl < p.N) {
+                const int cl = ocol + 4 * lane;
+                if (4 * lane < (hw ? CF::EPI_COLS / 2 : CF::EPI_COLS) && cl < p.N) {
                     if (!CF::GS && p.col_scale) cs_l = ld_bcast4(p.col_scale, cl, p.N);
                     if (p.bias) bias_l = ld_bcast4(p.bias, cl, p.N);
                 }
@@ -939,7 +975,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = j < UNIT ? gsum[u * UNIT + j] : 0.0f;
                 } else {
-                const int tcol = cbase + u * UNIT;
+                const int tcol = cb + u * UNIT;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 // K groups (the small-M form only): GB loads in flight per wait
@@ -985,7 +1021,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // this unit with plain global stores instead of a TMA box (the K
             // segments of a split tile each finish single units).
             auto finish = [&](int u, float (&v)[32], bool direct) {
-                const int col0 = nb * CF::BN + cbase + u * UNIT;
+                const int col0 = ocol + u * UNIT;
                 epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row, cs_l, bias_l,
                                                      u * UNIT / 4);
                 if constexpr (CF::MODE == MODE_ROWQ) {
@@ -1057,7 +1093,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // generic writes to buffers the TMA (async proxy) filled
             if (part && p.cluster_split) fence_proxy_async_smem();
 #pragma unroll U_UNROLL
-            for (int u = 0; u < NUNITS; ++u) {
+            for (int u = 0; u < nunits; ++u) {
                 float v[32];
                 load_acc(u, v);
                 if (part && owner(u) != seg) {
@@ -1080,7 +1116,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                     }
                 }
-                if (!CF::GS && u == NUNITS - 1) {
+                if (!CF::GS && u == nunits - 1) {
                     // Last read of this accumulator: hand it back to the MMA warp.
                     tc_fence_before();
                     __syncwarp();

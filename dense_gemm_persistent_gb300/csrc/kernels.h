@@ -10,12 +10,15 @@
 namespace dg {
 
 struct KernelInfo;
+// bh: B's tensor map for the loads of a tail half (K-major B: 64-row box).
 // cluster: CTAs per cluster for kernels that are not CTA pairs (1 = none).
-using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                                 const Params& p, int grid, cudaStream_t s, bool cooperative, int cluster);
+using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bh,
+                                 const CUtensorMap& d, const Params& p, int grid, cudaStream_t s, bool cooperative,
+                                 int cluster);
 
 struct KernelInfo {
     int bn, fp8, a_mn, b_mn, mode, pair, gs;
+    int halves;        // can run tail tiles as two N halves
     int stages, smem_bytes, tmem_cols, threads, epi_warps;
     int launch_regs;   // register split (setmaxnreg): registers per thread the split assumes at launch; 0 = none
     const void* func;  // host stub of the __global__ function (for attributes)
@@ -23,8 +26,8 @@ struct KernelInfo {
 };
 
 template <class CF>
-cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const Params& p,
-                           int grid, cudaStream_t s, bool cooperative, int cluster) {
+cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bh, const CUtensorMap& d,
+                           const Params& p, int grid, cudaStream_t s, bool cooperative, int cluster) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(CF::NUM_THREADS);
@@ -53,13 +56,13 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
     }
     cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, gemm_persistent<CF>, a, b, d, p);
+    return cudaLaunchKernelEx(&cfg, gemm_persistent<CF>, a, b, bh, d, p);
 }
 
 template <class CF>
 KernelInfo make_info() {
     return KernelInfo{CF::BN,     CF::FP8,    CF::A_MN,       CF::B_MN,      CF::MODE,
-                      CF::PAIR ? 1 : 0, CF::GS ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
+                      CF::PAIR ? 1 : 0, CF::GS ? 1 : 0, CF::HALVES ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
                       CF::EPI_WARPS, CF::REG_SPLIT ? CF::LAUNCH_REGS : 0,
                       reinterpret_cast<const void*>(&gemm_persistent<CF>), &launch_variant<CF>};
 }

@@ -121,11 +121,15 @@ typedef struct {
                               contiguous groups, each accumulated by the tensor
                               core separately and summed in FP32 (1 = off)      */
     int tail_tiles;        /* tiles of the last, partial wave that are split
-                              along K so the wave finishes sooner (0 = none)    */
+                              (along K, or along N with tail_halves) so the
+                              wave finishes sooner (0 = none)                  */
     int tail_split;        /* K segments per tail tile (1 = no splitting)       */
     int cluster_split;     /* 1: the K segments of each split tile run as one
                               thread-block cluster and are summed through
                               distributed shared memory (no workspace needed) */
+    int tail_halves;       /* 1: the tail_tiles run instead as two halves of
+                              tile_n / 2 columns each, every half over the
+                              whole K range (no workspace needed)            */
     size_t smem_bytes;     /* dynamic shared memory per CTA                     */
     size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
 } dgemm_plan_t;

@@ -96,8 +96,12 @@ def test_workspace_sizes(lib, monkeypatch):
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p["tail_tiles"], p["tail_split"]) == (28, 2)
     assert p["workspace_bytes"] == 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
-    # FP8 4096 x 11008 x 4096 has 32 K slices per tile: too short to split
-    assert dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)["tail_split"] == 1
+    # FP8 4096 x 11008 x 4096 has 32 K slices per tile: too short to split along
+    # K; its 4 leftover tiles run as 8 N halves instead, with no workspace
+    p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
+    assert (p["tail_tiles"], p["tail_split"], p["tail_halves"], p["workspace_bytes"]) == (4, 1, 1, 0)
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
+    assert dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)["tail_halves"] == 0
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "0")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)["workspace_bytes"] == 0
     assert dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax") == base
@@ -109,7 +113,7 @@ def test_plans_for_the_five_workloads(lib):
     p2 = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p2["cta_group"], p2["tile_m"], p2["tile_n"]) == (2, 256, 256)
     assert p2["num_tiles"] == 256 and p2["grid"] == 152 and p2["stages"] == 6
-    assert (p2["tail_tiles"], p2["tail_split"]) == (28, 2)      # 3 full waves + 28 tiles in halves
+    assert (p2["tail_tiles"], p2["tail_split"]) == (28, 2)      # 3 full waves + 28 tiles in K halves
     p3 = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
     assert p3["cta_group"] == 2 and p3["num_tiles"] == 16 * 43 and p3["grid"] == 152
     p4 = dg.dgemm_plan(0, 16, 18432, 7168, "nk", "bf16", num_sms=152)

@@ -128,25 +128,32 @@ def test_k_group_promotion_exact(M, kblocks):
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_bf16_wide_tile_single_and_pair_exact(layout, pair, monkeypatch):
+@pytest.mark.parametrize("pair,halves", [("0", "1"), ("1", "0"), ("1", "1")])
+def test_bf16_wide_tile_single_and_pair_exact(layout, pair, halves, monkeypatch):
     """128 x 256 tiles on one CTA and 256 x 256 tiles on a CTA pair (cta_group::2),
-    with M, N and K tails."""
+    with M, N and K tails; the pair's 12 tiles run whole, or (all of them
+    being the last wave's) as 24 halves of 128 columns."""
     monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
     monkeypatch.setenv("DGEMM_TILE_N", "256")
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", halves)
     plan = dg.dgemm_plan(0, 700, 776, 328, layout, "f32")
     assert plan["cta_group"] == (2 if pair == "1" else 1) and plan["tile_n"] == 256
+    assert plan["tail_halves"] == (1 if pair + halves == "11" else 0)
     got, ref = bf16_case(700, 776, 328, layout, seed=400 + int(pair))
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_fp8_wide_tile_single_and_pair_exact(layout, pair, monkeypatch):
+@pytest.mark.parametrize("pair,halves", [("0", "1"), ("1", "0"), ("1", "1")])
+def test_fp8_wide_tile_single_and_pair_exact(layout, pair, halves, monkeypatch):
+    """As above for E4M3; an MN-major E4M3 B (128-column atoms) has no half
+    tiles."""
     monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
     monkeypatch.setenv("DGEMM_TILE_N", "256")
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", halves)
     plan = dg.dgemm_plan(1, 700, 784, 400, layout, "f32")
     assert plan["cta_group"] == (2 if pair == "1" else 1) and plan["tile_n"] == 256
+    assert plan["tail_halves"] == (1 if pair + halves == "11" and layout == "nk" else 0)
     got, ref = fp8_case(700, 784, 400, layout, seed=500 + int(pair))
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
@@ -169,6 +176,7 @@ def test_tail_split_exact(shape, layout, pair, monkeypatch):
     workspace, last-arriving warp sums them): still bit-exact."""
     monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")   # split even these short tiles
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")      # along K, not N
     M, N, K = shape
     plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
     assert plan["tail_split"] >= 2
@@ -179,6 +187,7 @@ def test_tail_split_exact(shape, layout, pair, monkeypatch):
 @pytest.mark.parametrize("layout", ["nk", "kn"])
 def test_tail_split_fp8_exact(layout, monkeypatch):
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
     plan = dg.dgemm_plan(1, 4096, 11008, 2048, layout, "f32")
     assert plan["tail_split"] >= 2
     got, ref = fp8_case(4096, 11008, 2048, layout, seed=800, ws=True)
@@ -189,6 +198,7 @@ def test_tail_split_repeated_calls_reuse_workspace(monkeypatch):
     """Arrival counters are tagged with a per-launch epoch: the same workspace,
     even filled with garbage first, serves consecutive calls."""
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
     M, N, K = 4096, 4096, 1024
     ws = workspace(0, M, N, K, "nk")
     ws.fill_(0xA5)
@@ -202,9 +212,33 @@ def test_tail_split_repeated_calls_reuse_workspace(monkeypatch):
         assert np.array_equal(D.cpu().double().numpy(), ref)
 
 
-def test_tail_split_default_rule_on_long_tiles():
-    """Without forcing, a tail is split only for long tiles: 4096^3 BF16 (64 K
-    slices) splits its 28-tile tail, the same shape at K = 2048 does not."""
+@pytest.mark.parametrize("shape,layout", [((4096, 4096, 1024), "kn"), ((4096, 4096, 1024), "nk"),
+                                          ((4000, 1288, 1024), "kn"), ((2304, 2816, 2000), "nk")])
+def test_tail_halves_exact(shape, layout):
+    """The last partial wave's CTA-pair tiles, too short to split along K, run
+    as two 256 x 128 halves each (N = 128 MMAs over the whole K range, half of
+    B loaded): bit-exact, ragged edges included."""
+    M, N, K = shape
+    plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
+    assert plan["cta_group"] == 2 and plan["tail_halves"] == 1 and plan["tail_tiles"] > 0
+    assert plan["workspace_bytes"] == 0
+    got, ref = bf16_case(M, N, K, layout, seed=1000 + K)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("shape", [(4096, 11008, 1024), (4000, 10900, 640)])
+def test_tail_halves_fp8_exact(shape):
+    M, N, K = shape
+    plan = dg.dgemm_plan(1, M, N, K, "nk", "f32")
+    assert plan["cta_group"] == 2 and plan["tail_halves"] == 1 and plan["tail_tiles"] > 0
+    got, ref = fp8_case(M, N, K, "nk", seed=1100 + K)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+def test_tail_split_default_rule_on_long_tiles(monkeypatch):
+    """Without forcing, a tail is split along K only for long tiles: 4096^3 BF16
+    (64 K slices) splits its 28-tile tail, the same shape at K = 2048 does not."""
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tail_split"] == 2
     assert dg.dgemm_plan(0, 4096, 4096, 2048, "kn", "bf16")["tail_split"] == 1
     got, ref = bf16_case(2304, 2816, 3072, "nk", seed=900, ws=True)

@@ -146,11 +146,26 @@ def test_requant_tail_split(monkeypatch):
     and fold their row maxima in before the grid barrier. 90 tiles of 256 x 256
     on 76 pairs: the last 14 (rows 2048-2559 in the banded raster) are split."""
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
+    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
     w = wl.make(5, M=2560, N=2304, K=2048)
     plan = dg.dgemm_plan(1, w.M, w.N, w.K, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=0)
     if plan["cta_group"] != 2 or plan["grid"] != 152:
         pytest.skip("needs 76 resident CTA pairs")
     assert plan["tail_tiles"] == 14 and plan["tail_split"] == 2
+    q, s = run_workload(w)
+    rows = np.array(sorted(set(range(2048, 2560, 23)) | {0, 1000, 2047, 2559}), dtype=np.int64)
+    ok, msg = requant_ok(q.numpy()[rows], s.numpy()[rows], ref_of(w, rows=rows))
+    assert ok, msg
+
+
+def test_requant_tail_halves():
+    """The same 90 tiles with the last 14 run as 28 halves of 256 x 128: each
+    half stashes its columns and folds its row maxima in before the barrier."""
+    w = wl.make(5, M=2560, N=2304, K=2048)
+    plan = dg.dgemm_plan(1, w.M, w.N, w.K, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=0)
+    if plan["cta_group"] != 2 or plan["grid"] != 152:
+        pytest.skip("needs 76 resident CTA pairs")
+    assert plan["tail_tiles"] == 14 and plan["tail_halves"] == 1 and plan["tail_split"] == 1
     q, s = run_workload(w)
     rows = np.array(sorted(set(range(2048, 2560, 23)) | {0, 1000, 2047, 2559}), dtype=np.int64)
     ok, msg = requant_ok(q.numpy()[rows], s.numpy()[rows], ref_of(w, rows=rows))
