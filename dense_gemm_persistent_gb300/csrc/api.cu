@@ -20,7 +20,8 @@ namespace {
 __device__ unsigned int g_status = 0;  // sticky device-side error bits, one word per device
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kWsHeader = 256;  // grid-barrier counter lives here
+constexpr size_t kWsHeader = 256;  // requantisation: chunk claim counter + row-band counters
+static_assert(8 + 4 * dg::kMaxBands <= kWsHeader, "row-band counters fit the header");
 constexpr int64_t kMinTailSlices = 48;  // shortest tile (K slices) worth splitting
 
 struct DeviceState {
@@ -231,14 +232,19 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.num_tiles = static_cast<int>(tiles_m * tiles_n);
     const int units = pair ? max_pairs : num_sms;
     p.pub.grid = (pair ? 2 : 1) * static_cast<int>(p.pub.num_tiles < units ? p.pub.num_tiles : units);
-    // The requantising kernel's grid barrier needs every CTA resident: it is
-    // launched cooperatively (the grid is sized from the measured occupancy
-    // too). DGEMM_COOPERATIVE=0 drops the attribute, because Nsight Compute
-    // cannot launch cooperative cluster grids; on an otherwise idle GPU the
-    // grid is still co-resident, and the barrier's wait is bounded regardless.
+    // The requantising kernel's last waits (for the row bands other CTAs are
+    // still finishing) need every CTA resident: it is launched cooperatively
+    // (the grid is sized from the measured occupancy too). DGEMM_COOPERATIVE=0
+    // drops the attribute, because Nsight Compute cannot launch cooperative
+    // cluster grids; on an otherwise idle GPU the grid is still co-resident,
+    // and the waits are bounded regardless.
     const char* coop_env = std::getenv("DGEMM_COOPERATIVE");
     p.pub.cooperative = (p.mode == dg::MODE_ROWQ && !(coop_env && coop_env[0] == '0')) ? 1 : 0;
     p.pub.raster_group = static_cast<int>(tiles_m < 8 ? (tiles_m > 0 ? tiles_m : 1) : 8);
+    if (const char* g = std::getenv("DGEMM_RASTER_GROUP")) {   // tuning sweeps: tile rows per band
+        const int v = std::atoi(g);
+        if (v >= 1 && v <= tiles_m) p.pub.raster_group = v;
+    }
     p.pub.smem_bytes = static_cast<size_t>(k->smem_bytes);
 
     // Tail splitting: when the tiles do not fill the last wave, run the full
@@ -585,7 +591,12 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
         p.epoch = next_epoch();
     }
     if (plan.mode == dg::MODE_ROWQ) {
-        p.barrier = reinterpret_cast<unsigned*>(wsb);
+        // header: the chunk claim counter, then one arrival counter per row band
+        // (a band of rq_gpc raster groups, so that at most kMaxBands of them)
+        p.rq_next = reinterpret_cast<unsigned long long*>(wsb);
+        p.band_count = reinterpret_cast<unsigned*>(wsb + 8);
+        const int64_t groups = (p.tiles_m + p.group_m - 1) / p.group_m;
+        p.rq_gpc = static_cast<int>(groups > 0 ? (groups + dg::kMaxBands - 1) / dg::kMaxBands : 1);
         p.amax = reinterpret_cast<unsigned*>(wsb + kWsHeader);
         p.stash = reinterpret_cast<const uint16_t*>(wsb + kWsHeader + amax_bytes);
         p.q_out = static_cast<uint8_t*>(D);

@@ -28,8 +28,9 @@
 // finishes its share of the tile's 32-column units, reading the other
 // segments' partials from the workspace or, when the segments form one
 // cluster, from the peers' shared memory. The requantising form (MODE_ROWQ)
-// ends with a grid barrier and a pass that turns the BF16 stash into E4M3
-// codes with per-row scales.
+// turns the BF16 stash into E4M3 codes with per-row scales band by band: once
+// every work item of a row band has been counted in, epilogue warps convert
+// its rows between their own tiles, and the last band after their last tile.
 //
 // The method is the one the pages describe -- tiles of C per block, K walked in
 // slices through a multi-buffered shared-memory pipeline, FP32 accumulation,
@@ -50,14 +51,14 @@ namespace dg {
 enum Mode : int {
     MODE_TILE = 0,  // D tile stored as is (TMA store)
     MODE_SWAP = 1,  // the MMA computed D^T: store transposed with direct stores
-    MODE_ROWQ = 2,  // stash y, per-row amax, grid barrier, E4M3 requantisation
+    MODE_ROWQ = 2,  // stash y, per-row amax, E4M3 requantisation of finished row bands
 };
 
 enum ErrBits : unsigned {
     ERR_TIMEOUT_PRODUCER = 1u,
     ERR_TIMEOUT_MMA = 2u,
     ERR_TIMEOUT_EPILOGUE = 4u,
-    ERR_TIMEOUT_GRID_BARRIER = 8u,
+    ERR_TIMEOUT_ROW_BAND = 8u,
     ERR_TIMEOUT_DRAIN = 16u,
 };
 
@@ -90,7 +91,9 @@ struct Params {
     int act;                 // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
     // MODE_ROWQ
     unsigned* amax;          // [M] |y| maxima as float bits; zero before launch
-    unsigned* barrier;       // grid barrier counter; zero before launch
+    unsigned long long* rq_next;   // requantisation chunks claimed so far; zero before launch
+    unsigned* band_count;    // [row bands] epilogue-warp arrivals per band; zero before launch
+    int rq_gpc;              // raster groups per row band
     const uint16_t* stash;   // [M,N] BF16 y values (what tmD writes)
     uint8_t* q_out;          // [M,N] E4M3 codes
     float* out_row_scale;    // [M]
@@ -232,10 +235,6 @@ struct Cfg {
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     // split-K through the cluster parks a whole accumulator in the pipeline buffers
     static_assert(EPI_WARPS * BN / (EPI_WARPS / 4) * 32 * 4 <= STAGES * STAGE_BYTES, "parked partials fit");
-    // the requantisation pass double-buffers 8 KB stash chunks per warp in the
-    // pipeline buffers and keeps its barriers in the staging area
-    static_assert(MODE != MODE_ROWQ || 2 * (NUM_THREADS / 32) * 8192 <= STAGES * STAGE_BYTES, "requant slots fit");
-    static_assert(MODE != MODE_ROWQ || 2 * (NUM_THREADS / 32) * 8 <= STAGING_BYTES, "requant barriers fit");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
@@ -249,6 +248,26 @@ __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int
     const int r = t - g * group_tiles;
     mb = first_m + r % rows;
     nb = r / rows;
+}
+
+// Row bands of the requantising form: rq_gpc raster groups (group_m tile rows
+// with all their tile columns, consecutive in the raster) each, so that the
+// band counters fit the workspace header. A band's rows are final once every
+// epilogue warp of every CTA has counted in every work item of its tiles.
+constexpr int kMaxBands = 62;
+constexpr int RQ_CHUNK = 4096;   // values of one row converted per claim (16 x 16 bytes per lane)
+
+__device__ __forceinline__ int band_of_tile(const Params& p, int t) {
+    return t / (p.group_m * p.tiles_n) / p.rq_gpc;
+}
+
+template <class CF>
+__device__ __forceinline__ unsigned band_expected(const Params& p, int b) {
+    const int t0 = b * p.rq_gpc * p.group_m * p.tiles_n;
+    const int t1 = min((b + 1) * p.rq_gpc * p.group_m, p.tiles_m) * p.tiles_n;
+    const int tail = max(0, t1 - max(t0, p.dp_tiles));   // split tiles: several items each
+    const int extra = p.tail_halves ? 1 : p.split - 1;
+    return static_cast<unsigned>(t1 - t0 + tail * extra) * CF::CTAS * CF::EPI_WARPS;
 }
 
 // Activations applied to 32 values at once; the switch is taken once per
@@ -830,6 +849,87 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         int gcount = 0;   // GS: scale groups folded so far (both buffers alternate)
         bool cluster_done = false;   // passed the split-K cluster barrier
         bool ok = true;
+
+        // Requantisation (MODE_ROWQ): s[m] = amax[m] / 448; q = RN_E4M3(y * (1 / s[m])),
+        // saturating. The stash is cut into chunks of RQ_CHUNK values of one row,
+        // in row order (so in band order), claimed one at a time by epilogue
+        // warps through a global counter; the warp converting a row's first
+        // chunk writes the row scale. Lane l reads 8 x 16 bytes at once.
+        const int64_t rq_cpr = (p.N + RQ_CHUNK - 1) / RQ_CHUNK;   // chunks per row
+        const int64_t rq_chunks = static_cast<int64_t>(p.M) * rq_cpr;
+        auto band_of_chunk = [&](int64_t j) {
+            return static_cast<int>(j / rq_cpr) / CF::TILE_M / p.group_m / p.rq_gpc;
+        };
+        auto rq_convert = [&](int64_t j) {
+            const int64_t m = j / rq_cpr;
+            const int c0 = static_cast<int>(j % rq_cpr) * RQ_CHUNK;
+            const int len8 = min(RQ_CHUNK, p.N - c0) / 8;   // N is a multiple of 16
+            const float amax = __uint_as_float(__ldcg(p.amax + m));
+            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
+            if (lane == 0 && c0 == 0) p.out_row_scale[m] = s;
+            const uint4* src = reinterpret_cast<const uint4*>(p.stash + m * p.N + c0);
+            uint2* dst = reinterpret_cast<uint2*>(p.q_out + m * p.N + c0);
+            uint4 y[RQ_CHUNK / 256];
+#pragma unroll
+            for (int i = 0; i < RQ_CHUNK / 256; ++i) {
+                const int g = lane + 32 * i;
+                y[i] = g < len8 ? __ldcg(src + g) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < RQ_CHUNK / 256; ++i) {
+                const int g = lane + 32 * i;
+                if (g < len8) {
+                    const uint32_t w0 = pack_e4m3x2(bf16_lo(y[i].x) * inv, bf16_hi(y[i].x) * inv);
+                    const uint32_t w1 = pack_e4m3x2(bf16_lo(y[i].y) * inv, bf16_hi(y[i].y) * inv);
+                    const uint32_t w2 = pack_e4m3x2(bf16_lo(y[i].z) * inv, bf16_hi(y[i].z) * inv);
+                    const uint32_t w3 = pack_e4m3x2(bf16_lo(y[i].w) * inv, bf16_hi(y[i].w) * inv);
+                    dst[g] = make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));
+                }
+            }
+        };
+        // Chunks are claimed in order with one atomic add each (a compare-and-
+        // swap that claimed only ready chunks failed under the contention of a
+        // thousand warps). A claimed chunk whose band is not complete yet stays
+        // this warp's pending chunk until it is. rq_work converts chunks while
+        // their bands are complete and stop() is false; it returns with
+        // rq_pending >= 0 if it stopped at an incomplete band.
+        long long rq_pending = -1;
+        bool rq_done = false;   // every chunk has been claimed
+        int rq_ready_band = -1;   // a band this warp has seen complete (acquired)
+        auto rq_band_ready = [&](long long j) {
+            const int b = band_of_chunk(j);
+            if (b == rq_ready_band) return true;
+            unsigned ready = 0;
+            if (lane == 0) ready = ld_acquire_u32(p.band_count + b) >= band_expected<CF>(p, b) ? 1u : 0u;
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            __syncwarp();
+            if (ready) {
+                __threadfence();   // the band's stash and maxima after its count
+                rq_ready_band = b;
+            }
+            return ready != 0;
+        };
+        // lane 0: the next ticket, requested while the current chunk converts
+        auto rq_claim = [&]() -> long long {
+            long long j = 0;
+            if (lane == 0) j = static_cast<long long>(atomicAdd(p.rq_next, 1ull));
+            return j;
+        };
+        auto rq_work = [&](auto stop, int max_chunks) {
+            for (int c = 0; c < max_chunks && !rq_done && !stop(); ++c) {
+                if (rq_pending < 0) rq_pending = __shfl_sync(0xffffffffu, rq_claim(), 0);
+                if (rq_pending >= rq_chunks) {
+                    rq_done = true;
+                    break;
+                }
+                if (!rq_band_ready(rq_pending)) break;
+                const long long next = rq_claim();
+                rq_convert(rq_pending);
+                rq_pending = __shfl_sync(0xffffffffu, next, 0);
+            }
+        };
+
         Work w;
         for (int it = 0; next_work(p, unit0, units, it, w); ++it, ++local) {
             int mb, nb;
@@ -1255,25 +1355,59 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
+            if constexpr (CF::MODE == MODE_ROWQ) {
+                // This warp's share of the item is done: once its TMA stores have
+                // completed (and, like its plain stores and row maxima, are
+                // visible), count it into the item's row band.
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    bulk_wait_all();
+                    fence_proxy_async_global();
+                    __threadfence();
+                    red_release_add_u32(p.band_count + band_of_tile(p, w.tile), 1u);
+                }
+                __syncwarp();
+                // Until the next accumulator is ready, convert chunks of complete
+                // bands (never waiting for one: the MMA may need this warp soon).
+                Work wn;
+                if (next_work(p, unit0, units, it + 1, wn)) {
+                    const int nl = local + 1;
+                    rq_work([&]() { return mbar_test(&acc_full[nl & 1], static_cast<uint32_t>(nl >> 1) & 1u); }, 16);
+                }
+            }
         }
         if (!ok) raise_error(p, ERR_TIMEOUT_EPILOGUE, abort_flag);
         if constexpr (CF::MODE == MODE_ROWQ) {
-            // stash rows written with plain stores (split tiles) are read by the
-            // requantisation pass's bulk copies (async proxy)
-            fence_proxy_async_global();
-            __threadfence();
+            // The rest of the chunks, waiting (bounded) for their bands.
+            while (ok && !*abort_flag) {
+                rq_work([]() { return false; }, 1 << 30);
+                if (rq_done) break;
+                unsigned ready = 1;   // the pending chunk's band is not complete yet
+                if (lane == 0) {
+                    const int b = band_of_chunk(rq_pending);
+                    const unsigned want = band_expected<CF>(p, b);
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire_u32(p.band_count + b) < want) {
+                        if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
+                            ready = 0;
+                            break;
+                        }
+                        __nanosleep(500);
+                    }
+                }
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (!ready) {
+                    if (lane == 0) raise_error(p, ERR_TIMEOUT_ROW_BAND, abort_flag);
+                    break;
+                }
+            }
         }
         if (!CF::PAIR && p.cluster_split && !cluster_done) {   // the split-K barrier, once per thread
             __syncwarp();
             cluster_sync();
         }
-        if (lane == 0) {
-            bulk_wait_all();
-            if constexpr (CF::MODE == MODE_ROWQ) {
-                fence_proxy_async_global();
-                __threadfence();
-            }
-        }
+        if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
 
@@ -1294,109 +1428,6 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             tc_fence_after();
             tmem_dealloc(tmem_base, CF::TMEM_COLS);
         }
-    }
-
-    if constexpr (CF::MODE == MODE_ROWQ) {
-        // ---------------------------------------------------------- grid barrier
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(p.barrier, 1u);
-            const uint64_t t0 = globaltimer();
-            while (true) {
-                unsigned seen;
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(p.barrier) : "memory");
-                if (seen >= gridDim.x) break;
-                if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
-                    raise_error(p, ERR_TIMEOUT_GRID_BARRIER, abort_flag);
-                    break;
-                }
-                __nanosleep(256);
-            }
-            __threadfence();
-        }
-        __syncthreads();
-        if (*abort_flag) return;
-        // ---------------------------------------------------------- requantise
-        // s[m] = amax[m] / 448; q = RN_E4M3(y * (1 / s[m])), saturating.
-        // The stash is streamed through the idle pipeline buffers by bulk
-        // asynchronous copies: it is cut into chunks of up to RQ_CHUNK values of
-        // one row, dealt round-robin to the CTAs and then to their warps; each
-        // warp double-buffers its chunks (two 8 KB slots, one mbarrier each), so
-        // an SM keeps up to 2 x warps x 8 KB of the stash in flight. Lane l
-        // converts 16 values at a time and writes their 16 codes; the row scale
-        // is written by the warp that converts the row's first chunk.
-        constexpr int RQ_CHUNK = 4096;
-        const int nwarps = static_cast<int>(blockDim.x) >> 5;
-        const int64_t cpr = (p.N + RQ_CHUNK - 1) / RQ_CHUNK;   // chunks per row
-        const int64_t nchunks = static_cast<int64_t>(p.M) * cpr;
-        uint8_t* slot0 = stages + static_cast<size_t>(2 * warp) * RQ_CHUNK * 2;
-        uint64_t* rq_bar = reinterpret_cast<uint64_t*>(staging) + 2 * warp;   // epilogue staging is idle too
-        if (lane == 0) {
-            mbar_init(&rq_bar[0], 1);
-            mbar_init(&rq_bar[1], 1);
-            fence_mbarrier_init();
-        }
-        __syncwarp();
-        auto chunk_of = [&](int64_t t) {
-            return static_cast<int64_t>(blockIdx.x) +
-                   static_cast<int64_t>(gridDim.x) * (static_cast<int64_t>(warp) + static_cast<int64_t>(nwarps) * t);
-        };
-        int64_t issued = 0;   // (lane 0) chunks whose copy has been started
-        auto issue = [&](int64_t t) {
-            const int64_t j = chunk_of(t);
-            if (j >= nchunks) return;
-            const int64_t m = j / cpr;
-            const int c0 = static_cast<int>(j % cpr) * RQ_CHUNK;
-            const uint32_t bytes = static_cast<uint32_t>(min(RQ_CHUNK, p.N - c0)) * 2u;
-            fence_proxy_async_smem();   // the slot's earlier reads before the copy rewrites it
-            mbar_arrive_expect_tx(&rq_bar[t & 1], bytes);
-            bulk_load_1d(slot0 + (t & 1) * RQ_CHUNK * 2, p.stash + m * p.N + c0, bytes, &rq_bar[t & 1]);
-            issued = t + 1;
-        };
-        if (lane == 0) {
-            issue(0);
-            issue(1);
-        }
-        bool rq_ok = true;
-        int64_t t = 0;
-        for (; chunk_of(t) < nchunks; ++t) {
-            const int64_t j = chunk_of(t);
-            const int64_t m = j / cpr;
-            const int c0 = static_cast<int>(j % cpr) * RQ_CHUNK;
-            const int len = min(RQ_CHUNK, p.N - c0);   // a multiple of 16 (N is)
-            const float amax = __uint_as_float(__ldcg(p.amax + m));
-            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
-            const float inv = amax > 0.0f ? 1.0f / s : 0.0f;
-            if (lane == 0 && c0 == 0) p.out_row_scale[m] = s;
-            if (!mbar_wait(&rq_bar[t & 1], static_cast<uint32_t>(t >> 1) & 1u, abort_flag)) {
-                rq_ok = false;
-                break;
-            }
-            const uint4* src = reinterpret_cast<const uint4*>(slot0 + (t & 1) * RQ_CHUNK * 2);
-            uint4* dst = reinterpret_cast<uint4*>(p.q_out + m * p.N + c0);
-            for (int g = lane; g < len / 16; g += 32) {
-                const uint4 y0 = src[2 * g], y1 = src[2 * g + 1];
-                const uint32_t w[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint32_t lo = pack_e4m3x2(bf16_lo(w[2 * h]) * inv, bf16_hi(w[2 * h]) * inv);
-                    const uint32_t hi = pack_e4m3x2(bf16_lo(w[2 * h + 1]) * inv, bf16_hi(w[2 * h + 1]) * inv);
-                    o[h] = lo | (hi << 16);
-                }
-                dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            __syncwarp();   // every lane is done with this slot
-            if (lane == 0) issue(t + 2);
-        }
-        if (lane == 0) {
-            if (!rq_ok) raise_error(p, ERR_TIMEOUT_EPILOGUE, abort_flag);
-            // no copy into this CTA's shared memory may outlive it
-            for (int64_t u = t + (rq_ok ? 0 : 1); u < issued; ++u)
-                if (!mbar_wait(&rq_bar[u & 1], static_cast<uint32_t>(u >> 1) & 1u, nullptr))
-                    raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
-        }
-        __syncwarp();
     }
 }
 

@@ -115,7 +115,8 @@ typedef struct {
     int stages;            /* shared-memory pipeline depth                      */
     int num_tiles;         /* output tiles                                      */
     int grid;              /* CTAs launched (persistent: <= SM count)           */
-    int cooperative;       /* 1: launched cooperatively (grid-wide barrier)     */
+    int cooperative;       /* 1: launched cooperatively (CTAs wait on row bands
+                              other CTAs finish: all must be resident)        */
     int raster_group;      /* tile rows per band of the swizzled raster         */
     int k_groups;          /* K-group promotion: K is split into this many
                               contiguous groups, each accumulated by the tensor
@@ -141,8 +142,8 @@ typedef struct {
  *            epi->out_quant == DGEMM_QUANT_E4M3_ROW_AMAX.
  *   ws       device workspace of ws_bytes bytes, its contents arbitrary on
  *            entry. With the requantising epilogue it is required: at least
- *            256 + 4 * ceil(M / 64) * 64 + 2 * M * N bytes (barrier header, row
- *            maxima, BF16 stash); dgemm_workspace_size(...) also counts room
+ *            256 + 4 * ceil(M / 64) * 64 + 2 * M * N bytes (a header of
+ *            progress counters, row maxima, BF16 stash); dgemm_workspace_size(...) also counts room
  *            for splitting the last partial wave of tiles along K. Otherwise
  *            optional: with at least dgemm_workspace_size(...) bytes, tiles may
  *            be split along K (the last partial wave, or every tile when the
@@ -217,7 +218,7 @@ dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream);
  * GEMM: code inside a custom memory pool or allocator callback, a real-time
  * path that must not block on cudaMalloc's device-wide synchronisation, or an
  * embedded runtime whose memory is carved out once at start-up. The per-row
- * E4M3 requantisation epilogue needs scratch memory (a barrier counter, the
+ * E4M3 requantisation epilogue needs scratch memory (progress counters, the
  * row maxima and a BF16 copy of the pre-quantisation tile values), which
  * dgemm_fp8_scaled takes from a caller-provided workspace. This entry point
  * takes it instead from one statically sized device array inside the library,

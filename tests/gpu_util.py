@@ -22,7 +22,7 @@ def run_workload(w: wl.Workload, d_dtype: str | None = None):
     D = torch.empty(w.M, w.N, dtype=tdt, device=dev())
     s = None
     if w.out_quant != "none":
-        s = torch.empty(w.M, dtype=torch.float32, device=dev())
+        s = torch.full((w.M,), -1.0, dtype=torch.float32, device=dev())   # (every row must be written)
     # the workspace the library can use (tail splitting, requantisation)
     nbytes = dg.dgemm_workspace_size(w.form == "fp8", w.M, w.N, w.K, w.b_layout, out_quant=w.out_quant)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev()) if nbytes else None

@@ -143,7 +143,7 @@ def test_fp8_with_c_bias_and_f32_output(M):
 def test_requant_tail_split(monkeypatch):
     """The requantising epilogue with the last partial wave split along K: the
     split tiles' segments finish their units with plain stores into the stash
-    and fold their row maxima in before the grid barrier. 90 tiles of 256 x 256
+    and fold their row maxima in before counting their row band. 90 tiles of 256 x 256
     on 76 pairs: the last 14 (rows 2048-2559 in the banded raster) are split."""
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
     monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
@@ -160,7 +160,7 @@ def test_requant_tail_split(monkeypatch):
 
 def test_requant_tail_halves():
     """The same 90 tiles with the last 14 run as 28 halves of 256 x 128: each
-    half stashes its columns and folds its row maxima in before the barrier."""
+    half stashes its columns and folds its row maxima in before counting its band."""
     w = wl.make(5, M=2560, N=2304, K=2048)
     plan = dg.dgemm_plan(1, w.M, w.N, w.K, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=0)
     if plan["cta_group"] != 2 or plan["grid"] != 152:
@@ -170,6 +170,24 @@ def test_requant_tail_halves():
     rows = np.array(sorted(set(range(2048, 2560, 23)) | {0, 1000, 2047, 2559}), dtype=np.int64)
     ok, msg = requant_ok(q.numpy()[rows], s.numpy()[rows], ref_of(w, rows=rows))
     assert ok, msg
+
+
+@pytest.mark.parametrize("M,N,K", [(8192, 512, 256), (130000, 64, 128)])
+def test_requant_row_bands(M, N, K):
+    """Row bands converted while later bands are still being multiplied: short
+    K makes each tile quick, so bands finish throughout the call (32 raster
+    groups of 2048 rows); 130000 rows make 64 raster groups, more than the
+    header's band counters, so each band spans two groups (and N = 64 is one
+    ragged quarter of a tile)."""
+    w = wl.make(5, M=M, N=N, K=K)
+    plan = dg.dgemm_plan(1, M, N, K, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=0)
+    assert plan["cooperative"] == 1
+    q, s = run_workload(w)
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([rng.integers(0, M, 200), [0, 2047, 2048, M - 1]])).astype(np.int64)
+    ok, msg = requant_ok(q.numpy()[rows], s.numpy()[rows], ref_of(w, rows=rows))
+    assert ok, msg
+    assert np.all(s.numpy() > 0)   # every row's scale was written
 
 
 def test_requant_from_bf16_form():
