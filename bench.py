@@ -195,14 +195,19 @@ def make_workload(args):
     if getattr(args, "k_group", 0):
         if args.config != 3:
             raise SystemExit("--k-group applies to workload 3 (FP8 E4M3 4096 x 11008 x 4096)")
-        return wl.fp8_grouped(k_group=args.k_group)
+        return wl.fp8_grouped(k_group=args.k_group, b_block=getattr(args, "b_block", 1))
+    if getattr(args, "b_block", 1) != 1:
+        raise SystemExit("--b-block applies with --k-group")
     return wl.make(args.config)
 
 
 def workload_key(args) -> str:
     if getattr(args, "shape", None):
         return "2s" + "x".join(str(v) for v in parse_shape(args.shape))
-    return f"{args.config}g{args.k_group}" if getattr(args, "k_group", 0) else str(args.config)
+    if getattr(args, "k_group", 0):
+        blk = getattr(args, "b_block", 1)
+        return f"{args.config}g{args.k_group}" + (f"b{blk}" if blk != 1 else "")
+    return str(args.config)
 
 
 def describe(args) -> str:
@@ -211,8 +216,10 @@ def describe(args) -> str:
         M, N, K = parse_shape(args.shape)
         return f"BF16 GEMM M={M} N={N} K={K}, entries N(0,1)/sqrt(K), B stored N x K -> BF16 D"
     if getattr(args, "k_group", 0):
+        blk = getattr(args, "b_block", 1)
+        wgt = f"per-({blk}-channel block, K group)" if blk != 1 else "per-(channel, K group)"
         d = d.replace("per-token x per-channel scales",
-                      f"per-(token, {args.k_group}-element K group) x per-(channel, K group) scales")
+                      f"per-(token, {args.k_group}-element K group) x {wgt} scales")
     return d
 
 
@@ -235,7 +242,7 @@ def oracle_sample(w, seconds: float):
         else:
             y = oracle.fp8_gemm_ref(A, B, w.b_layout, w.a_scale.numpy(), w.b_scale.numpy(), C, w.alpha, w.beta,
                                     None if w.bias is None else w.bias.numpy(), w.act, rows=rows,
-                                    nthreads=threads, k_group=w.k_group)
+                                    nthreads=threads, k_group=w.k_group, b_block=w.b_block)
             if w.out_quant != "none":
                 oracle.requant_rows(y)
         done = rows[1]
@@ -285,7 +292,7 @@ def run_ours(args, rank, world, local):
         if w.form == "bf16":
             dg.dgemm_bf16(g.A, g.B, D, **kw)
         else:
-            dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, **kw)
+            dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, b_block=w.b_block, **kw)
 
     dist = world > 1
     if dist:
@@ -420,7 +427,8 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.form == "bf16" else "e4m3", "data": "synthetic",
         "config": {"workload": describe(args), "number": args.config, "M": w.M, "N": w.N, "K": w.K,
-                   "b_layout": w.b_layout, "k_group": w.k_group, "parallelism": f"replicas x{world}",
+                   "b_layout": w.b_layout, "k_group": w.k_group, "b_block": w.b_block,
+                   "parallelism": f"replicas x{world}",
                    "l2": f"rotating {nsets} input sets of {set_bytes / 2**20:.0f} MiB (> L2 129 MiB)",
                    "plan": {k: plan[k] for k in ("swap_ab", "tile_m", "tile_n", "stages", "num_tiles", "grid",
                                                  "cooperative")}},
@@ -450,6 +458,8 @@ def main():
                     help="M,N,K: workload 2's BF16 recipe at this size, B stored N x K (e.g. 1024,1024,4096)")
     ap.add_argument("--k-group", type=int, default=0,
                     help="workload 3 with per-K-group FP8 scales of this group size (multiple of 128)")
+    ap.add_argument("--b-block", type=int, default=1, choices=[1, 128],
+                    help="with --k-group: output channels per weight scale (128: block-scaled weights)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="wall time the reference arm spends on warm-up + steps")
     args = ap.parse_args()
@@ -508,7 +518,7 @@ def run_reference(args, world):
         else:
             y = oracle.fp8_gemm_ref(A, B, w.b_layout, w.a_scale.numpy(), w.b_scale.numpy(), C, w.alpha, w.beta,
                                     None if w.bias is None else w.bias.numpy(), w.act, rows=rows,
-                                    nthreads=threads, k_group=w.k_group)
+                                    nthreads=threads, k_group=w.k_group, b_block=w.b_block)
             if w.out_quant != "none":
                 oracle.requant_rows(y)
         return rows[1] - rows[0]
@@ -527,7 +537,7 @@ def run_reference(args, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": describe(args), "number": args.config, "M": w.M, "N": w.N, "K": w.K,
-                   "b_layout": w.b_layout, "k_group": w.k_group},
+                   "b_layout": w.b_layout, "k_group": w.k_group, "b_block": w.b_block},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} rows of {w.M} per step of the same workload, float64 "
                                    f"oracle, OpenMP"},

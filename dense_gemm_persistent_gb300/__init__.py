@@ -93,24 +93,33 @@ def dgemm_bf16(A, B, D, *, b_layout="kn", C=None, alpha=1.0, beta=0.0, bias=None
     return D
 
 
-def dgemm_fp8_scaled(Aq, Bq, a_scale, b_scale, D, *, b_layout="nk", k_group=0, C=None, alpha=1.0,
+def dgemm_fp8_scaled(Aq, Bq, a_scale, b_scale, D, *, b_layout="nk", k_group=0, b_block=1, C=None, alpha=1.0,
                      beta=0.0, bias=None, act="none", out_quant="none", out_row_scale=None, ws=None,
                      stream=None):
     """D = epilogue(alpha * diag(a_scale) (Aq . op(Bq)) diag(b_scale) + beta * C), E4M3 inputs.
 
     Aq [M,K] and Bq [N,K] ("nk") or [K,N] ("kn") are float8_e4m3fn (or uint8 codes);
-    a_scale [M] and b_scale [N] fp32. Other arguments as for dgemm_bf16. Returns D.
+    a_scale [M] and b_scale [N] fp32. k_group = g > 0: per-K-group scales,
+    a_scale [G,M] and b_scale [G,N]; with b_block=128 as well, one weight scale
+    per 128 output channels, b_scale [G, ceil(N/128)] (dgemm_fp8_blockscaled).
+    Other arguments as for dgemm_bf16. Returns D.
     """
     M, N, K = _dims(Aq, Bq, b_layout)
     epi = _epilogue(bias, act, out_quant, out_row_scale)
-    code = load().dgemm_fp8_scaled(_ptr(Aq), _ptr(Bq), B_KN if b_layout == "kn" else B_NK, _ptr(a_scale),
+    if b_block != 1:
+        if b_block != 128:
+            raise ValueError("b_block must be 1 or 128")
+        entry, name = load().dgemm_fp8_blockscaled, "dgemm_fp8_blockscaled"
+    else:
+        entry, name = load().dgemm_fp8_scaled, "dgemm_fp8_scaled"
+    code = entry(_ptr(Aq), _ptr(Bq), B_KN if b_layout == "kn" else B_NK, _ptr(a_scale),
                                    _ptr(b_scale), int(k_group), _ptr(C),
                                    _dtype_code(C) if C is not None else F32, _ptr(D), _dtype_code(D),
                                    M, N, K, float(alpha), float(beta),
                                    ctypes.byref(epi) if epi is not None else None,
                                    _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                    _stream(stream))
-    _check(code, "dgemm_fp8_scaled")
+    _check(code, name)
     return D
 
 

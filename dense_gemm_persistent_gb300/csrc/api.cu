@@ -20,6 +20,8 @@ namespace {
 __device__ unsigned int g_status = 0;  // sticky device-side error bits, one word per device
 
 constexpr int kMaxDevices = 64;
+constexpr int kWeightBlock = 128;       // output channels per weight scale (block-scaled entry)
+constexpr int kWeightBlockShift = 7;
 constexpr size_t kWsHeader = 256;  // requantisation: chunk claim counter + row-band counters
 static_assert(8 + 4 * dg::kMaxBands <= kWsHeader, "row-band counters fit the header");
 constexpr int64_t kMinTailSlices = 48;  // shortest tile (K slices) worth splitting
@@ -464,8 +466,9 @@ CUtensorMapDataType tm_type(dgemm_dtype_t t) {
 dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, const float* a_scale,
                    const float* b_scale, const void* C, dgemm_dtype_t c_dtype, void* D, dgemm_dtype_t d_dtype,
                    int64_t M, int64_t N, int64_t K, float alpha, float beta, const dgemm_epilogue_t* epi, void* ws,
-                   size_t ws_bytes, cudaStream_t stream, int k_group = 0) {
+                   size_t ws_bytes, cudaStream_t stream, int k_group = 0, int b_block = 1) {
     // ---- arguments that need no device
+    if (b_block != 1 && (b_block != kWeightBlock || k_group <= 0)) return DGEMM_ERR_INVALID_VALUE;
     Plan plan;
     dgemm_status_t st = make_plan(fp8, M, N, K, bl, d_dtype, epi, 2, 1, 0, false, &plan, k_group);
     if (st != DGEMM_OK) return st;
@@ -569,11 +572,16 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.ldd = N;
     p.d_f32 = d_dtype == DGEMM_F32;
     if (plan.gs) {
-        // group-major tables: a_scale [G][M], b_scale [G][N]
+        // group-major tables: a_scale [G][M], b_scale [G][N] (block-scaled
+        // weights: [G][ceil(N / 128)])
+        const int64_t nb_cols = b_block > 1 ? (N + b_block - 1) / b_block : N;
+        const int shift = b_block > 1 ? kWeightBlockShift : 0;
         p.row_gscale = plan.pub.swap_ab ? b_scale : a_scale;
         p.col_gscale = plan.pub.swap_ab ? a_scale : b_scale;
-        p.gs_ld_row = plan.Mm;
-        p.gs_ld_col = plan.Nm;
+        p.gs_ld_row = plan.pub.swap_ab ? nb_cols : M;
+        p.gs_ld_col = plan.pub.swap_ab ? M : nb_cols;
+        p.gs_row_shift = plan.pub.swap_ab ? shift : 0;
+        p.gs_col_shift = plan.pub.swap_ab ? 0 : shift;
         p.group_kb = plan.group_kb;
     } else {
         p.row_scale = plan.pub.swap_ab ? b_scale : a_scale;
@@ -630,6 +638,16 @@ dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t
                                 const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes, dgemm_stream_t stream) {
     return run(1, Aq, Bq, b_layout, a_scale, b_scale, C, c_dtype, D, d_dtype, M, N, K, alpha, beta, epi, ws,
                ws_bytes, reinterpret_cast<cudaStream_t>(stream), k_group);
+}
+
+dgemm_status_t dgemm_fp8_blockscaled(const void* Aq, const void* Bq, dgemm_b_layout_t b_layout,
+                                     const float* a_scale, const float* b_scale, int k_group, const void* C,
+                                     dgemm_dtype_t c_dtype, void* D, dgemm_dtype_t d_dtype, int64_t M, int64_t N,
+                                     int64_t K, float alpha, float beta, const dgemm_epilogue_t* epi, void* ws,
+                                     size_t ws_bytes, dgemm_stream_t stream) {
+    if (k_group <= 0) return DGEMM_ERR_INVALID_VALUE;
+    return run(1, Aq, Bq, b_layout, a_scale, b_scale, C, c_dtype, D, d_dtype, M, N, K, alpha, beta, epi, ws,
+               ws_bytes, reinterpret_cast<cudaStream_t>(stream), k_group, kWeightBlock);
 }
 
 size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,

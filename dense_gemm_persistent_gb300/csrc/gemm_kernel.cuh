@@ -86,6 +86,10 @@ struct Params {
     const float* row_gscale;
     const float* col_gscale;
     int64_t gs_ld_row, gs_ld_col;
+    // Block-scaled weights: one scale per (K group, block of 2^shift MMA rows /
+    // columns) instead of one per row / column (0 = per row / column). Entry
+    // of row m in group j: row_gscale[j * gs_ld_row + (m >> gs_row_shift)].
+    int gs_row_shift, gs_col_shift;
     int group_kb;
     const float* bias;       // per output channel, or null
     int act;                 // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
@@ -231,6 +235,8 @@ struct Cfg {
     static_assert(MODE == MODE_SWAP || EPI_COLS % 64 == 0, "tile epilogue works in 64-column boxes");
     static_assert(STAGES >= 2, "pipeline depth");
     static_assert(!GS || (FP8 && MODE != MODE_ROWQ), "per-K-group scales: FP8, tile or small-M form");
+    // block-scaled weights: a warp's columns lie inside one 128-column block
+    static_assert(!GS_SMEM || 128 % EPI_COLS == 0, "warp columns within a weight block");
     static_assert(BN < 32 || BN % 32 == 0, "epilogue reads 32-column units");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     // split-K through the cluster parks a whole accumulator in the pipeline buffers
@@ -325,6 +331,14 @@ template <int UNIT>
 __device__ __forceinline__ void gs_fold_smem(float* sum, const uint32_t (&r)[UNIT], float rs, const float* cs) {
 #pragma unroll
     for (int c = 0; c < UNIT; c += 4) gs_fold4(sum + c, r + c, rs, *reinterpret_cast<const float4*>(cs + c));
+}
+
+// One scale for all of this warp's columns (block-scaled weights: the warp's
+// columns lie in one block), so one fused multiply-add per output per group.
+template <int UNIT>
+__device__ __forceinline__ void gs_fold_uniform(float* sum, const uint32_t (&r)[UNIT], float s) {
+#pragma unroll
+    for (int c = 0; c < UNIT; c += 2) ffma2(sum[c], sum[c + 1], __uint_as_float(r[c]), __uint_as_float(r[c + 1]), s, s);
 }
 
 // Column scales read from global memory one by one (the small-M form, whose
@@ -810,10 +824,18 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     float* dst = gs_area + slot * CF::SLOT_FLOATS;
                     const float* cs = p.col_gscale + j * p.gs_ld_col;
                     const float* rs = p.row_gscale + j * p.gs_ld_row;
+                    if (p.gs_col_shift == 0) {
 #pragma unroll
-                    for (int c = lane * 4; c < CF::BN; c += 128) {
-                        const int n = col0 + c;
-                        cp_async_16(dst + c, cs + (n < p.N ? n : 0), n < p.N ? 16u : 0u);
+                        for (int c = lane * 4; c < CF::BN; c += 128) {
+                            const int n = col0 + c;
+                            cp_async_16(dst + c, cs + (n < p.N ? n : 0), n < p.N ? 16u : 0u);
+                        }
+                    } else {   // each column gets its block's scale
+#pragma unroll
+                        for (int c = lane; c < CF::BN; c += 32) {
+                            const int n = col0 + c;
+                            cp_async_4(dst + c, cs + ((n < p.N ? n : 0) >> p.gs_col_shift), n < p.N ? 4u : 0u);
+                        }
                     }
 #pragma unroll
                     for (int r = lane; r < CF::BM; r += 32) {
@@ -989,12 +1011,14 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     const int j0 = w.kb0 / p.group_kb, j1 = (w.kb1 - 1) / p.group_kb + 1;
                     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(cbase);
                     const int colw = nb * CF::BN + cbase;   // this warp's first MMA column
+                    const bool blk_cols = p.gs_col_shift != 0;
                     // Tile modes: scales from the scale producer's slot gcount % SC_SLOTS.
                     // Small-M form: row scale one per lane into a register, fetched
                     // two groups ahead (after the hand-back arrive, which is relaxed
                     // so it does not wait for them); column scales read directly.
                     auto load_rs = [&](int j) {
-                        return (j < j1 && row < p.M) ? __ldg(p.row_gscale + j * p.gs_ld_row + row) : 0.0f;
+                        return (j < j1 && row < p.M) ? __ldg(p.row_gscale + j * p.gs_ld_row + (row >> p.gs_row_shift))
+                                                     : 0.0f;
                     };
                     float rs_cur = 0.0f, rs_nxt = 0.0f;
                     if constexpr (!CF::GS_SMEM) {
@@ -1040,9 +1064,12 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             tmem_ld_wait();
 #pragma unroll
                             for (int h = 0; h < PAIRED; ++h) {
-                                if constexpr (CF::GS_SMEM)
-                                    gs_fold_smem<UNIT>(gsum + (u + h) * UNIT, r[h], rsj, csj + (u + h) * UNIT);
-                                else
+                                if constexpr (CF::GS_SMEM) {
+                                    if (blk_cols)
+                                        gs_fold_uniform<UNIT>(gsum + (u + h) * UNIT, r[h], rsj * csj[0]);
+                                    else
+                                        gs_fold_smem<UNIT>(gsum + (u + h) * UNIT, r[h], rsj, csj + (u + h) * UNIT);
+                                } else
                                     gs_fold<UNIT>(gsum + (u + h) * UNIT, r[h], rsj, csj, colw + (u + h) * UNIT, p.N);
                             }
                         }

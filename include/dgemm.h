@@ -186,6 +186,24 @@ dgemm_status_t dgemm_fp8_scaled(const void* Aq, const void* Bq, dgemm_b_layout_t
                                 const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes,
                                 dgemm_stream_t stream);
 
+/* FP8 E4M3 GEMM with block-scaled weights: dgemm_fp8_scaled with k_group = g
+ * > 0, except that one weight scale covers a block of 128 output channels
+ * by g K elements (the last block of each group may be narrower in N):
+ *   a_scale  [G][M] FP32, one per (row of A, K group), as for dgemm_fp8_scaled;
+ *   b_scale  [G][ceil(N / 128)] FP32: b_scale[j * ceil(N / 128) + n / 128]
+ *            scales code Bq[k][n] (or Bq[n][k]) of group j = k / g.
+ * Every 128 columns of a tile then share one scale per group, so the epilogue
+ * folds each group with one fused multiply-add per output instead of two.
+ * Errors: k_group <= 0 gives DGEMM_ERR_INVALID_VALUE; otherwise as for
+ * dgemm_fp8_scaled. [W3] §3.2 (per-group scale granularity). */
+dgemm_status_t dgemm_fp8_blockscaled(const void* Aq, const void* Bq, dgemm_b_layout_t b_layout,
+                                     const float* a_scale, const float* b_scale, int k_group,
+                                     const void* C, dgemm_dtype_t c_dtype,
+                                     void* D, dgemm_dtype_t d_dtype,
+                                     int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                     const dgemm_epilogue_t* epi, void* ws, size_t ws_bytes,
+                                     dgemm_stream_t stream);
+
 /* Workspace bytes a call with these arguments can use (0 when none). Query it
  * once and pass a buffer at least this large ([W3] §5.1). Uses the current
  * device's SM count when a device is present (else 152, a GB300); no kernel

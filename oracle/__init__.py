@@ -278,18 +278,34 @@ def bf16_gemm_ref(A_bits, B_bits, b_layout, C=None, alpha=1.0, beta=0.0, rows=No
     return gemm(A, B, b_layout, Cd, alpha, beta, None, nthreads)
 
 
+def block_scales_per_channel(b_scale: np.ndarray, N: int, block: int) -> np.ndarray:
+    """A weight-block scale table [G, ceil(N / block)] written out per output
+    channel, [G, N]: channel n takes the scale of block n // block ([W3] §3.2,
+    one scale per group of weights)."""
+    b_scale = np.asarray(b_scale, dtype=np.float32)
+    if b_scale.ndim != 2 or b_scale.shape[1] != -(-N // block):
+        raise ValueError("block scale shape")
+    return np.ascontiguousarray(b_scale[:, np.arange(N) // block])
+
+
 def fp8_gemm_ref(Aq, Bq, b_layout, a_scale, b_scale, C=None, alpha=1.0, beta=0.0,
-                 bias=None, act="none", rows=None, nthreads=None, k_group=0) -> np.ndarray:
+                 bias=None, act="none", rows=None, nthreads=None, k_group=0, b_block=1) -> np.ndarray:
     """Reference for the FP8 form: D = alpha * diag(sa) (Aq Bq) diag(sb) + beta*C,
     then + bias and the activation, on the dequantised E4M3 values ([W3] §3.2).
     With k_group > 0 the scales are per K group: a_scale [G, M] and b_scale
     [G, N] (G = ceil(K / k_group)), and each code is dequantised with its own
-    group's scale before the plain GEMM."""
+    group's scale before the plain GEMM. b_block = 128 (with k_group > 0): one
+    weight scale per block of 128 output channels, b_scale [G, ceil(N / 128)]."""
+    if b_block != 1 and not k_group:
+        raise ValueError("weight blocks need k_group")
     if k_group:
         if np.shape(a_scale) != (-(-Aq.shape[1] // k_group), Aq.shape[0]):
             raise ValueError("a_scale shape")
         Ad = dequant_grouped(_row_select(Aq, rows), np.asarray(a_scale)[:, _rows_index(rows, Aq.shape[0])],
                              1, k_group)
+        N = Bq.shape[0] if b_layout == "nk" else Bq.shape[1]
+        if b_block != 1:
+            b_scale = block_scales_per_channel(b_scale, N, b_block)
         Bd = dequant_grouped(Bq, b_scale, 1 if b_layout == "nk" else 0, k_group)
     else:
         Ad = dequant(_row_select(Aq, rows), _row_select(a_scale, rows), 0)

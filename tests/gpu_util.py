@@ -31,7 +31,7 @@ def run_workload(w: wl.Workload, d_dtype: str | None = None):
     if w.form == "bf16":
         dg.dgemm_bf16(g.A, g.B, D, **kw)
     else:
-        dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, **kw)
+        dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, b_block=w.b_block, **kw)
     assert dg.dgemm_query_device_status() == 0
     return D.cpu(), (None if s is None else s.cpu())
 

@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == sorted(["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_workspace_size", "dgemm_plan",
+    assert names == sorted(["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_fp8_blockscaled", "dgemm_workspace_size",
+                            "dgemm_plan",
                             "dgemm_status_string", "dgemm_query_device_status",
                             "dgemm_fp8_rowquant_noalloc"])
 
@@ -82,6 +83,12 @@ def test_argument_errors_return_before_any_device_call(lib):
     assert fp8(64) == 2 and fp8(200) == 2
     epi = _lib.Epilogue(None, 0, 1, 16)
     assert fp8(128, ctypes.byref(epi), d_dt=2) == 2
+    # block-scaled weights: a per-group form (k_group > 0), same group rules
+    def blk(k_group):
+        return lib.dgemm_fp8_blockscaled(16, 16, 1, 16, 16, k_group, None, 0, 16, 1, 128, 128, 256, 1.0, 0.0,
+                                         None, None, 0, None)
+    assert blk(0) == 1 and blk(-128) == 1
+    assert blk(64) == 2
 
 
 def test_workspace_sizes(lib, monkeypatch):

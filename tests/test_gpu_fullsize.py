@@ -72,3 +72,13 @@ def test_fp8_grouped_scales_full_size_sampled_rows():
     rows = sample_rows(w.M, 24, seed=6)
     ok, msg = bf16_ulp_ok(to_f64(D)[rows], ref_of(w, rows=rows))
     assert ok, msg
+
+
+def test_fp8_block_scaled_full_size_sampled_rows():
+    """The same projection with block-scaled weights: one scale per (128-channel
+    block, 128-element K group)."""
+    w = wl.fp8_grouped(4096, 11008, 4096, k_group=128, b_block=128)
+    D, _ = run_workload(w)
+    rows = sample_rows(w.M, 24, seed=7)
+    ok, msg = bf16_ulp_ok(to_f64(D)[rows], ref_of(w, rows=rows))
+    assert ok, msg

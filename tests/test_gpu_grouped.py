@@ -24,21 +24,22 @@ from tolerances import bf16_ulp_ok, c1_ok
 pytestmark = pytest.mark.gpu
 
 
-def grouped_int_case(M, N, K, g, layout, seed, d_dtype=torch.float32):
+def grouped_int_case(M, N, K, g, layout, seed, d_dtype=torch.float32, b_block=1):
     rng = np.random.default_rng(seed)
     G = -(-K // g)
     Aq = torch.from_numpy(rng.integers(-4, 5, size=(M, K)).astype(np.float32)).to(torch.float8_e4m3fn)
     shape_b = (K, N) if layout == "kn" else (N, K)
     Bq = torch.from_numpy(rng.integers(-4, 5, size=shape_b).astype(np.float32)).to(torch.float8_e4m3fn)
     sa = torch.from_numpy(np.exp2(rng.integers(-1, 2, size=(G, M))).astype(np.float32))
-    sb = torch.from_numpy(np.exp2(rng.integers(-1, 2, size=(G, N))).astype(np.float32))
+    sb = torch.from_numpy(np.exp2(rng.integers(-1, 2, size=(G, -(-N // b_block)))).astype(np.float32))
     n = dg.dgemm_workspace_size(1, M, N, K, layout)
     ws = torch.empty(n, dtype=torch.uint8, device=dev()) if n else None
     D = torch.empty(M, N, dtype=d_dtype, device=dev())
     dg.dgemm_fp8_scaled(Aq.to(dev()), Bq.to(dev()), sa.to(dev()), sb.to(dev()), D, b_layout=layout, k_group=g,
-                        ws=ws)
+                        b_block=b_block, ws=ws)
     assert dg.dgemm_query_device_status() == 0
-    ref = oracle.fp8_gemm_ref(wl.codes_u8(Aq), wl.codes_u8(Bq), layout, sa.numpy(), sb.numpy(), k_group=g)
+    ref = oracle.fp8_gemm_ref(wl.codes_u8(Aq), wl.codes_u8(Bq), layout, sa.numpy(), sb.numpy(), k_group=g,
+                              b_block=b_block)
     return D.cpu().to(torch.float64).numpy(), ref
 
 
@@ -84,6 +85,57 @@ def test_grouped_tail_split_exact(monkeypatch):
     assert plan["tail_tiles"] > 0 and plan["tail_split"] == 2
     got, ref = grouped_int_case(M, N, K, 384, "nk", seed=7)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("g", [128, 256])
+@pytest.mark.parametrize("layout,bn,pair", [("nk", 64, "0"), ("nk", 128, "0"), ("nk", 256, "0"), ("nk", 256, "1"),
+                                            ("kn", 128, "0"), ("kn", 256, "1")])
+def test_block_scaled_tile_exact(layout, bn, pair, g, monkeypatch):
+    """Weights scaled per (128-channel block, K group): each warp's columns
+    share one scale per group (one fused multiply-add per output). N = 400
+    ends inside the fourth block."""
+    monkeypatch.setenv("DGEMM_TILE_N", str(bn))
+    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
+    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "0")
+    got, ref = grouped_int_case(300, 400, 1040, g, layout, seed=bn + g + 7 * int(pair), b_block=128)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_block_scaled_small_m_exact(layout, M):
+    """The transposed small-M form: output channels run along the MMA's rows,
+    so the weight block scale is per row (one per 128 rows of the tile)."""
+    assert dg.dgemm_plan(1, M, 528, 1040, layout, "f32")["swap_ab"] == 1
+    got, ref = grouped_int_case(M, 528, 1040, 128, layout, seed=M + 3, b_block=128)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("cluster", ["1", "0"])
+def test_block_scaled_split_k_exact(cluster, monkeypatch):
+    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
+    plan = dg.dgemm_plan(1, 256, 512, 4096, "nk", "f32", num_sms=0)
+    assert plan["tail_split"] > 1
+    got, ref = grouped_int_case(256, 512, 4096, 384, "nk", seed=31, b_block=128)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("shape,layout", [((300, 528, 1024), "nk"), ((257, 512, 1024), "kn"),
+                                          ((16, 4224, 1024), "nk")])
+def test_block_scaled_recipe(shape, layout):
+    w = wl.fp8_grouped(*shape, k_group=128, b_layout=layout, seed=sum(shape) + 1, b_block=128)
+    D, _ = run_workload(w)
+    ok, msg = bf16_ulp_ok(to_f64(D), ref_of(w))
+    assert ok, msg
+
+
+def test_block_scaled_needs_k_group():
+    A = torch.zeros(16, 128, dtype=torch.float8_e4m3fn, device=dev())
+    B = torch.zeros(128, 128, dtype=torch.float8_e4m3fn, device=dev())
+    s = torch.ones(1, device=dev())
+    D = torch.empty(16, 128, device=dev())
+    with pytest.raises(dg.DgemmError):
+        dg.dgemm_fp8_scaled(A, B, s, s, D, b_layout="nk", k_group=0, b_block=128)
 
 
 def test_grouped_bf16_output_rounds_once():

