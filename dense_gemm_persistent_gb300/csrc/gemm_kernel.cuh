@@ -239,6 +239,8 @@ struct Cfg {
     static_assert(!GS_SMEM || 128 % EPI_COLS == 0, "warp columns within a weight block");
     static_assert(BN < 32 || BN % 32 == 0, "epilogue reads 32-column units");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
+    // full/empty per stage, 2 + 2 accumulator, drain, scale slots; TMEM address + abort flag
+    static_assert((2 * STAGES + 5 + 2 * SC_SLOTS) * 8 + 8 <= BAR_BYTES, "barriers fit");
     // split-K through the cluster parks a whole accumulator in the pipeline buffers
     static_assert(EPI_WARPS * BN / (EPI_WARPS / 4) * 32 * 4 <= STAGES * STAGE_BYTES, "parked partials fit");
 };
