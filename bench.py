@@ -389,7 +389,7 @@ def run_ours(args, rank, world, local):
 
     # ---- roofline of the kernel (one launch per step)
     plan = dg.dgemm_plan(w.form == "fp8", w.M, w.N, w.K, w.b_layout, w.d_dtype, out_quant=w.out_quant,
-                         act=w.act, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+                         act=w.act, k_group=w.k_group, num_sms=0)
     dsz = {"f32": 4, "bf16": 2, "e4m3": 1}[w.d_dtype]
     esz = 2 if w.form == "bf16" else 1
     c_in = 4 if (w.C is not None and w.beta != 0) else 0

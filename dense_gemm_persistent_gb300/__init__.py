@@ -147,13 +147,14 @@ def dgemm_workspace_size(is_fp8, M, N, K, b_layout="nk", *, out_quant="none", ac
 
 
 def dgemm_plan(is_fp8, M, N, K, b_layout="nk", d_dtype="bf16", *, out_quant="none", act="none",
-               num_sms=152) -> dict:
-    """The plan the library would use (host-only; no GPU needed)."""
+               k_group=0, num_sms=152) -> dict:
+    """The plan the library would use (host-only; no GPU needed). k_group as for
+    dgemm_fp8_scaled."""
     epi = Epilogue(None, ACT[act], QUANT[out_quant], None)
     plan = Plan()
     d = {"f32": F32, "bf16": BF16, "e4m3": E4M3}[d_dtype]
     code = load().dgemm_plan(int(bool(is_fp8)), M, N, K, B_KN if b_layout == "kn" else B_NK, d,
-                             ctypes.byref(epi), int(num_sms), ctypes.byref(plan))
+                             ctypes.byref(epi), int(k_group), int(num_sms), ctypes.byref(plan))
     _check(code, "dgemm_plan")
     return {name: getattr(plan, name) for name, _ in Plan._fields_}
 

@@ -45,7 +45,7 @@ SIGNATURES = {
     "dgemm_fp8_blockscaled": (_i32, [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i64, _i64, _i64,
                                      _f32, _f32, ctypes.POINTER(Epilogue), _vp, _sz, _vp]),
     "dgemm_workspace_size": (_sz, [_i32, _i64, _i64, _i64, _i32, ctypes.POINTER(Epilogue)]),
-    "dgemm_plan": (_i32, [_i32, _i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Epilogue), _i32,
+    "dgemm_plan": (_i32, [_i32, _i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Epilogue), _i32, _i32,
                           ctypes.POINTER(Plan)]),
     "dgemm_status_string": (ctypes.c_char_p, [_i32]),
     "dgemm_query_device_status": (_i32, [_vp]),

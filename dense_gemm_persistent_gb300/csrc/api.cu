@@ -678,7 +678,8 @@ size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b
 }
 
 dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t b_layout,
-                          dgemm_dtype_t d_dtype, const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan) {
+                          dgemm_dtype_t d_dtype, const dgemm_epilogue_t* epi, int k_group, int num_sms,
+                          dgemm_plan_t* plan) {
     if (!plan) return DGEMM_ERR_INVALID_VALUE;
     int pairs = num_sms / 2, quads = quads_estimate(num_sms);
     if (num_sms <= 0) {  // the current device: its SM count and measured cluster occupancy
@@ -692,7 +693,7 @@ dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K, dgemm_b_l
     }
     Plan p;
     const dgemm_status_t st =
-        make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, pairs, quads, true, &p);
+        make_plan(is_fp8 ? 1 : 0, M, N, K, b_layout, d_dtype, epi, num_sms, pairs, quads, true, &p, k_group);
     if (st == DGEMM_OK) *plan = p.pub;
     return st;
 }

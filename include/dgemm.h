@@ -214,12 +214,13 @@ size_t dgemm_workspace_size(int is_fp8, int64_t M, int64_t N, int64_t K,
 /* The plan a call with these arguments would use on a GPU with num_sms SMs
  * (host-only, no GPU needed; CTA pairs assumed to fill half the SMs), or, with
  * num_sms <= 0, on the current device (its SM count and measured CTA-pair
- * occupancy). Assumes a workspace of at least dgemm_workspace_size bytes.
- * Returns DGEMM_OK and fills *plan, or the same argument error the GEMM call
- * would return for these sizes. */
+ * occupancy). k_group as for dgemm_fp8_scaled (0 for BF16 and per-row scales;
+ * the block-scaled entry plans like its k_group). Assumes a workspace of at
+ * least dgemm_workspace_size bytes. Returns DGEMM_OK and fills *plan, or the
+ * same argument error the GEMM call would return for these sizes. */
 dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K,
                           dgemm_b_layout_t b_layout, dgemm_dtype_t d_dtype,
-                          const dgemm_epilogue_t* epi, int num_sms, dgemm_plan_t* plan);
+                          const dgemm_epilogue_t* epi, int k_group, int num_sms, dgemm_plan_t* plan);
 
 /* Static English description of a status code; never NULL. */
 const char* dgemm_status_string(dgemm_status_t status);

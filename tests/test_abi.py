@@ -131,6 +131,17 @@ def test_plans_for_the_five_workloads(lib):
         assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
 
 
+def test_plan_of_per_group_scales(lib):
+    """The plan query takes k_group: K groups of 128 on workload 3's shape are
+    32 scale groups on the CTA-pair 256 x 256 kernel with 5 stages (one fewer:
+    the scale ring takes shared memory); invalid groups fail as the call would."""
+    p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=128, num_sms=152)
+    assert (p["k_groups"], p["cta_group"], p["tile_n"], p["stages"]) == (32, 2, 256, 5)
+    assert dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)["stages"] == 6
+    with pytest.raises(dg.DgemmError):
+        dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=64, num_sms=152)
+
+
 def test_tile_width_and_pair_overrides(lib, monkeypatch):
     monkeypatch.setenv("DGEMM_TILE_N", "128")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tile_n"] == 128

@@ -47,9 +47,12 @@ def grouped_int_case(M, N, K, g, layout, seed, d_dtype=torch.float32, b_block=1)
 @pytest.mark.parametrize("layout,bn,pair", [("nk", 64, "0"), ("nk", 128, "0"), ("nk", 256, "0"), ("nk", 256, "1"),
                                             ("kn", 128, "0"), ("kn", 256, "0"), ("kn", 256, "1")])
 def test_grouped_tile_exact(layout, bn, pair, g, monkeypatch):
+    """Every tile variant, with the plan checked to use it."""
     monkeypatch.setenv("DGEMM_TILE_N", str(bn))
     monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "0")
+    plan = dg.dgemm_plan(1, 300, 528, 1040, layout, "f32", k_group=g, num_sms=0)
+    assert (plan["tile_n"], plan["cta_group"], plan["k_groups"]) == (bn, 2 if pair == "1" else 1, -(-1040 // g))
     # K = 1040: nine K slices, the last one partial; groups of 128 or 384
     got, ref = grouped_int_case(300, 528, 1040, g, layout, seed=bn + g + int(pair))
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
@@ -70,7 +73,7 @@ def test_grouped_split_k_segments_inside_groups_exact(M, N, K, cluster, monkeypa
     """Under-filled grids split every tile into K segments of 8 slices; with
     groups of 3 slices (384 elements) most segments start inside a group."""
     monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
-    plan = dg.dgemm_plan(1, M, N, K, "nk", "f32", num_sms=0)
+    plan = dg.dgemm_plan(1, M, N, K, "nk", "f32", k_group=384, num_sms=0)
     assert plan["tail_split"] > 1 and plan["cluster_split"] == int(cluster)
     got, ref = grouped_int_case(M, N, K, 384, "nk", seed=K + M)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
@@ -81,7 +84,7 @@ def test_grouped_tail_split_exact(monkeypatch):
     monkeypatch.setenv("DGEMM_TILE_N", "64")
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
     M, N, K = 1280, 1024, 2064     # 160 tiles of 128 x 64: the last 8 are split
-    plan = dg.dgemm_plan(1, M, N, K, "nk", "f32", num_sms=0)
+    plan = dg.dgemm_plan(1, M, N, K, "nk", "f32", k_group=384, num_sms=0)
     assert plan["tail_tiles"] > 0 and plan["tail_split"] == 2
     got, ref = grouped_int_case(M, N, K, 384, "nk", seed=7)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
@@ -114,8 +117,8 @@ def test_block_scaled_small_m_exact(layout, M):
 @pytest.mark.parametrize("cluster", ["1", "0"])
 def test_block_scaled_split_k_exact(cluster, monkeypatch):
     monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
-    plan = dg.dgemm_plan(1, 256, 512, 4096, "nk", "f32", num_sms=0)
-    assert plan["tail_split"] > 1
+    plan = dg.dgemm_plan(1, 256, 512, 4096, "nk", "f32", k_group=384, num_sms=0)
+    assert plan["tail_split"] > 1 and plan["cluster_split"] == int(cluster)
     got, ref = grouped_int_case(256, 512, 4096, 384, "nk", seed=31, b_block=128)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
