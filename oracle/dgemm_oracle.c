@@ -13,7 +13,7 @@
  *  [W1] DeepGEMM write-up, czchanglian.com/news/51329
  *  [W3] "DeepGEMM: FP8 Tensor Core GEMM", bjdmk.com.cn/news/6078902
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *  - beta == 0 means C is not read (BLAS convention).
  *  - E4M3 is the "fn" variant: bias 7, no infinities, S.1111.111 is NaN, max
  *    finite 448 (the per-row scale amax/448 of the workloads pins max = 448).
