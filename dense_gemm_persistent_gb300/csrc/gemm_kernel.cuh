@@ -104,12 +104,16 @@ struct Params {
     unsigned* status;        // sticky device error word
     // Split tiles (all modes): tiles [0, dp_tiles) run whole; each of the
     // remaining tiles is split along K into `split` segments (tail_items in
-    // all), every unit taking at most one, as its last item. 32-column unit u
-    // of each epilogue warp's region belongs to segment u % split: a segment
-    // parks the units others own as FP32 partials in `partials`, counts its
-    // arrival in tail_count, waits (bounded) for every segment of the region,
-    // and finishes its own units from its accumulator plus the others' partials.
+    // all), every unit taking at most one (before its whole tiles, if any;
+    // with seg_first the split tiles are the first num_tiles - dp_tiles of the
+    // raster instead of the last).
+    // 32-column unit u of each epilogue warp's region belongs to segment
+    // u % split: a segment parks the units others own as FP32 partials in
+    // `partials`, counts its arrival in tail_count, waits (bounded) for every
+    // segment of the region, and finishes its own units from its accumulator
+    // plus the others' partials.
     int dp_tiles, split, tail_items;
+    int seg_first;           // 1: a unit runs its split item before its whole tiles
     float* partials;         // [tail_items][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4
     // Split-K through distributed shared memory (single-CTA kernels, under-
     // filled grids): the split K segments of a tile are the CTAs of one
@@ -120,7 +124,7 @@ struct Params {
     // the tiles from dp_tiles on is run as two 256 x 128 halves (tail_items =
     // 2 x those tiles), each a whole K range with an N = 128 MMA; no partials.
     int tail_halves;
-    unsigned long long* tail_count;  // [num_tiles - dp_tiles][CTAS][EPI_WARPS]: (epoch << 8) | arrivals
+    unsigned long long* tail_count;  // [split tile][CTAS][EPI_WARPS]: (epoch << 8) | arrivals
     unsigned long long epoch;        // unique per launch (56 bits): stale counters need no clearing
 };
 
@@ -130,18 +134,41 @@ struct Work {
     int half;   // -1: the whole tile; 0 / 1: that 128-column half (tail_halves)
 };
 
-// The iter-th work item of a unit (a CTA, or a CTA pair): first its whole
-// tiles unit, unit + units, ... below dp_tiles, then tail items likewise.
+// The iter-th work item of a unit (a CTA, or a CTA pair): its whole tiles
+// unit, unit + units, ... (dp_tiles of them in all), then its tail item (a K
+// segment or an N half of a split tile), or with seg_first its K segment first.
 __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, int iter, Work& w) {
+    // With seg_first, a unit's K segment of a split tile runs before its whole
+    // tiles, so that the segments' exchange of partial sums (a chain of L2 round
+    // trips) overlaps the next tile's mainloop instead of ending the kernel.
+    // Every segment of a split tile is then its unit's first item, all running
+    // at once, and the split tiles are the raster's first ones (tiles [0, S),
+    // whole tiles from S on), next to the whole tiles started alongside them.
+    const bool front = p.seg_first && p.split > 1 && !p.tail_halves && p.dp_tiles > 0;
+    const bool seg_first = front && unit < p.tail_items;
+    const int dp0 = front ? p.num_tiles - p.dp_tiles : 0;   // first whole tile
+    if (seg_first) {
+        if (iter == 0) {
+            const int seg = unit % p.split;
+            w.half = -1;
+            w.tile = unit / p.split;
+            w.kb0 = (seg * p.k_blocks) / p.split;
+            w.kb1 = ((seg + 1) * p.k_blocks) / p.split;
+            w.item = unit;
+            return true;
+        }
+        --iter;
+    }
     const int dp_count = p.dp_tiles > unit ? (p.dp_tiles - unit + units - 1) / units : 0;
     w.half = -1;
     if (iter < dp_count) {
-        w.tile = unit + iter * units;
+        w.tile = dp0 + unit + iter * units;
         w.kb0 = 0;
         w.kb1 = p.k_blocks;
         w.item = -1;
         return true;
     }
+    if (seg_first) return false;   // its split item ran first
     const int j = unit + (iter - dp_count) * units;
     if (j >= p.tail_items) return false;
     if (p.tail_halves) {
@@ -1216,7 +1243,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // adds the others' partials of its own units to its accumulator and
             // stores them directly: about one round trip through L2 per segment
             // instead of a single warp reading every partial unit by unit.
-            const int item0 = part ? (w.tile - p.dp_tiles) * p.split : 0;
+            const int item0 = part ? (w.item / p.split) * p.split : 0;
             const int seg = part ? w.item - item0 : 0;
             auto owner = [&](int u) { return u % p.split; };
             // generic writes to buffers the TMA (async proxy) filled
@@ -1245,8 +1272,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                     }
                 }
-                if (!CF::GS && u == nunits - 1) {
-                    // Last read of this accumulator: hand it back to the MMA warp.
+                if (!CF::GS && u == nunits - 1 && !part) {
+                    // Last read of this accumulator: hand it back to the MMA warp
+                    // (a K segment's, after its units are finished: it reads its own
+                    // units again then).
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -1308,15 +1337,15 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     // The counter word holds (launch epoch << 8) | arrivals; a word
                     // left by any earlier launch counts as zero arrivals. Every
                     // segment of a tile runs at once (each unit takes at most one
-                    // split item, as its last, and the grid is resident), and the
-                    // wait is bounded regardless.
+                    // split item, before its whole tiles, and the grid is
+                    // resident), and the wait is bounded regardless.
                     __threadfence();   // this lane's partial stores before the count
                     __syncwarp();
                     const bool owns = seg < NUNITS;
                     unsigned ready = 0;
                     if (lane == 0) {
                         unsigned long long* cnt =
-                            p.tail_count + ((w.tile - p.dp_tiles) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
+                            p.tail_count + ((w.item / p.split) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
                         __threadfence();
                         unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), next = 0;
                         for (int tries = 0; tries < 4096; ++tries) {
@@ -1344,9 +1373,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         if (!ready) {
                             ok = false;
                         } else {
-                            // Own segment from Tensor Memory (the unit's last item, so
-                            // its accumulator is never overwritten), the others from
-                            // the workspace, all their loads in flight together.
+                            // Own segment from Tensor Memory (handed back to the MMA
+                            // only after this), the others from the workspace, all
+                            // their loads in flight together.
 #pragma unroll U_UNROLL
                             for (int u = 0; u < NUNITS; ++u) {
                                 if (owner(u) != seg) continue;
@@ -1384,6 +1413,17 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
+            if (!CF::GS && part) {
+                // the K segment's last read of this accumulator is done
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (CF::PAIR && rank != 0)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
+                    else
+                        mbar_arrive(&acc_empty[buf]);
+                }
+            }
             if constexpr (CF::MODE == MODE_ROWQ) {
                 // This warp's share of the item is done: once its TMA stores have
                 // completed (and, like its plain stores and row maxima, are
