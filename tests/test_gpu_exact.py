@@ -168,12 +168,16 @@ def test_pair_phases_across_many_tiles_exact(kblocks):
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
+@pytest.mark.parametrize("seg_first", ["1", "0"])
 @pytest.mark.parametrize("shape,layout,pair", [((4096, 4096, 1024), "kn", "1"), ((4096, 4096, 1024), "nk", "0"),
                                                ((2304, 2816, 1024), "nk", "1"), ((2560, 2048, 1024), "kn", "0"),
                                                ((4000, 1288, 1024), "kn", "1")])
-def test_tail_split_exact(shape, layout, pair, monkeypatch):
+def test_tail_split_exact(shape, layout, pair, seg_first, monkeypatch):
     """The last partial wave's tiles split along K (FP32 partials in the
-    workspace, last-arriving warp sums them): still bit-exact."""
+    workspace, each segment finishing its share of the units): still
+    bit-exact, with the segments run before the whole tiles (at the raster's
+    start) and after them (at its end)."""
+    monkeypatch.setenv("DGEMM_SEG_FIRST", seg_first)
     monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")   # split even these short tiles
     monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")      # along K, not N
@@ -184,8 +188,10 @@ def test_tail_split_exact(shape, layout, pair, monkeypatch):
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
+@pytest.mark.parametrize("seg_first", ["1", "0"])
 @pytest.mark.parametrize("layout", ["nk", "kn"])
-def test_tail_split_fp8_exact(layout, monkeypatch):
+def test_tail_split_fp8_exact(layout, seg_first, monkeypatch):
+    monkeypatch.setenv("DGEMM_SEG_FIRST", seg_first)
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
     monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
     plan = dg.dgemm_plan(1, 4096, 11008, 2048, layout, "f32")

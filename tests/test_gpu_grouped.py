@@ -79,7 +79,9 @@ def test_grouped_split_k_segments_inside_groups_exact(M, N, K, cluster, monkeypa
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
-def test_grouped_tail_split_exact(monkeypatch):
+@pytest.mark.parametrize("seg_first", ["1", "0"])
+def test_grouped_tail_split_exact(seg_first, monkeypatch):
+    monkeypatch.setenv("DGEMM_SEG_FIRST", seg_first)
     monkeypatch.setenv("DGEMM_CTA_PAIR", "0")
     monkeypatch.setenv("DGEMM_TILE_N", "64")
     monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
