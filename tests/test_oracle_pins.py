@@ -195,6 +195,15 @@ def test_silu_and_gelu_closed_forms():
     assert oracle.gelu(40.0) == 40.0 and oracle.silu(-800.0) == 0.0
 
 
+def test_gelu_is_the_erf_form():
+    # gelu(x) = x * Phi(x) with the exact normal CDF: standard-normal table values
+    # Phi(1) = 0.841344746068543, Phi(2) = 0.977249868051821, Phi(-0.5) =
+    # 0.308537538725987. The tanh approximation misses these by 2e-5 to 2e-4.
+    assert abs(oracle.gelu(1.0) - 0.841344746068543) < 1e-14
+    assert abs(oracle.gelu(2.0) - 2 * 0.977249868051821) < 1e-14
+    assert abs(oracle.gelu(-0.5) - (-0.5) * 0.308537538725987) < 1e-14
+
+
 def test_epilogue_bias_then_activation():
     X = np.array([[-1.0, 0.0, 2.0]])
     bias = np.array([0.5, -0.25, 1.0], np.float32)
