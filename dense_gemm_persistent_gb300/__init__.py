@@ -40,6 +40,46 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _on_device(t) -> bool:
+    return t.is_cuda
+
+
+def _require(t, name, shape=None, dtypes=None):
+    """The C ABI takes dense row-major device buffers and trusts their sizes, so
+    a tensor that is not one (a CPU tensor, a transposed or sliced view, a wrong
+    shape or element type) is refused here instead of being read as one."""
+    if t is None:
+        return
+    if not _on_device(t):
+        raise ValueError(f"{name} must be a CUDA tensor (it is on {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major); pass {name}.contiguous()")
+    if shape is not None and tuple(t.shape) != shape:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {[str(d) for d in dtypes]}")
+
+
+def _require_common(M, N, C, beta, D, bias, out_row_scale, ws):
+    torch = _torch()
+    _require(D, "D", (M, N), (torch.float32, torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    if beta != 0.0:   # C is read only then (and may be None otherwise)
+        _require(C, "C", (M, N), (torch.float32, torch.bfloat16))
+    _require(bias, "bias", (N,), (torch.float32,))
+    _require(out_row_scale, "out_row_scale", (M,), (torch.float32,))
+    _require(ws, "ws")
+
+
+def _require_fp8(Aq, Bq, a_scale, b_scale):
+    torch = _torch()
+    codes = (torch.float8_e4m3fn, torch.uint8)
+    _require(Aq, "Aq", None, codes)
+    _require(Bq, "Bq", None, codes)
+    # the scale tables' shapes depend on k_group and b_block: the library checks those
+    _require(a_scale, "a_scale", None, (torch.float32,))
+    _require(b_scale, "b_scale", None, (torch.float32,))
+
+
 def _stream(stream):
     if stream is None:
         return _torch().cuda.current_stream().cuda_stream
@@ -83,6 +123,10 @@ def dgemm_bf16(A, B, D, *, b_layout="kn", C=None, alpha=1.0, beta=0.0, bias=None
     least dgemm_workspace_size(...) bytes. Returns D.
     """
     M, N, K = _dims(A, B, b_layout)
+    torch = _torch()
+    _require(A, "A", None, (torch.bfloat16,))
+    _require(B, "B", None, (torch.bfloat16,))
+    _require_common(M, N, C, beta, D, bias, out_row_scale, ws)
     epi = _epilogue(bias, act, out_quant, out_row_scale)
     code = load().dgemm_bf16(_ptr(A), _ptr(B), B_KN if b_layout == "kn" else B_NK, _ptr(C),
                              _dtype_code(C) if C is not None else F32, _ptr(D), _dtype_code(D),
@@ -105,6 +149,8 @@ def dgemm_fp8_scaled(Aq, Bq, a_scale, b_scale, D, *, b_layout="nk", k_group=0, b
     Other arguments as for dgemm_bf16. Returns D.
     """
     M, N, K = _dims(Aq, Bq, b_layout)
+    _require_fp8(Aq, Bq, a_scale, b_scale)
+    _require_common(M, N, C, beta, D, bias, out_row_scale, ws)
     epi = _epilogue(bias, act, out_quant, out_row_scale)
     if b_block != 1:
         if b_block != 128:
@@ -130,6 +176,8 @@ def dgemm_fp8_rowquant_noalloc(Aq, Bq, a_scale, b_scale, Dq, out_row_scale, *, b
     array inside the library (M*N up to about 16.7 million; calls that overlap
     on the GPU race on it). Dq [M,N] uint8 E4M3 codes, out_row_scale [M] fp32."""
     M, N, K = _dims(Aq, Bq, b_layout)
+    _require_fp8(Aq, Bq, a_scale, b_scale)
+    _require_common(M, N, C, beta, Dq, bias, out_row_scale, None)
     epi = _epilogue(bias, act, "e4m3_row_amax", out_row_scale)
     code = load().dgemm_fp8_rowquant_noalloc(_ptr(Aq), _ptr(Bq), B_KN if b_layout == "kn" else B_NK,
                                              _ptr(a_scale), _ptr(b_scale), _ptr(C),
