@@ -151,3 +151,56 @@ def test_tile_width_and_pair_overrides(lib, monkeypatch):
     monkeypatch.setenv("DGEMM_CTA_PAIR", "0")
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")
     assert (p["cta_group"], p["tile_m"], p["tile_n"], p["num_tiles"], p["stages"]) == (1, 128, 256, 512, 4)
+
+
+C_CALLER = r"""
+/* A plain C11 caller of the library: the header must compile as C, and the
+ * host-only entry points must link and behave without Python or a GPU. */
+#include <stdio.h>
+#include <string.h>
+#include "dgemm.h"
+
+int main(void) {
+    dgemm_plan_t plan;
+    memset(&plan, 0, sizeof plan);
+    /* BF16 4096^3, B stored K x N, BF16 out, on a 152-SM GPU */
+    dgemm_status_t st = dgemm_plan(0, 4096, 4096, 4096, DGEMM_B_KN, DGEMM_BF16, NULL, 0, 152, &plan);
+    printf("plan %d %d %d %d %d %d\n", (int)st, plan.tile_m, plan.tile_n, plan.cta_group, plan.num_tiles,
+           plan.swap_ab);
+    /* decode shape: small M runs transposed */
+    st = dgemm_plan(0, 16, 18432, 7168, DGEMM_B_NK, DGEMM_BF16, NULL, 0, 152, &plan);
+    printf("decode %d %d\n", (int)st, plan.swap_ab);
+    dgemm_epilogue_t epi = {NULL, DGEMM_ACT_SILU, DGEMM_QUANT_E4M3_ROW_AMAX, NULL};
+    printf("ws %zu\n", dgemm_workspace_size(1, 256, 512, 384, DGEMM_B_NK, &epi));
+    /* an argument error returns before any device call */
+    st = dgemm_bf16(NULL, NULL, DGEMM_B_KN, NULL, DGEMM_F32, NULL, DGEMM_BF16, 128, 128, 128, 1.0f, 0.0f,
+                    NULL, NULL, 0, NULL);
+    printf("null %d %s\n", (int)st, dgemm_status_string(st));
+    return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(_lib.lib_path())
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), "-L", libdir, "-ldgemm", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    lines = dict(line.split(" ", 1) for line in out.stdout.strip().splitlines())
+    assert lines["plan"] == "0 256 256 2 256 0"          # CTA-pair 256 x 256 tiles, 256 of them
+    assert lines["decode"] == "0 1"                        # transposed small-M form
+    ws = dg.dgemm_workspace_size(1, 256, 512, 384, "nk", out_quant="e4m3_row_amax", act="silu")
+    assert int(lines["ws"]) == ws > 2 * 256 * 512          # at least the BF16 stash
+    code, text = lines["null"].split(" ", 1)
+    assert int(code) == 1 and text == dg.dgemm_status_string(1)   # DGEMM_ERR_INVALID_VALUE
