@@ -121,9 +121,13 @@ typedef struct {
     int k_groups;          /* K-group promotion: K is split into this many
                               contiguous groups, each accumulated by the tensor
                               core separately and summed in FP32 (1 = off)      */
-    int tail_tiles;        /* tiles of the last, partial wave that are split
+    int tail_tiles;        /* tiles beyond the last whole wave that are split
                               (along K, or along N with tail_halves) so the
-                              wave finishes sooner (0 = none)                  */
+                              partial wave finishes sooner (0 = none). In the
+                              plain (not requantising) form their K segments
+                              run first, as the raster's first tiles, and their
+                              partial sums are exchanged while whole tiles
+                              run; otherwise they run last                    */
     int tail_split;        /* K segments per tail tile (1 = no splitting)       */
     int cluster_split;     /* 1: the K segments of each split tile run as one
                               thread-block cluster and are summed through
