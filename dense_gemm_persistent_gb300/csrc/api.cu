@@ -593,9 +593,10 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     p.dp_tiles = plan.dp_tiles;
     p.split = plan.split;
     p.tail_items = plan.tail_items;
-    // K segments of the last partial wave's tiles run first in the plain tile
-    // form (their exchange then overlaps whole tiles: +2 % at 4096^3 BF16); the
-    // requantising form keeps them last (no gain measured there).
+    // The K segments of split tiles run first in the plain tile form, as the
+    // raster's first tiles, so their exchange of partial sums overlaps whole
+    // tiles (+5 % at 4096^3 BF16); the requantising form keeps them last (its
+    // row bands count the split tiles at the end of the raster).
     // DGEMM_SEG_FIRST=0 keeps them last everywhere (comparisons).
     const char* sf_env = std::getenv("DGEMM_SEG_FIRST");
     p.seg_first = (plan.mode == dg::MODE_TILE && !(sf_env && sf_env[0] == '0')) ? 1 : 0;
