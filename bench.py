@@ -7,7 +7,14 @@ seeded workloads of workloads.py). The default workload is number 2, the BF16
 GEMM M = N = K = 4096, on which the headline metric (TFLOPS and fraction of the
 dense tensor-core peak) is quoted; --config picks another. Input sets are
 rotated so that the operands of every timed call were evicted from L2 (their
-total is several times the 129 MB L2).
+total is several times the 129 MB L2). After the headline, the other four
+workloads are timed the same way in the same process and reported under
+"workloads" in the same JSON line (--no-extra skips them).
+
+SM clocks, power and clock-event reasons are read in-process through NVML
+while the timed region runs on the GPU (polled until its end event
+completes), so even a region of a millisecond or two carries its own clock
+record.
 
 Rank 0 prints ONE JSON line. Under torchrun (N > 1) every rank runs the same
 workload on its own GPU (independent replicas: GEMM problems shard without any
@@ -135,8 +142,118 @@ def recorded_traffic(workload):
     return None
 
 
+class NvmlClocks:
+    """SM clock, power and clock-event reasons read in-process through NVML
+    (the driver's libnvidia-ml.so.1, through ctypes; only reads). sample()
+    returns (sm_mhz, power_w, reason_bits) or None."""
+    # clock-event reason bits (nvml.h): the ones a run is judged by
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, torch_index: int):
+        import ctypes
+        self.ok = False
+        self.max_mhz = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        self.c = ctypes
+        self.lib = lib
+        if lib.nvmlInit_v2() != 0:
+            return
+        self.h = ctypes.c_void_p()
+        found = False
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(torch_index).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            found = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) == 0
+        except Exception:
+            found = False
+        if not found:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = torch_index
+            parts = [x for x in vis.split(",") if x.strip()]
+            if parts and parts[0].strip().isdigit() and torch_index < len(parts):
+                idx = int(parts[torch_index])
+            found = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(self.h)) == 0
+        if not found:
+            return
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self.ok = True
+
+    def sample(self):
+        if not self.ok:
+            return None
+        c = self.c
+        mhz, mw, bits = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, c.byref(mhz)) != 0:
+            return None
+        power = float(mw.value) / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw)) == 0 else None
+        reasons = int(bits.value) if (self.reasons_fn and self.reasons_fn(self.h, c.byref(bits)) == 0) else 0
+        return float(mhz.value), power, reasons
+
+
+def summarize_clock_samples(samples, max_mhz, before=None, after=None) -> dict:
+    """Median SM clock, power and the clock-event reasons seen over the samples
+    taken while the timed region ran (each (sm_mhz, power_w, reason_bits))."""
+    sm = [x[0] for x in samples]
+    power = [x[1] for x in samples if x[1] is not None]
+    bits = 0
+    for x in samples:
+        bits |= x[2]
+    reasons = sorted(name for b, name in NvmlClocks.REASONS.items() if bits & b)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max_mhz,
+            "sm_mhz_min": min(sm) if sm else None, "sm_mhz_max": max(sm) if sm else None,
+            "power_w_max": max(power) if power else None, "reasons": reasons, "samples": len(sm),
+            "sm_mhz_before": None if before is None else before[0],
+            "sm_mhz_after": None if after is None else after[0],
+            "source": "NVML in-process, polled while the timed region ran on the GPU"}
+
+
+class RegionClocks:
+    """Clock record of one timed region: one NVML sample right before it, then
+    samples polled until its end event has completed, then one right after;
+    nvidia-smi sampling (100 ms) where NVML cannot be loaded."""
+
+    def __init__(self, torch_index: int):
+        self.nvml = NvmlClocks(torch_index)
+        self.smi = None if self.nvml.ok else ClockSampler(torch_index)
+
+    def start(self):
+        self.samples = []
+        self.before = self.nvml.sample() if self.nvml.ok else None
+        if self.smi:
+            self.smi.start()
+
+    def poll_until(self, event):
+        """Samples while `event` (recorded after the timed launches) is pending."""
+        import time as _t
+        while not event.query():
+            if self.nvml.ok:
+                x = self.nvml.sample()
+                if x is not None:
+                    self.samples.append(x)
+            else:
+                _t.sleep(0.001)
+
+    def stop(self) -> dict:
+        if self.smi:
+            return self.smi.stop()
+        after = self.nvml.sample()
+        return summarize_clock_samples(self.samples, self.nvml.max_mhz, self.before, after)
+
+
 class ClockSampler:
-    """nvidia-smi sampling of SM clock, power and throttle reasons."""
+    """nvidia-smi sampling of SM clock, power and throttle reasons (used when
+    NVML cannot be loaded in-process)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -256,43 +373,158 @@ def oracle_sample(w, seconds: float):
 
 # ------------------------------------------------------------------ our arm
 
+class Rig:
+    """Device-resident input sets of one workload, rotated so that every timed
+    call finds its operands out of L2, and the library call on set i."""
+
+    def __init__(self, w, dev, stream):
+        import torch
+        import dense_gemm_persistent_gb300 as dg
+        self.w, self.dev, self.stream, self.dg = w, dev, stream, dg
+        self.tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}[w.d_dtype]
+        self.ws_bytes = dg.dgemm_workspace_size(w.form == "fp8", w.M, w.N, w.K, w.b_layout, out_quant=w.out_quant)
+        in_bytes = sum(t.numel() * t.element_size() for t in w.tensors().values())
+        out_bytes = w.M * w.N * torch.tensor([], dtype=self.tdt).element_size()
+        self.set_bytes = in_bytes + out_bytes + self.ws_bytes
+        self.nsets = max(2, min(160, math.ceil(3 * L2_BYTES / max(self.set_bytes, 1))))
+        self.sets = []
+        for _ in range(self.nsets):
+            g = w.to(dev)
+            D = torch.empty(w.M, w.N, dtype=self.tdt, device=dev)
+            s = torch.empty(w.M, dtype=torch.float32, device=dev) if w.out_quant != "none" else None
+            ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev) if self.ws_bytes else None
+            self.sets.append((g, D, s, ws))
+
+    def l2_note(self) -> str:
+        return f"rotating {self.nsets} input sets of {self.set_bytes / 2**20:.0f} MiB (> L2 129 MiB)"
+
+    def call(self, i, bufs=None):
+        w, dg = self.w, self.dg
+        g, D, s, ws = (bufs or self.sets)[i % (len(bufs) if bufs else self.nsets)]
+        kw = dict(b_layout=w.b_layout, C=g.C, alpha=w.alpha, beta=w.beta, bias=g.bias, act=w.act,
+                  out_quant=w.out_quant, out_row_scale=s, ws=ws, stream=self.stream)
+        if w.form == "bf16":
+            dg.dgemm_bf16(g.A, g.B, D, **kw)
+        else:
+            dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, b_block=w.b_block, **kw)
+
+    def status_ok(self) -> bool:
+        """No bounded device wait gave up in any call so far (every set's
+        workspace status word and the per-device word; each query clears)."""
+        dg = self.dg
+        ok = dg.dgemm_query_device_status(None, stream=self.stream) == 0
+        for _, _, _, ws in self.sets:
+            if ws is not None and dg.dgemm_query_device_status(ws, stream=self.stream) != 0:
+                ok = False
+        return ok
+
+    def free(self):
+        import torch
+        self.sets = []
+        torch.cuda.empty_cache()
+
+
+def timed_region(rig, steps, warmup, dev, barrier, clocks):
+    """W untimed calls, then exactly `steps` calls between CUDA events on the
+    launching stream, bracketed by a barrier and a device synchronisation on
+    both sides; the SM clocks are sampled while the region runs. Returns the
+    milliseconds of the region (max over ranks) and its clock record."""
+    import torch
+    for i in range(warmup):
+        rig.call(i)
+    torch.cuda.synchronize(dev)
+    if not rig.status_ok():
+        raise RuntimeError("device status after warm-up")
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(rig.stream)
+    for i in range(steps):
+        rig.call(i)
+    e1.record(rig.stream)
+    clocks.poll_until(e1)
+    torch.cuda.synchronize(dev)
+    record = clocks.stop()
+    barrier()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
+    if not rig.status_ok():
+        raise RuntimeError("device status after the timed region")
+    return ms_total, record
+
+
+def roofline_of(w, ms_step, clocks, peaks, peak_kind, n_sm, skinny, plan, traffic):
+    """Achieved rate of the kernel (one launch per step) against its roofline:
+    TFLOP/s against the tensor-core peak, or for skinny (HBM-bound) shapes the
+    compulsory bytes against the measured copy bandwidth; beside it the tensor
+    core's rate at the SM clock sampled during the region."""
+    from dense_gemm_persistent_gb300 import roofline
+    dsz = {"f32": 4, "bf16": 2, "e4m3": 1}[w.d_dtype]
+    esz = 2 if w.form == "bf16" else 1
+    c_in = 4 if (w.C is not None and w.beta != 0) else 0
+    comp = roofline.compulsory_bytes(w.M, w.N, w.K, esz, esz, c_in, dsz)
+    flops = w.flops
+    if skinny:
+        achieved = comp / (ms_step * 1e-3) / 1e9
+        peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+    else:
+        achieved = flops / (ms_step * 1e-3) / 1e12
+        base = peaks["bf16_tflops"]
+        peak = base if w.form == "bf16" else 2.0 * base   # FP8:BF16 dense ratio 2
+        unit, bound = "TFLOP/s", "tensor"
+    # SMs x dense FLOP per clock per SM (128 x 256 x 16 BF16 or x 32 E4M3 MACs
+    # per 128 cycles, measured at that rate) x the median sampled clock
+    flop_per_clk = 8192 if w.form == "bf16" else 16384
+    theo = (n_sm * flop_per_clk * clocks["sm_mhz"] * 1e6 / 1e12) if clocks.get("sm_mhz") else None
+    tflops = flops / (ms_step * 1e-3) / 1e12
+    return {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{peak_kind}" + ("" if w.form == "bf16" or skinny else " bf16 x 2 (FP8:BF16 ratio)"),
+            "compulsory_bytes": int(comp),
+            "tensor_peak_at_clock_tflops": None if theo is None else round(theo, 1),
+            "frac_of_peak_at_clock": None if (theo is None or skinny) else round(tflops / theo, 4),
+            "tiled_traffic_bytes_no_l2": int(roofline.tiled_read_elements(w.M, w.N, w.K, plan["tile_m"],
+                                                                          plan["tile_n"]) * esz
+                                             + w.M * w.N * (dsz + c_in))}
+
+
+def plan_of(dg, w):
+    return dg.dgemm_plan(w.form == "fp8", w.M, w.N, w.K, w.b_layout, w.d_dtype, out_quant=w.out_quant,
+                         act=w.act, k_group=w.k_group, num_sms=0)
+
+
+def is_skinny(w, number, shape, peaks):
+    """HBM-bound: workload 4, or a --shape whose intensity is below the ridge point."""
+    from dense_gemm_persistent_gb300 import roofline
+    if number == 4:
+        return True
+    if not shape:
+        return False
+    esz = 2 if w.form == "bf16" else 1
+    comp = roofline.compulsory_bytes(w.M, w.N, w.K, esz, esz, 0, 2)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return w.flops / comp < ridge
+
+
+def config_of(args, w) -> dict:
+    """The workload's identity: the same dict in both arms."""
+    return {"workload": describe(args), "number": args.config, "M": w.M, "N": w.N, "K": w.K,
+            "b_layout": w.b_layout, "k_group": w.k_group, "b_block": w.b_block}
+
+
 def run_ours(args, rank, world, local):
     import torch
 
     import dense_gemm_persistent_gb300 as dg
-    import workloads as wl
-    from dense_gemm_persistent_gb300 import roofline
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dg.load()
     w = make_workload(args)
     peaks, peak_kind = measured_peaks()
-
-    # ---- rotating input sets (each timed call finds its operands out of L2)
-    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}[w.d_dtype]
-    ws_bytes = dg.dgemm_workspace_size(w.form == "fp8", w.M, w.N, w.K, w.b_layout, out_quant=w.out_quant)
-    in_bytes = sum(t.numel() * t.element_size() for t in w.tensors().values())
-    out_bytes = w.M * w.N * torch.tensor([], dtype=tdt).element_size()
-    set_bytes = in_bytes + out_bytes + ws_bytes
-    nsets = max(2, min(160, math.ceil(3 * L2_BYTES / max(set_bytes, 1))))
-    sets = []
-    for _ in range(nsets):
-        g = w.to(dev)
-        D = torch.empty(w.M, w.N, dtype=tdt, device=dev)
-        s = torch.empty(w.M, dtype=torch.float32, device=dev) if w.out_quant != "none" else None
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
-        sets.append((g, D, s, ws))
     stream = torch.cuda.current_stream(dev)
-
-    def call(i):
-        g, D, s, ws = sets[i % nsets]
-        kw = dict(b_layout=w.b_layout, C=g.C, alpha=w.alpha, beta=w.beta, bias=g.bias, act=w.act,
-                  out_quant=w.out_quant, out_row_scale=s, ws=ws, stream=stream)
-        if w.form == "bf16":
-            dg.dgemm_bf16(g.A, g.B, D, **kw)
-        else:
-            dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, b_block=w.b_block, **kw)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clocks = RegionClocks(local)
 
     dist = world > 1
     if dist:
@@ -302,27 +534,8 @@ def run_ours(args, rank, world, local):
         if dist:
             tdist.barrier()
 
-    for i in range(args.warmup):
-        call(i)
-    torch.cuda.synchronize(dev)
-    if dg.dgemm_query_device_status(stream) != 0:
-        raise RuntimeError("device status after warm-up")
-
-    sampler = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize(dev)
-    sampler.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        call(i)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
-    barrier()
-    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
-    if dg.dgemm_query_device_status(stream) != 0:
-        raise RuntimeError("device status after the timed region")
+    rig = Rig(w, dev, stream)
+    ms_total, clock_rec = timed_region(rig, args.steps, args.warmup, dev, barrier, clocks)
     ms_step = ms_total / args.steps
     flops = w.flops
     tflops = job_rate(flops * args.steps, world, ms_total * 1e-3) / 1e12
@@ -336,7 +549,7 @@ def run_ours(args, rank, world, local):
     # for the readback of that set's previous result.
     host = {k: t.pin_memory() for k, t in w.tensors().items()}
     nbuf = 2
-    bufs = [sets[b % nsets] for b in range(nbuf)]
+    bufs = [rig.sets[b % rig.nsets] for b in range(nbuf)]
     Dh = [torch.empty(bufs[0][1].shape, dtype=bufs[0][1].dtype, pin_memory=True) for _ in range(nbuf)]
     sh = [torch.empty(w.M, dtype=torch.float32, pin_memory=True) if bufs[0][2] is not None else None
           for _ in range(nbuf)]
@@ -361,7 +574,7 @@ def run_ours(args, rank, world, local):
         stream.wait_event(uploaded[b])
         if read_back[b] is not None:
             stream.wait_event(read_back[b])
-        call(b)
+        rig.call(b, bufs)
         computed[b] = ev()
         computed[b].record(stream)
         with torch.cuda.stream(down):
@@ -386,53 +599,27 @@ def run_ours(args, rank, world, local):
     f1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
+    if not rig.status_ok():
+        raise RuntimeError("device status after the end-to-end steps")
 
-    # ---- roofline of the kernel (one launch per step)
-    plan = dg.dgemm_plan(w.form == "fp8", w.M, w.N, w.K, w.b_layout, w.d_dtype, out_quant=w.out_quant,
-                         act=w.act, k_group=w.k_group, num_sms=0)
-    dsz = {"f32": 4, "bf16": 2, "e4m3": 1}[w.d_dtype]
-    esz = 2 if w.form == "bf16" else 1
-    c_in = 4 if (w.C is not None and w.beta != 0) else 0
-    comp = roofline.compulsory_bytes(w.M, w.N, w.K, esz, esz, c_in, dsz)
-    # HBM-bound: workload 4, or a --shape whose intensity is below the ridge point
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    skinny = args.config == 4 or (bool(args.shape) and flops / comp < ridge)
-    if skinny:
-        achieved = comp / (ms_step * 1e-3) / 1e9
-        peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
-    else:
-        achieved = flops / (ms_step * 1e-3) / 1e12
-        base = peaks["bf16_tflops"]
-        peak = base if w.form == "bf16" else 2.0 * base   # FP8:BF16 dense ratio 2
-        unit, bound = "TFLOP/s", "tensor"
-    # The tensor core's rate at the SM clock seen during the timed region:
-    # SMs x dense FLOP per clock per SM (128 x 256 x 16 BF16 or x 32 E4M3 MACs
-    # per 128 cycles, measured at that rate) x the median sampled clock.
-    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    flop_per_clk = 8192 if w.form == "bf16" else 16384
-    theo = (n_sm * flop_per_clk * clocks["sm_mhz"] * 1e6 / 1e12) if clocks.get("sm_mhz") else None
-    traffic = recorded_traffic(workload_key(args))
-    roof = {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic,
-            "peak_source": f"{peak_kind}" + ("" if w.form == "bf16" or skinny else " bf16 x 2 (FP8:BF16 ratio)"),
-            "compulsory_bytes": int(comp),
-            "tensor_peak_at_clock_tflops": None if theo is None else round(theo, 1),
-            "frac_of_peak_at_clock": None if (theo is None or skinny) else round(flops / (ms_step * 1e-3) / 1e12 / theo, 4),
-            "tiled_traffic_bytes_no_l2": int(roofline.tiled_read_elements(w.M, w.N, w.K, plan["tile_m"],
-                                                                          plan["tile_n"]) * esz
-                                             + w.M * w.N * (dsz + c_in))}
+    plan = plan_of(dg, w)
+    skinny = is_skinny(w, args.config, args.shape, peaks)
+    roof = roofline_of(w, ms_step, clock_rec, peaks, peak_kind, n_sm, skinny, plan,
+                       recorded_traffic(workload_key(args)))
+    l2_note = rig.l2_note()
+    rig.free()
+    del host, bufs, Dh, sh
 
     result = {
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.form == "bf16" else "e4m3", "data": "synthetic",
-        "config": {"workload": describe(args), "number": args.config, "M": w.M, "N": w.N, "K": w.K,
-                   "b_layout": w.b_layout, "k_group": w.k_group, "b_block": w.b_block,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"rotating {nsets} input sets of {set_bytes / 2**20:.0f} MiB (> L2 129 MiB)",
-                   "plan": {k: plan[k] for k in ("swap_ab", "tile_m", "tile_n", "stages", "num_tiles", "grid",
-                                                 "cooperative")}},
-        "clocks": clocks,
+        "config": config_of(args, w),
+        "setup": {"parallelism": f"replicas x{world}", "l2": l2_note,
+                  "plan": {k: plan[k] for k in ("swap_ab", "tile_m", "tile_n", "cta_group", "stages", "num_tiles",
+                                                "grid", "cooperative", "tail_tiles", "tail_split", "tail_halves",
+                                                "cluster_split")}},
+        "clocks": clock_rec,
         "e2e": {"value": round(job_rate(flops, world, e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "pipelining": "double-buffered: step i+1's upload overlaps step i's GEMM and readback"},
@@ -440,8 +627,52 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
     }
     if skinny:
-        result["hbm_gbs"] = round(achieved, 1)
+        result["hbm_gbs"] = round(roof["achieved"], 1)
+
+    # ---- the other workloads, timed the same way in the same process
+    if not args.no_extra and not args.shape and not args.k_group:
+        extra = {}
+        launches = args.steps
+        for number in sorted(DESCRIPTIONS):
+            if number == args.config:
+                continue
+            steps = args.steps if args.steps_given else DEFAULT_STEPS[number]
+            extra[str(number)] = time_other(number, steps, args.warmup, dev, stream, barrier, clocks, peaks,
+                                            peak_kind, n_sm, world)
+            launches += steps
+        result["workloads"] = extra
+        result["gpu_launches_all"] = launches
     return result, w
+
+
+def time_other(number, steps, warmup, dev, stream, barrier, clocks, peaks, peak_kind, n_sm, world):
+    """One more workload at its full size, timed like the headline (rotating
+    input sets, CUDA events on the launching stream, clocks sampled during the
+    region): microseconds per call, rate and roofline."""
+    import dense_gemm_persistent_gb300 as dg
+
+    class A:
+        pass
+    a = A()
+    a.config, a.shape, a.k_group, a.b_block = number, None, 0, 1
+    w = make_workload(a)
+    rig = Rig(w, dev, stream)
+    ms_total, rec = timed_region(rig, steps, warmup, dev, barrier, clocks)
+    ms_step = ms_total / steps
+    plan = plan_of(dg, w)
+    skinny = number == 4
+    roof = roofline_of(w, ms_step, rec, peaks, peak_kind, n_sm, skinny, plan, recorded_traffic(str(number)))
+    out = {"workload": DESCRIPTIONS[number], "M": w.M, "N": w.N, "K": w.K, "steps": steps, "warmup": warmup,
+           "us_per_call": round(ms_step * 1e3, 3),
+           "value": round(job_rate(w.flops * steps, world, ms_total * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+           "dtype": "bf16" if w.form == "bf16" else "e4m3", "l2": rig.l2_note(),
+           "plan": {k: plan[k] for k in ("swap_ab", "tile_m", "tile_n", "cta_group", "num_tiles", "grid",
+                                         "cooperative", "tail_tiles", "tail_split", "tail_halves")},
+           "roofline": roof, "clocks": rec}
+    if skinny:
+        out["hbm_gbs"] = roof["achieved"]
+    rig.free()
+    return out
 
 
 def main():
@@ -462,7 +693,10 @@ def main():
                     help="with --k-group: output channels per weight scale (128: block-scaled weights)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="wall time the reference arm spends on warm-up + steps")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the selected workload (not the other four after it)")
     args = ap.parse_args()
+    args.steps_given = args.steps is not None
     if args.steps is None:
         args.steps = 2000 if args.shape else DEFAULT_STEPS[args.config]
     args.warmup = max(args.warmup, 3)
@@ -536,8 +770,7 @@ def run_reference(args, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(args), "number": args.config, "M": w.M, "N": w.N, "K": w.K,
-                   "b_layout": w.b_layout, "k_group": w.k_group, "b_block": w.b_block},
+        "config": config_of(args, w),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} rows of {w.M} per step of the same workload, float64 "
                                    f"oracle, OpenMP"},

@@ -12,11 +12,12 @@ from __future__ import annotations
 
 import ctypes
 
-from ._lib import (ACT, B_KN, B_NK, BF16, E4M3, F32, QUANT, DgemmError, Epilogue, Plan, load,
+from ._lib import (ACT, B_KN, B_NK, BF16, E4M3, F32, QUANT, DgemmError, Epilogue, Overrides, Plan, load,
                    lib_path)
 
 __all__ = ["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_fp8_rowquant_noalloc", "dgemm_workspace_size", "dgemm_plan",
-           "dgemm_status_string", "dgemm_query_device_status", "DgemmError", "load", "lib_path"]
+           "dgemm_status_string", "dgemm_query_device_status", "set_overrides", "get_overrides", "overrides",
+           "DgemmError", "load", "lib_path"]
 
 
 def _torch():
@@ -211,6 +212,55 @@ def dgemm_status_string(code: int) -> str:
     return load().dgemm_status_string(int(code)).decode()
 
 
-def dgemm_query_device_status(stream=None) -> int:
-    """Synchronises the stream and returns (and clears) the sticky device error code."""
-    return int(load().dgemm_query_device_status(_stream(stream)))
+def dgemm_query_device_status(ws=None, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) a status word: the one
+    at the start of workspace ws (errors of the calls given that workspace), or
+    with ws=None the per-device word (calls without a workspace)."""
+    if ws is not None:
+        _require(ws, "ws")
+    return int(load().dgemm_query_device_status(_ptr(ws), _stream(stream)))
+
+
+_OVR_FIELDS = [name for name, _ in Overrides._fields_]
+
+
+def get_overrides() -> dict:
+    """The planner overrides in force (see dgemm_set_overrides in dgemm.h)."""
+    o = Overrides()
+    _check(load().dgemm_get_overrides(ctypes.byref(o)), "dgemm_get_overrides")
+    return {name: getattr(o, name) for name in _OVR_FIELDS}
+
+
+def set_overrides(**fields) -> None:
+    """Sets the planner overrides for later calls: the named fields, every other
+    one at its default (the planner's choice). set_overrides() restores all."""
+    o = Overrides()
+    lib = load()
+    lib.dgemm_overrides_init(ctypes.byref(o))
+    for name, value in fields.items():
+        if name not in _OVR_FIELDS:
+            raise ValueError(f"unknown override {name!r}; known: {_OVR_FIELDS}")
+        setattr(o, name, int(value))
+    _check(lib.dgemm_set_overrides(ctypes.byref(o)), "dgemm_set_overrides")
+
+
+class overrides:
+    """Context manager: ``with overrides(tile_n=128): ...`` sets the named
+    overrides and restores the previous ones on exit."""
+
+    def __init__(self, **fields):
+        self.fields = fields
+        self.saved = None
+
+    def __enter__(self):
+        self.saved = get_overrides()
+        merged = dict(self.saved)
+        merged.update(self.fields)
+        o = Overrides(**{k: int(v) for k, v in merged.items()})
+        _check(load().dgemm_set_overrides(ctypes.byref(o)), "dgemm_set_overrides")
+        return self
+
+    def __exit__(self, *exc):
+        o = Overrides(**{k: int(v) for k, v in self.saved.items()})
+        _check(load().dgemm_set_overrides(ctypes.byref(o)), "dgemm_set_overrides")
+        return False

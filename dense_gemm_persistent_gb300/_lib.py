@@ -29,6 +29,12 @@ class Epilogue(ctypes.Structure):
     _fields_ = [("bias", _vp), ("act", _i32), ("out_quant", _i32), ("out_row_scale", _vp)]
 
 
+class Overrides(ctypes.Structure):
+    _fields_ = [("tile_n", _i32), ("cta_pair", _i32), ("tail_split", _i32), ("tail_halves", _i32),
+                ("cluster_split", _i32), ("seg_first", _i32), ("raster_group", _i32), ("cooperative", _i32),
+                ("wait_limit_ns", _i64), ("stall_after_loads", _i64)]
+
+
 class Plan(ctypes.Structure):
     _fields_ = [("swap_ab", _i32), ("tile_m", _i32), ("tile_n", _i32), ("cta_group", _i32), ("stages", _i32),
                 ("num_tiles", _i32), ("grid", _i32), ("cooperative", _i32), ("raster_group", _i32), ("k_groups", _i32),
@@ -48,11 +54,15 @@ SIGNATURES = {
     "dgemm_plan": (_i32, [_i32, _i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Epilogue), _i32, _i32,
                           ctypes.POINTER(Plan)]),
     "dgemm_status_string": (ctypes.c_char_p, [_i32]),
-    "dgemm_query_device_status": (_i32, [_vp]),
+    "dgemm_query_device_status": (_i32, [_vp, _vp]),
+    "dgemm_overrides_init": (None, [ctypes.POINTER(Overrides)]),
+    "dgemm_set_overrides": (_i32, [ctypes.POINTER(Overrides)]),
+    "dgemm_get_overrides": (_i32, [ctypes.POINTER(Overrides)]),
     "dgemm_fp8_rowquant_noalloc": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, _f32, _f32,
                                           ctypes.POINTER(Epilogue), _vp]),
 }
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+WS_STATUS_BYTES = 256
 
 _lock = threading.Lock()
 _lib = None

@@ -1,5 +1,5 @@
 // api.cu -- the C ABI: argument validation, planning, TMA tensor maps, launch,
-// and the sticky device-side status word. Interface as on the FP8 page
+// the device-side status words, and the planner overrides. Interface as on the FP8 page
 // ("DeepGEMM: FP8 Tensor Core GEMM", bjdmk.com.cn/news/6078902, §5.1): pointers,
 // M/N/K, scale descriptor, a workspace whose size is queried beforehand, and a
 // stream; nothing is allocated per call.
@@ -22,8 +22,10 @@ __device__ unsigned int g_status = 0;  // sticky device-side error bits, one wor
 constexpr int kMaxDevices = 64;
 constexpr int kWeightBlock = 128;       // output channels per weight scale (block-scaled entry)
 constexpr int kWeightBlockShift = 7;
+constexpr size_t kWsStatus = DGEMM_WS_STATUS_BYTES;  // every workspace: the call's status word first
 constexpr size_t kWsHeader = 256;  // requantisation: chunk claim counter + row-band counters
 static_assert(8 + 4 * dg::kMaxBands <= kWsHeader, "row-band counters fit the header");
+static_assert(kWsStatus % 256 == 0 && kWsStatus >= 8, "status header keeps the layout 256-byte aligned");
 constexpr int64_t kMinTailSlices = 48;  // shortest tile (K slices) worth splitting
 
 struct DeviceState {
@@ -33,6 +35,68 @@ struct DeviceState {
     unsigned* status = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
+
+// ---- planner overrides (tuning sweeps, tests): process-wide, defaults = the
+// planner's own choices. The DGEMM_* environment variables are read once, at
+// the first call, and only when DGEMM_ENV_OVERRIDES=1.
+void overrides_defaults(dgemm_overrides_t* o) {
+    o->tile_n = 0;
+    o->cta_pair = -1;
+    o->tail_split = -1;
+    o->tail_halves = -1;
+    o->cluster_split = -1;
+    o->seg_first = -1;
+    o->raster_group = 0;
+    o->cooperative = -1;
+    o->wait_limit_ns = 0;
+    o->stall_after_loads = -1;
+}
+
+std::mutex g_ovr_mutex;
+dgemm_overrides_t g_ovr;                   // guarded by g_ovr_mutex
+std::atomic<bool> g_ovr_set{false};        // g_ovr differs from the defaults
+std::once_flag g_ovr_once;
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    if (v[0] == 'f') return 1;             // "force" (DGEMM_TAIL_SPLIT)
+    return std::atoi(v);
+}
+
+void init_overrides() {
+    dgemm_overrides_t o;
+    overrides_defaults(&o);
+    const char* opt_in = std::getenv("DGEMM_ENV_OVERRIDES");
+    if (opt_in && opt_in[0] == '1') {
+        o.tile_n = env_int("DGEMM_TILE_N", 0);
+        o.cta_pair = env_int("DGEMM_CTA_PAIR", -1);
+        o.tail_split = env_int("DGEMM_TAIL_SPLIT", -1);
+        o.tail_halves = env_int("DGEMM_TAIL_HALVES", -1);
+        o.cluster_split = env_int("DGEMM_CLUSTER_SPLIT", -1);
+        o.seg_first = env_int("DGEMM_SEG_FIRST", -1);
+        o.raster_group = env_int("DGEMM_RASTER_GROUP", 0);
+        o.cooperative = env_int("DGEMM_COOPERATIVE", -1);
+        if (const char* w = std::getenv("DGEMM_WAIT_LIMIT_NS")) o.wait_limit_ns = std::atoll(w);
+    }
+    std::lock_guard<std::mutex> lk(g_ovr_mutex);
+    g_ovr = o;
+    dgemm_overrides_t d;
+    overrides_defaults(&d);
+    g_ovr_set.store(std::memcmp(&o, &d, sizeof o) != 0, std::memory_order_release);
+}
+
+// The overrides in force for one call (the defaults unless some were set).
+dgemm_overrides_t overrides_now() {
+    std::call_once(g_ovr_once, init_overrides);
+    dgemm_overrides_t o;
+    if (!g_ovr_set.load(std::memory_order_acquire)) {
+        overrides_defaults(&o);
+        return o;
+    }
+    std::lock_guard<std::mutex> lk(g_ovr_mutex);
+    return g_ovr;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -86,19 +150,40 @@ int64_t underfill_split(int64_t tiles, int64_t units, int64_t k_blocks) {
 // launch within a process and started from a per-process pseudo-random point,
 // so counter words left in a reused workspace (by any earlier call, or by other
 // data) are not mistaken for this launch's arrivals.
+// Every launch gets one; the workspace status word is tagged with it too.
+constexpr unsigned long long kEpochMask = (1ull << 56) - 1;
 std::atomic<unsigned long long> g_epoch{0};
+unsigned long long g_epoch_first = 0;   // the first epoch this process issues
 std::once_flag g_epoch_once;
 
-unsigned long long next_epoch() {
+void init_epoch() {
     std::call_once(g_epoch_once, []() {
         unsigned long long x = static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count());
         x ^= reinterpret_cast<uintptr_t>(&g_epoch) * 0x9E3779B97F4A7C15ull;
         x ^= x >> 31;
         x *= 0xBF58476D1CE4E5B9ull;
         x ^= x >> 29;
+        g_epoch_first = (x + 1) & kEpochMask;
         g_epoch.store(x, std::memory_order_relaxed);
     });
-    return (g_epoch.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 56) - 1);
+}
+
+unsigned long long next_epoch() {
+    init_epoch();
+    unsigned long long e;
+    do {   // 0 tags a cleared status word: never issued
+        e = (g_epoch.fetch_add(1, std::memory_order_relaxed) + 1) & kEpochMask;
+    } while (e == 0);
+    return e;
+}
+
+// Whether epoch e was issued by this process (so a status word tagged with it
+// was written by one of its launches, not left by other data).
+bool issued_epoch(unsigned long long e) {
+    init_epoch();
+    if (e == 0) return false;
+    const unsigned long long last = g_epoch.load(std::memory_order_relaxed) & kEpochMask;
+    return ((e - g_epoch_first) & kEpochMask) <= ((last - g_epoch_first) & kEpochMask);
 }
 
 struct Plan {
@@ -114,6 +199,7 @@ struct Plan {
     int dp_tiles, split, tail_items;   // tail splitting (MODE_TILE)
     int cluster_split;                 // split K segments of a tile form a cluster of `split` CTAs
     int tail_halves;                   // tail tiles run as two N halves (tail_items = 2 x tail tiles)
+    int seg_first;                     // split K segments run before the whole tiles
     size_t split_offset;               // workspace offset of the split area (after the requant stash)
     size_t tail_count_bytes;           // workspace: per-warp arrival counters
 };
@@ -124,6 +210,7 @@ struct Plan {
 dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layout_t bl, dgemm_dtype_t d_dtype,
                          const dgemm_epilogue_t* epi, int num_sms, int max_pairs, int max_quads, bool allow_split,
                          Plan* out, int k_group = 0) {
+    const dgemm_overrides_t ov = overrides_now();
     if (M < 0 || N < 0 || K < 0 || num_sms <= 0 || k_group < 0) return DGEMM_ERR_INVALID_VALUE;
     if (bl != DGEMM_B_KN && bl != DGEMM_B_NK) return DGEMM_ERR_INVALID_VALUE;
     if (d_dtype != DGEMM_F32 && d_dtype != DGEMM_BF16 && d_dtype != DGEMM_E4M3) return DGEMM_ERR_INVALID_VALUE;
@@ -150,15 +237,12 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.gs = gs;
     p.group_kb = gs ? k_group / p.bk : 0;
     const bool swap = (oq == DGEMM_QUANT_NONE) && M <= 64;
-    const char* pair_env = std::getenv("DGEMM_CTA_PAIR");  // "0" disables, "1" forces CTA pairs (tests, sweeps)
-    const bool pairs_ok = max_pairs > 0 && !(pair_env && pair_env[0] == '0');
-    const char* split_env = std::getenv("DGEMM_TAIL_SPLIT");
-    const bool force_split = split_env && split_env[0] == 'f';
+    const bool pairs_ok = max_pairs > 0 && ov.cta_pair != 0;
+    const bool force_split = ov.tail_split == 1;
     // (the requantising epilogue takes the tail split, not split-K of under-filled grids)
-    const bool split_ok = allow_split && !(split_env && split_env[0] == '0');
-    const char* cl_env = std::getenv("DGEMM_CLUSTER_SPLIT");   // "0": split-K through the workspace only
-    if (cl_env && cl_env[0] == '0') max_quads = 0;
-    const bool cluster_ok = !(cl_env && cl_env[0] == '0');
+    const bool split_ok = allow_split && ov.tail_split != 0;
+    if (ov.cluster_split == 0) max_quads = 0;   // split-K through the workspace only
+    const bool cluster_ok = ov.cluster_split != 0;
     const int64_t kb_all = (K + (128 / static_cast<int64_t>(esz)) - 1) / (128 / static_cast<int64_t>(esz));
     int bn;
     int pair = 0;
@@ -207,17 +291,17 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
             }
         }
     }
-    // DGEMM_TILE_N overrides the tile width when such a variant exists (used to
-    // exercise every variant in tests and for tuning sweeps).
-    if (const char* f = std::getenv("DGEMM_TILE_N")) {
-        const int v = std::atoi(f);
+    // The tile width override applies when such a variant exists (tests reach
+    // every variant with it; tuning sweeps).
+    if (ov.tile_n > 0) {
+        const int v = ov.tile_n;
         if (v != bn && find_kernel(v, fp8, p.a_mn, p.b_mn, p.mode, 0, gs) >= 0) {
             bn = v;
             pair = 0;
         }
     }
-    // DGEMM_CTA_PAIR=1 forces the CTA-pair variant when one exists for this tile.
-    if (pair_env && pair_env[0] == '1' && !swap && M > 128 && max_pairs > 0 &&
+    // cta_pair = 1 forces the CTA-pair variant when one exists for this tile.
+    if (ov.cta_pair == 1 && !swap && M > 128 && max_pairs > 0 &&
         find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, 1, gs) >= 0)
         pair = 1;
     p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair, gs);
@@ -234,19 +318,8 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.num_tiles = static_cast<int>(tiles_m * tiles_n);
     const int units = pair ? max_pairs : num_sms;
     p.pub.grid = (pair ? 2 : 1) * static_cast<int>(p.pub.num_tiles < units ? p.pub.num_tiles : units);
-    // The requantising kernel's last waits (for the row bands other CTAs are
-    // still finishing) need every CTA resident: it is launched cooperatively
-    // (the grid is sized from the measured occupancy too). DGEMM_COOPERATIVE=0
-    // drops the attribute, because Nsight Compute cannot launch cooperative
-    // cluster grids; on an otherwise idle GPU the grid is still co-resident,
-    // and the waits are bounded regardless.
-    const char* coop_env = std::getenv("DGEMM_COOPERATIVE");
-    p.pub.cooperative = (p.mode == dg::MODE_ROWQ && !(coop_env && coop_env[0] == '0')) ? 1 : 0;
     p.pub.raster_group = static_cast<int>(tiles_m < 8 ? (tiles_m > 0 ? tiles_m : 1) : 8);
-    if (const char* g = std::getenv("DGEMM_RASTER_GROUP")) {   // tuning sweeps: tile rows per band
-        const int v = std::atoi(g);
-        if (v >= 1 && v <= tiles_m) p.pub.raster_group = v;
-    }
+    if (ov.raster_group >= 1 && ov.raster_group <= tiles_m) p.pub.raster_group = ov.raster_group;
     p.pub.smem_bytes = static_cast<size_t>(k->smem_bytes);
 
     // Tail splitting: when the tiles do not fill the last wave, run the full
@@ -262,14 +335,18 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.split = 1;
     p.tail_items = 0;
     p.tail_count_bytes = 0;
+    // workspace: status header, per-warp arrival counters, one FP32 partial
+    // tile per unit
+    size_t split_bytes = 0;
     auto use_split = [&](int dp_tiles, int split, int items) {
         p.dp_tiles = dp_tiles;
         p.split = split;
         p.tail_items = items;
         p.pub.grid = pair_ctas(pair) * (items > units ? units : (dp_tiles > 0 ? units : items));
         p.tail_count_bytes = round_up(static_cast<size_t>(units) * pair_ctas(pair) * k->epi_warps * 8, 256);
-        p.pub.workspace_bytes =
-            p.tail_count_bytes + static_cast<size_t>(units) * pair_ctas(pair) * 128 * static_cast<size_t>(bn) * 4;
+        split_bytes = p.tail_count_bytes + static_cast<size_t>(units) * pair_ctas(pair) * 128 * static_cast<size_t>(bn) * 4;
+        p.split_offset = kWsStatus;
+        p.pub.workspace_bytes = kWsStatus + split_bytes;
     };
     // Split-K when the tiles do not fill one wave (decode shapes, small M x N
     // with long K): every tile is split into K segments run on the idle units.
@@ -307,9 +384,8 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         // split (half of both) finishes the wave sooner despite its reduction:
         // 4096^3 BF16 ran at 1654 TFLOP/s split along K, 1590 in halves;
         // FP8 4096 x 11008 x 4096 (too short to split) at 3197 in halves,
-        // 3165 with whole tiles. DGEMM_TAIL_HALVES=0 disables it.
-        const char* halves_env = std::getenv("DGEMM_TAIL_HALVES");
-        if (p.split == 1 && rem > 0 && k->halves && 2 * rem <= units && !(halves_env && halves_env[0] == '0')) {
+        // 3165 with whole tiles. The tail_halves = 0 override disables it.
+        if (p.split == 1 && rem > 0 && k->halves && 2 * rem <= units && ov.tail_halves != 0) {
             p.tail_halves = 1;
             p.dp_tiles = p.pub.num_tiles - rem;
             p.tail_items = 2 * rem;
@@ -336,18 +412,40 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.tail_split = p.split;
     p.pub.cluster_split = p.cluster_split;
     p.pub.tail_halves = p.tail_halves;
-    // Requantisation: barrier header, row maxima, BF16 stash, then (tail split)
-    // the split area.
-    p.split_offset = 0;
+    // Requantisation: status header, barrier header, row maxima, BF16 stash,
+    // then (tail split) the split area.
     if (oq) {
-        const size_t base = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
+        const size_t base =
+            kWsStatus + kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
         if (p.split > 1) {
             p.split_offset = round_up(base, 256);
-            p.pub.workspace_bytes += p.split_offset;
+            p.pub.workspace_bytes = p.split_offset + split_bytes;
         } else {
             p.pub.workspace_bytes = base;
         }
     }
+    // Cross-CTA waits. The requantising kernel's last waits (for the row bands
+    // other CTAs are still finishing) need every CTA resident: it is launched
+    // cooperatively (the grid is sized from the measured occupancy too). Split
+    // tiles that exchange partial sums through the workspace either run in a
+    // cooperative launch, where every segment waits for all (under-filled
+    // grids: the exchange ends the kernel, so its shortest form pays), or in a
+    // plain launch, where no segment waits for one that may not have started
+    // (the last to arrive finishes the tile: the tail split, whose exchange
+    // overlaps whole tiles and which keeps programmatic dependent launch).
+    // The cooperative = 0 override drops the attribute (profilers that cannot
+    // launch cooperative cluster grids); the requantising form's band waits
+    // then rely on an otherwise idle GPU, and every wait stays bounded.
+    const bool ws_exchange = p.split > 1 && !p.cluster_split;
+    int coop = (p.mode == dg::MODE_ROWQ || (ws_exchange && p.dp_tiles == 0)) ? 1 : 0;
+    if (ov.cooperative == 0) coop = 0;
+    if (ov.cooperative == 1 && ws_exchange) coop = 1;
+    p.pub.cooperative = coop;
+    // The K segments of split tiles run first in the plain tile form, as the
+    // raster's first tiles, so their exchange of partial sums overlaps whole
+    // tiles (+5 % at 4096^3 BF16); the requantising form keeps them last (its
+    // row bands count the split tiles at the end of the raster).
+    p.seg_first = (p.mode == dg::MODE_TILE && ov.seg_first != 0) ? 1 : 0;
     *out = p;
     return DGEMM_OK;
 }
@@ -463,10 +561,14 @@ CUtensorMapDataType tm_type(dgemm_dtype_t t) {
                           : t == DGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
 }
 
+// status_in_ws: device-side errors of the call go to the status word at the
+// start of ws (when ws holds at least kWsStatus bytes) instead of the
+// per-device word.
 dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, const float* a_scale,
                    const float* b_scale, const void* C, dgemm_dtype_t c_dtype, void* D, dgemm_dtype_t d_dtype,
                    int64_t M, int64_t N, int64_t K, float alpha, float beta, const dgemm_epilogue_t* epi, void* ws,
-                   size_t ws_bytes, cudaStream_t stream, int k_group = 0, int b_block = 1) {
+                   size_t ws_bytes, cudaStream_t stream, int k_group = 0, int b_block = 1,
+                   bool status_in_ws = true) {
     // ---- arguments that need no device
     if (b_block != 1 && (b_block != kWeightBlock || k_group <= 0)) return DGEMM_ERR_INVALID_VALUE;
     Plan plan;
@@ -547,7 +649,8 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
         if (!encode_2d(&tmD, tm_type(d_dtype), D, N, M, N * dsz, static_cast<uint32_t>(128 / dsz), 32))
             return DGEMM_ERR_CUDA;
     } else if (plan.mode == dg::MODE_ROWQ) {
-        if (!encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wsb + kWsHeader + amax_bytes, N, M, N * 2, 64, 32))
+        if (!encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wsb + kWsStatus + kWsHeader + amax_bytes, N, M, N * 2,
+                       64, 32))
             return DGEMM_ERR_CUDA;
     }
 
@@ -589,34 +692,35 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     }
     p.bias = bias;
     p.act = epi ? epi->act : 0;
+    const dgemm_overrides_t ov = overrides_now();
     p.status = dev->status;
+    p.epoch = next_epoch();
+    p.ws_status = (status_in_ws && ws && ws_bytes >= kWsStatus) ? static_cast<unsigned long long*>(ws) : nullptr;
+    p.wait_ns = ov.wait_limit_ns > 0 ? static_cast<uint64_t>(ov.wait_limit_ns) : dg::kWaitLimitNs;
+    p.stall_after = ov.stall_after_loads;
     p.dp_tiles = plan.dp_tiles;
     p.split = plan.split;
     p.tail_items = plan.tail_items;
-    // The K segments of split tiles run first in the plain tile form, as the
-    // raster's first tiles, so their exchange of partial sums overlaps whole
-    // tiles (+5 % at 4096^3 BF16); the requantising form keeps them last (its
-    // row bands count the split tiles at the end of the raster).
-    // DGEMM_SEG_FIRST=0 keeps them last everywhere (comparisons).
-    const char* sf_env = std::getenv("DGEMM_SEG_FIRST");
-    p.seg_first = (plan.mode == dg::MODE_TILE && !(sf_env && sf_env[0] == '0')) ? 1 : 0;
+    p.seg_first = plan.seg_first;
+    p.split_sym = plan.pub.cooperative;
     if (plan.split > 1) {
         p.tail_count = reinterpret_cast<unsigned long long*>(wsb + plan.split_offset);
         p.partials = reinterpret_cast<float*>(wsb + plan.split_offset + plan.tail_count_bytes);
-        p.epoch = next_epoch();
     }
     if (plan.mode == dg::MODE_ROWQ) {
-        // header: the chunk claim counter, then one arrival counter per row band
-        // (a band of rq_gpc raster groups, so that at most kMaxBands of them)
-        p.rq_next = reinterpret_cast<unsigned long long*>(wsb);
-        p.band_count = reinterpret_cast<unsigned*>(wsb + 8);
+        // after the status header: the chunk claim counter, then one arrival
+        // counter per row band (a band of rq_gpc raster groups, so that at
+        // most kMaxBands of them)
+        uint8_t* hdr = wsb + kWsStatus;
+        p.rq_next = reinterpret_cast<unsigned long long*>(hdr);
+        p.band_count = reinterpret_cast<unsigned*>(hdr + 8);
         const int64_t groups = (p.tiles_m + p.group_m - 1) / p.group_m;
         p.rq_gpc = static_cast<int>(groups > 0 ? (groups + dg::kMaxBands - 1) / dg::kMaxBands : 1);
-        p.amax = reinterpret_cast<unsigned*>(wsb + kWsHeader);
-        p.stash = reinterpret_cast<const uint16_t*>(wsb + kWsHeader + amax_bytes);
+        p.amax = reinterpret_cast<unsigned*>(hdr + kWsHeader);
+        p.stash = reinterpret_cast<const uint16_t*>(hdr + kWsHeader + amax_bytes);
         p.q_out = static_cast<uint8_t*>(D);
         p.out_row_scale = epi->out_row_scale;
-        if (cudaMemsetAsync(ws, 0, kWsHeader + amax_bytes, stream) != cudaSuccess) return DGEMM_ERR_CUDA;
+        if (cudaMemsetAsync(hdr, 0, kWsHeader + amax_bytes, stream) != cudaSuccess) return DGEMM_ERR_CUDA;
     }
     p.cluster_split = plan.cluster_split;
     p.tail_halves = plan.tail_halves;
@@ -719,18 +823,60 @@ const char* dgemm_status_string(dgemm_status_t s) {
     return "unknown status";
 }
 
-dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream) {
+dgemm_status_t dgemm_query_device_status(const void* ws, dgemm_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DGEMM_ERR_CUDA;
     DeviceState* dev = nullptr;
     int devid = 0;
     const dgemm_status_t st = device_state(&dev, &devid);
     if (st != DGEMM_OK) return st;
+    if (ws != nullptr) {
+        // the workspace's status word: errors of calls that used this workspace,
+        // tagged with their launch epoch (any other content reads as no error)
+        if (!aligned16(ws)) return DGEMM_ERR_MISALIGNED;
+        unsigned long long w = 0;
+        if (cudaMemcpy(&w, ws, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess) return DGEMM_ERR_CUDA;
+        if ((w & 0xFFull) == 0 || !issued_epoch(w >> 8)) return DGEMM_OK;
+        const unsigned long long zero = 0;
+        if (cudaMemcpy(const_cast<void*>(ws), &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return DGEMM_ERR_CUDA;
+        return DGEMM_ERR_DEVICE_TIMEOUT;
+    }
     unsigned v = 0;
     if (cudaMemcpyFromSymbol(&v, g_status, sizeof v) != cudaSuccess) return DGEMM_ERR_CUDA;
     if (v == 0) return DGEMM_OK;
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) return DGEMM_ERR_CUDA;
     return DGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+void dgemm_overrides_init(dgemm_overrides_t* o) {
+    if (o) overrides_defaults(o);
+}
+
+dgemm_status_t dgemm_set_overrides(const dgemm_overrides_t* o) {
+    std::call_once(g_ovr_once, init_overrides);
+    dgemm_overrides_t v;
+    overrides_defaults(&v);
+    if (o) {
+        if (o->tile_n < 0 || o->cta_pair < -1 || o->cta_pair > 1 || o->tail_split < -1 || o->tail_split > 1 ||
+            o->tail_halves < -1 || o->tail_halves > 0 || o->cluster_split < -1 || o->cluster_split > 0 ||
+            o->seg_first < -1 || o->seg_first > 1 || o->raster_group < 0 || o->cooperative < -1 ||
+            o->cooperative > 1 || o->wait_limit_ns < 0 || o->stall_after_loads < -1)
+            return DGEMM_ERR_INVALID_VALUE;
+        v = *o;
+    }
+    dgemm_overrides_t d;
+    overrides_defaults(&d);
+    std::lock_guard<std::mutex> lk(g_ovr_mutex);
+    g_ovr = v;
+    g_ovr_set.store(std::memcmp(&v, &d, sizeof v) != 0, std::memory_order_release);
+    return DGEMM_OK;
+}
+
+dgemm_status_t dgemm_get_overrides(dgemm_overrides_t* o) {
+    if (!o) return DGEMM_ERR_INVALID_VALUE;
+    *o = overrides_now();
+    return DGEMM_OK;
 }
 
 }  // extern "C"
@@ -764,7 +910,8 @@ extern "C" dgemm_status_t dgemm_fp8_rowquant_noalloc(const void* Aq, const void*
     if (M < 0 || N < 0 || K < 0) return DGEMM_ERR_INVALID_VALUE;
     // the requantising scratch without a split area (with too little room for
     // one, run() keeps whole tiles)
-    const size_t need = kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
+    const size_t need =
+        kWsStatus + kWsHeader + round_up(static_cast<size_t>(M) * 4, 256) + static_cast<size_t>(M) * N * 2;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || need > DGEMM_NOALLOC_SCRATCH_BYTES)
         return DGEMM_ERR_WORKSPACE_TOO_SMALL;
     DeviceState* dev = nullptr;
@@ -776,6 +923,7 @@ extern "C" dgemm_status_t dgemm_fp8_rowquant_noalloc(const void* Aq, const void*
         s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch);
     });
     if (s.err != cudaSuccess || s.ptr == nullptr) return DGEMM_ERR_CUDA;
+    // (device-side errors go to the per-device word: the caller cannot name the array)
     return run(1, Aq, Bq, b_layout, a_scale, b_scale, C, c_dtype, Dq, DGEMM_E4M3, M, N, K, alpha, beta, epi, s.ptr,
-               DGEMM_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
+               DGEMM_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream), 0, 1, false);
 }

@@ -60,6 +60,7 @@ enum ErrBits : unsigned {
     ERR_TIMEOUT_EPILOGUE = 4u,
     ERR_TIMEOUT_ROW_BAND = 8u,
     ERR_TIMEOUT_DRAIN = 16u,
+    ERR_ARRIVAL = 32u,   // a split tile's arrival counter could not be updated
 };
 
 struct Params {
@@ -101,7 +102,16 @@ struct Params {
     const uint16_t* stash;   // [M,N] BF16 y values (what tmD writes)
     uint8_t* q_out;          // [M,N] E4M3 codes
     float* out_row_scale;    // [M]
-    unsigned* status;        // sticky device error word
+    unsigned* status;        // sticky device error word (calls without a workspace status word)
+    // The call's status word in the caller's workspace, or null: (epoch << 8) |
+    // error bits, tagged with this launch's epoch so that a word left by an
+    // earlier launch (or any other data) is replaced instead of merged.
+    unsigned long long* ws_status;
+    uint64_t wait_ns;        // limit of every bounded device-side wait
+    // Testing of the bounded waits: < 0 off; otherwise the TMA producer of
+    // every CTA stops after issuing this many stage loads, so that the MMA's
+    // wait for the next stage runs out and the kernel drains and returns.
+    long long stall_after;
     // Split tiles (all modes): tiles [0, dp_tiles) run whole; each of the
     // remaining tiles is split along K into `split` segments (tail_items in
     // all), every unit taking at most one (before its whole tiles, if any;
@@ -124,8 +134,17 @@ struct Params {
     // the tiles from dp_tiles on is run as two 256 x 128 halves (tail_items =
     // 2 x those tiles), each a whole K range with an N = 128 MMA; no partials.
     int tail_halves;
-    unsigned long long* tail_count;  // [split tile][CTAS][EPI_WARPS]: (epoch << 8) | arrivals
+    // [split tile][CTAS][EPI_WARPS]: (epoch << 8) | (parked << 4) | arrivals
+    unsigned long long* tail_count;
     unsigned long long epoch;        // unique per launch (56 bits): stale counters need no clearing
+    // Exchange of a split tile's partial sums through the workspace.
+    // 1 (the launch is cooperative, so every segment is resident): every
+    //   segment parks the units others own, waits for all, and finishes its own.
+    // 0 (no residency guarantee): no segment waits for one that may not have
+    //   started. A segment counts its arrival first; all but the last to arrive
+    //   park every unit and leave, and the last waits only for those (already
+    //   running) segments' parking, then finishes every unit.
+    int split_sym;
 };
 
 // One unit of work: a whole tile (item < 0) or one K segment of a split tile.
@@ -328,8 +347,25 @@ __device__ __forceinline__ void activation32(float (&v)[32], int act) {
     }
 }
 
+// Records error bits: in the call's workspace status word when it has one
+// (tagged with the launch epoch), else in the per-device word.
+__device__ __forceinline__ void record_error(const Params& p, unsigned bit) {
+    if (p.ws_status != nullptr) {
+        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(p.ws_status);
+        for (int tries = 0; tries < 4096; ++tries) {
+            const bool mine = (old >> 8) == p.epoch;
+            if (mine && (old & bit) == bit) return;
+            const unsigned long long next = mine ? (old | bit) : ((p.epoch << 8) | bit);
+            const unsigned long long seen = atomicCAS(p.ws_status, old, next);
+            if (seen == old) return;
+            old = seen;
+        }
+    }
+    atomicOr(p.status, bit);   // no workspace word (or it could not be updated)
+}
+
 __device__ __forceinline__ void raise_error(const Params& p, unsigned bit, volatile int* abort) {
-    atomicOr(p.status, bit);
+    record_error(p, bit);
     *abort = 1;
 }
 
@@ -610,9 +646,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 const uint64_t pol = policy_evict_last();
                 uint32_t stage = 0, phase = 0;
                 int64_t issued = 0;
-                bool ok = true;
+                bool ok = true, stalled = false;
                 Work w;
-                for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it) {
+                for (int it = 0; ok && !stalled && next_work(p, unit0, units, it, w); ++it) {
                     int mb, nb;
                     tile_coords(w.tile, p, mb, nb);
                     const int row0 = mb * CF::TILE_M + static_cast<int>(rank) * CF::BM;   // this CTA's A rows
@@ -621,7 +657,11 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     const int col0 = half ? nb * CF::BN + w.half * (CF::BN / 2) + static_cast<int>(rank) * (CF::BN_CTA / 2)
                                           : nb * CF::BN + static_cast<int>(rank) * CF::BN_CTA;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                        if (issued == p.stall_after) {   // testing the bounded waits: stop here
+                            stalled = true;
+                            break;
+                        }
+                        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -679,7 +719,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 for (int s = 0; s < S; ++s) {
                     const int64_t cnt = issued > s ? (issued - s + S - 1) / S : 0;
                     uint64_t* bar = (CF::PAIR && rank != 0) ? &empty[s] : &full[s];
-                    if (cnt > 0 && !mbar_wait(bar, static_cast<uint32_t>((cnt - 1) & 1), nullptr))
+                    if (cnt > 0 && !mbar_wait(bar, static_cast<uint32_t>((cnt - 1) & 1), nullptr, p.wait_ns))
                         raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
                 }
             }
@@ -743,14 +783,14 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             const bool first = (kb == w.kb0) || kin == 0;
                             if (first) {
                                 gb = gcount & 1;
-                                if (!mbar_wait(&acc_empty[gb], ((gcount >> 1) & 1) ^ 1, abort_flag)) {
+                                if (!mbar_wait(&acc_empty[gb], ((gcount >> 1) & 1) ^ 1, abort_flag, p.wait_ns)) {
                                     ok = false;
                                     break;
                                 }
                                 tc_fence_after();
                                 d_tmem = tmem_base + static_cast<uint32_t>(gb * p.acc_stride);
                             }
-                            if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                            if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
                                 ok = false;
                                 break;
                             }
@@ -775,7 +815,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 for (int it = 0; ok && next_work(p, unit0, units, it, w); ++it, ++local) {
                     const int buf = local & 1;
                     const uint32_t acc_phase = (local >> 1) & 1;
-                    if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, abort_flag)) {
+                    if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -792,7 +832,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     // a tail half is one MMA of half the width
                     const uint32_t idesc_item = (CF::HALVES && w.half >= 0) ? CF::IDESC_HALF : CF::IDESC;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -823,7 +863,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     mma_commit_pair(drain, 1);
                 else
                     mma_commit(drain);
-                if (!mbar_wait(drain, 0, nullptr)) raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
+                if (!mbar_wait(drain, 0, nullptr, p.wait_ns)) raise_error(p, ERR_TIMEOUT_DRAIN, abort_flag);
             }
             __syncwarp();
         } else if (CF::GS_SMEM && warp == 2) {
@@ -846,7 +886,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 for (int j = j0; j < j1; ++j, ++gcount) {
                     const int slot = gcount % (CF::SC_SLOTS > 0 ? CF::SC_SLOTS : 1);
                     const uint32_t ph = static_cast<uint32_t>(gcount / (CF::SC_SLOTS > 0 ? CF::SC_SLOTS : 1)) & 1u;
-                    if (!mbar_wait(&sc_empty[slot], ph ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&sc_empty[slot], ph ^ 1u, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -1013,7 +1053,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             if constexpr (CF::MODE != MODE_SWAP && !CF::GS) load_cols();
             if constexpr (!CF::GS) {
                 const uint32_t acc_phase = (local >> 1) & 1;
-                if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag)) {
+                if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -1061,7 +1101,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         float rsj;
                         if constexpr (CF::GS_SMEM) {
                             const uint32_t ph = static_cast<uint32_t>(gcount / CF::SC_SLOTS) & 1u;
-                            if (!mbar_wait(&sc_full[slot], ph, abort_flag)) {
+                            if (!mbar_wait(&sc_full[slot], ph, abort_flag, p.wait_ns)) {
                                 ok = false;
                                 break;
                             }
@@ -1072,7 +1112,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             csj = p.col_gscale + j * p.gs_ld_col;
                             rsj = rs_cur;
                         }
-                        if (!mbar_wait(&acc_full[gb], (gcount >> 1) & 1, abort_flag)) {
+                        if (!mbar_wait(&acc_full[gb], (gcount >> 1) & 1, abort_flag, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -1238,54 +1278,59 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 
             // A split tile is finished by all of its K segments together: unit u
             // (32 columns) of this warp's region belongs to segment u % split.
-            // Each segment parks the units other segments own as FP32 partials,
+            // When every segment is resident (a cluster, or a cooperative
+            // launch), each parks the units other segments own as FP32 partials,
             // counts its arrival, waits until every segment has arrived, then
             // adds the others' partials of its own units to its accumulator and
             // stores them directly: about one round trip through L2 per segment
             // instead of a single warp reading every partial unit by unit.
+            // Otherwise the last segment to arrive finishes the region (below).
             const int item0 = part ? (w.item / p.split) * p.split : 0;
             const int seg = part ? w.item - item0 : 0;
             auto owner = [&](int u) { return u % p.split; };
             // generic writes to buffers the TMA (async proxy) filled
             if (part && p.cluster_split) fence_proxy_async_smem();
+            const bool unit_pass = !part || p.cluster_split || p.split_sym;
+            if (unit_pass) {
 #pragma unroll U_UNROLL
-            for (int u = 0; u < nunits; ++u) {
-                float v[32];
-                load_acc(u, v);
-                if (part && owner(u) != seg) {
-                    // a unit another segment finishes: park the raw FP32
-                    // accumulator; each warp-wide store writes 512 contiguous bytes
-                    if (p.cluster_split) {
-                        // into this CTA's idle pipeline buffers (every stage has been
-                        // consumed: this is the unit's last item), for the peers
-                        float4* dst = reinterpret_cast<float4*>(stages) + (ew * NUNITS + u) * (UNIT_F4 * 32) + lane;
+                for (int u = 0; u < nunits; ++u) {
+                    float v[32];
+                    load_acc(u, v);
+                    if (part && owner(u) != seg) {
+                        // a unit another segment finishes: park the raw FP32
+                        // accumulator; each warp-wide store writes 512 contiguous bytes
+                        if (p.cluster_split) {
+                            // into this CTA's idle pipeline buffers (every stage has been
+                            // consumed: this is the unit's last item), for the peers
+                            float4* dst = reinterpret_cast<float4*>(stages) + (ew * NUNITS + u) * (UNIT_F4 * 32) + lane;
 #pragma unroll
-                        for (int j = 0; j < UNIT_F4; ++j)
-                            dst[32 * j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(p.partials) + w.item * ITEM_F4 +
-                                      ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
-                                          (UNIT_F4 * 32) +
-                                      lane;
+                            for (int j = 0; j < UNIT_F4; ++j)
+                                dst[32 * j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(p.partials) + w.item * ITEM_F4 +
+                                          ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
+                                              (UNIT_F4 * 32) +
+                                          lane;
 #pragma unroll
-                        for (int j = 0; j < UNIT_F4; ++j)
-                            __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                            for (int j = 0; j < UNIT_F4; ++j)
+                                __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                        }
                     }
-                }
-                if (!CF::GS && u == nunits - 1 && !part) {
-                    // Last read of this accumulator: hand it back to the MMA warp
-                    // (a K segment's, after its units are finished: it reads its own
-                    // units again then).
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (CF::PAIR && rank != 0)
-                            mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
-                        else
-                            mbar_arrive(&acc_empty[buf]);
+                    if (!CF::GS && u == nunits - 1 && !part) {
+                        // Last read of this accumulator: hand it back to the MMA warp
+                        // (a K segment's, after its units are finished: it reads its own
+                        // units again then).
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (CF::PAIR && rank != 0)
+                                mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
+                            else
+                                mbar_arrive(&acc_empty[buf]);
+                        }
                     }
+                    if (!part) finish(u, v, false);
                 }
-                if (!part) finish(u, v, false);
             }
             if constexpr (CF::MODE == MODE_ROWQ) {
                 if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
@@ -1332,81 +1377,152 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             }
             {
                 if (part && !p.cluster_split) {
-                    // Count this warp's region of the segment in, then (if this
-                    // segment owns boxes of the region) wait for all segments.
-                    // The counter word holds (launch epoch << 8) | arrivals; a word
-                    // left by any earlier launch counts as zero arrivals. Every
-                    // segment of a tile runs at once (each unit takes at most one
-                    // split item, before its whole tiles, and the grid is
-                    // resident), and the wait is bounded regardless.
-                    __threadfence();   // this lane's partial stores before the count
-                    __syncwarp();
-                    const bool owns = seg < NUNITS;
-                    unsigned ready = 0;
-                    if (lane == 0) {
-                        unsigned long long* cnt =
-                            p.tail_count + ((w.item / p.split) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
-                        __threadfence();
-                        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), next = 0;
+                    // The split tile's counter word for this warp's region:
+                    // (launch epoch << 8) | (segments parked << 4) | arrivals; a word
+                    // left by any earlier launch counts as zero of each.
+                    unsigned long long* cnt =
+                        p.tail_count + ((w.item / p.split) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
+                    // lane 0: counts this segment in; returns how many had arrived
+                    // before it, or -1 if the word could not be updated.
+                    auto arrive = [&]() -> int {
+                        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt);
                         for (int tries = 0; tries < 4096; ++tries) {
-                            next = ((old >> 8) == p.epoch) ? old + 1 : ((p.epoch << 8) | 1ull);
+                            const bool cur = (old >> 8) == p.epoch;
+                            const unsigned long long next = cur ? old + 1 : ((p.epoch << 8) | 1ull);
                             const unsigned long long seen = atomicCAS(cnt, old, next);
-                            if (seen == old) break;
+                            if (seen == old) return cur ? static_cast<int>(old & 0xFull) : 0;
                             old = seen;
                         }
-                        if (owns) {
-                            const unsigned long long want = (p.epoch << 8) | static_cast<unsigned long long>(p.split);
-                            unsigned long long seen = next;
-                            const uint64_t t0 = globaltimer();
-                            while (seen != want) {
-                                if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) break;
-                                __nanosleep(32);
-                                asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(seen) : "l"(cnt) : "memory");
-                            }
-                            ready = seen == want ? 1u : 0u;
-                            __threadfence();
+                        return -1;
+                    };
+                    // lane 0: bounded wait until the word satisfies done(word)
+                    auto await = [&](auto done) -> unsigned {
+                        unsigned long long seen = ld_acquire_u64(cnt);
+                        const uint64_t t0 = globaltimer();
+                        while (!done(seen)) {
+                            if (*abort_flag || globaltimer() - t0 > p.wait_ns) return 0u;
+                            __nanosleep(32);
+                            seen = ld_acquire_u64(cnt);
                         }
-                    }
-                    if (owns) {
+                        return 1u;
+                    };
+                    // v += the other segments' partials of unit u, all loads in flight together
+                    auto add_partials = [&](int u, float (&v)[32]) {
+                        const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
+                                            ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
+                                                (UNIT_F4 * 32) +
+                                            lane;
+                        float4 f[3][UNIT_F4];
+#pragma unroll
+                        for (int o = 0; o < 3; ++o) {
+                            const int sgi = o + (o >= seg ? 1 : 0);
+#pragma unroll
+                            for (int j = 0; j < UNIT_F4; ++j)
+                                f[o][j] = sgi < p.split ? __ldcg(src + sgi * ITEM_F4 + 32 * j)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int o = 0; o < 3; ++o)
+#pragma unroll
+                            for (int j = 0; j < UNIT_F4; ++j) {
+                                v[4 * j] += f[o][j].x;
+                                v[4 * j + 1] += f[o][j].y;
+                                v[4 * j + 2] += f[o][j].z;
+                                v[4 * j + 3] += f[o][j].w;
+                            }
+                    };
+                    if (p.split_sym) {
+                        // Every segment of the tile is resident (cooperative launch):
+                        // count this warp's parked units in, then (if this segment
+                        // owns units of the region) wait for all segments and finish
+                        // them: own accumulator from Tensor Memory (handed back to
+                        // the MMA only after this), the others from the workspace.
+                        __threadfence();   // this lane's partial stores before the count
+                        __syncwarp();
+                        const bool owns = seg < NUNITS;
+                        unsigned ready = 0;
+                        if (lane == 0) {
+                            __threadfence();
+                            const int before = arrive();
+                            if (before < 0) {
+                                record_error(p, ERR_ARRIVAL);
+                            } else if (owns) {
+                                const unsigned long long want = (p.epoch << 8) | static_cast<unsigned long long>(p.split);
+                                ready = await([&](unsigned long long x) { return x == want; });
+                                __threadfence();
+                            } else {
+                                ready = 1u;
+                            }
+                        }
                         ready = __shfl_sync(0xffffffffu, ready, 0);
                         __threadfence();   // the other segments' partials after their count
                         if (!ready) {
                             ok = false;
-                        } else {
-                            // Own segment from Tensor Memory (handed back to the MMA
-                            // only after this), the others from the workspace, all
-                            // their loads in flight together.
+                        } else if (owns) {
 #pragma unroll U_UNROLL
                             for (int u = 0; u < NUNITS; ++u) {
                                 if (owner(u) != seg) continue;
                                 float v[32];
                                 load_acc(u, v);
-                                const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
-                                                    ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
-                                                        (UNIT_F4 * 32) +
-                                                    lane;
-                                float4 f[3][UNIT_F4];
-#pragma unroll
-                                for (int o = 0; o < 3; ++o) {
-                                    const int sgi = o + (o >= seg ? 1 : 0);
-#pragma unroll
-                                    for (int j = 0; j < UNIT_F4; ++j)
-                                        f[o][j] = sgi < p.split ? __ldcg(src + sgi * ITEM_F4 + 32 * j)
-                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                                }
-#pragma unroll
-                                for (int o = 0; o < 3; ++o)
-#pragma unroll
-                                    for (int j = 0; j < UNIT_F4; ++j) {
-                                        v[4 * j] += f[o][j].x;
-                                        v[4 * j + 1] += f[o][j].y;
-                                        v[4 * j + 2] += f[o][j].z;
-                                        v[4 * j + 3] += f[o][j].w;
-                                    }
+                                add_partials(u, v);
                                 finish(u, v, true);
                             }
                             if constexpr (CF::MODE == MODE_ROWQ) {   // the row maxima of the units finished here
                                 if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
+                            }
+                        }
+                    } else {
+                        // No residency guarantee: never wait for a segment that may
+                        // not have started. Arrive first; all but the last arrival
+                        // park every unit and leave; the last waits only for the
+                        // earlier arrivals (running, and waiting on nothing) to
+                        // finish parking, then finishes every unit of the region.
+                        int before = 0;
+                        if (lane == 0) before = arrive();
+                        before = __shfl_sync(0xffffffffu, before, 0);
+                        if (before < 0) {
+                            if (lane == 0) record_error(p, ERR_ARRIVAL);
+                            ok = false;
+                        } else if (before < p.split - 1) {
+#pragma unroll U_UNROLL
+                            for (int u = 0; u < NUNITS; ++u) {
+                                float v[32];
+                                load_acc(u, v);
+                                float4* dst = reinterpret_cast<float4*>(p.partials) + w.item * ITEM_F4 +
+                                              ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
+                                                  (UNIT_F4 * 32) +
+                                              lane;
+#pragma unroll
+                                for (int j = 0; j < UNIT_F4; ++j)
+                                    __stcg(dst + 32 * j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                            }
+                            __threadfence();   // this lane's partial stores before the count
+                            __syncwarp();
+                            if (lane == 0) red_release_add_u64(cnt, 1ull << 4);
+                        } else {
+                            unsigned ready = 0;
+                            if (lane == 0) {
+                                const unsigned long long want = static_cast<unsigned long long>(p.split - 1);
+                                ready = await([&](unsigned long long x) {
+                                    return (x >> 8) == p.epoch && ((x >> 4) & 0xFull) == want;
+                                });
+                                __threadfence();
+                            }
+                            ready = __shfl_sync(0xffffffffu, ready, 0);
+                            __threadfence();   // the other segments' partials after their count
+                            if (!ready) {
+                                ok = false;
+                            } else {
+#pragma unroll U_UNROLL
+                                for (int u = 0; u < NUNITS; ++u) {
+                                    float v[32];
+                                    load_acc(u, v);
+                                    add_partials(u, v);
+                                    finish(u, v, true);
+                                }
+                                if constexpr (CF::MODE == MODE_ROWQ) {
+                                    if (row < p.M) atomicMax(&p.amax[row], __float_as_uint(rowmax));
+                                }
                             }
                         }
                     }
@@ -1458,7 +1574,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     const unsigned want = band_expected<CF>(p, b);
                     const uint64_t t0 = globaltimer();
                     while (ld_acquire_u32(p.band_count + b) < want) {
-                        if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
+                        if (*abort_flag || globaltimer() - t0 > p.wait_ns) {
                             ready = 0;
                             break;
                         }

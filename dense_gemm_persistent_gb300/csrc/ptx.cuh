@@ -9,8 +9,9 @@
 
 namespace dg {
 
-// Wall-clock limit of every device-side wait, in nanoseconds (~1 s). A wait
-// that runs out sets the sticky error flag and the kernel drains and returns.
+// Default wall-clock limit of every device-side wait, in nanoseconds (~1 s).
+// A wait that runs out records an error and the kernel drains and returns.
+// Each launch carries its own limit (Params::wait_ns); this is its default.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -77,16 +78,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed. Gives up after
-// kWaitLimitNs, or as soon as *abort becomes non-zero when abort is not null
-// (the drain waits pass null: they must outlast an abort); returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// limit_ns nanoseconds, or as soon as *abort becomes non-zero when abort is
+// not null (the drain waits pass null: they must outlast an abort); returns
+// false then.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(a, parity)) return true;
         if (abort != nullptr && *abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -145,6 +147,14 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 }
 __device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_last() {

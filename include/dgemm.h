@@ -42,11 +42,17 @@
  *     D (in-place update) when c_dtype == d_dtype.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream). Argument errors return synchronously, before launch.
- *     A failed launch returns DGEMM_ERR_CUDA. A device-side wait that gives up
- *     (bounded waits, about one second) sets a sticky per-device flag that
- *     dgemm_query_device_status reports.
+ *     A failed launch returns DGEMM_ERR_CUDA. Every device-side wait is
+ *     bounded (about one second); one that gives up is recorded in the call's
+ *     status word -- the first DGEMM_WS_STATUS_BYTES bytes of its workspace
+ *     when it was given one at least that large, else a per-device word --
+ *     and the kernel drains and returns. dgemm_query_device_status reports it.
  *   - The device must be compute capability 10.3 (GB300, sm_103a); any other
  *     device gives DGEMM_ERR_ARCH.
+ *   - The library caches per-device state on first use (properties, kernel
+ *     attributes, the device addresses of its own __device__ words). Do not
+ *     keep using it on a device after cudaDeviceReset: a reset frees those
+ *     addresses, and later calls would launch with stale ones.
  */
 #ifndef DGEMM_H
 #define DGEMM_H
@@ -74,6 +80,10 @@ typedef enum {
 } dgemm_status_t;
 
 typedef enum { DGEMM_F32 = 0, DGEMM_BF16 = 1, DGEMM_E4M3 = 2 } dgemm_dtype_t;
+
+/* Bytes at the start of a workspace that hold the call's status word (an
+ * epoch-tagged word: its contents on entry do not matter). */
+#define DGEMM_WS_STATUS_BYTES 256
 
 typedef enum {
     DGEMM_B_KN = 0, /* B stored K x N row-major                      */
@@ -115,8 +125,10 @@ typedef struct {
     int stages;            /* shared-memory pipeline depth                      */
     int num_tiles;         /* output tiles                                      */
     int grid;              /* CTAs launched (persistent: <= SM count)           */
-    int cooperative;       /* 1: launched cooperatively (CTAs wait on row bands
-                              other CTAs finish: all must be resident)        */
+    int cooperative;       /* 1: launched cooperatively, so every CTA is
+                              resident: CTAs wait on row bands other CTAs
+                              finish (requantisation) or on every K segment of
+                              a split tile (partials through the workspace)   */
     int raster_group;      /* tile rows per band of the swizzled raster         */
     int k_groups;          /* K-group promotion: K is split into this many
                               contiguous groups, each accumulated by the tensor
@@ -145,15 +157,20 @@ typedef struct {
  *   D        [M,N] of d_dtype: F32 or BF16, or E4M3 with
  *            epi->out_quant == DGEMM_QUANT_E4M3_ROW_AMAX.
  *   ws       device workspace of ws_bytes bytes, its contents arbitrary on
- *            entry. With the requantising epilogue it is required: at least
- *            256 + 4 * ceil(M / 64) * 64 + 2 * M * N bytes (a header of
- *            progress counters, row maxima, BF16 stash); dgemm_workspace_size(...) also counts room
- *            for splitting the last partial wave of tiles along K. Otherwise
- *            optional: with at least dgemm_workspace_size(...) bytes, tiles may
- *            be split along K (the last partial wave, or every tile when the
- *            tiles do not fill the GPU) with FP32 partials in the workspace;
- *            with less, only splits that need no workspace are made (the K
- *            segments of a tile running as one thread-block cluster).
+ *            entry. Its first DGEMM_WS_STATUS_BYTES bytes hold the call's
+ *            status word (when ws_bytes is at least that; read it with
+ *            dgemm_query_device_status(ws, stream)). With the requantising
+ *            epilogue it is required: at least
+ *            256 + 256 + 4 * ceil(M / 64) * 64 + 2 * M * N bytes (status
+ *            header, progress counters, row maxima, BF16 stash);
+ *            dgemm_workspace_size(...) also counts room for splitting the last
+ *            partial wave of tiles along K, which is made only when ws_bytes
+ *            covers it. Otherwise optional: with at least
+ *            dgemm_workspace_size(...) bytes, tiles may be split along K (the
+ *            last partial wave, or every tile when the tiles do not fill the
+ *            GPU) with FP32 partials in the workspace; with less, only splits
+ *            that need no workspace are made (the K segments of a tile running
+ *            as one thread-block cluster).
  * [W1] §1.1, §3.1, §6. */
 dgemm_status_t dgemm_bf16(const void* A, const void* B, dgemm_b_layout_t b_layout,
                           const void* C, dgemm_dtype_t c_dtype,
@@ -229,11 +246,65 @@ dgemm_status_t dgemm_plan(int is_fp8, int64_t M, int64_t N, int64_t K,
 /* Static English description of a status code; never NULL. */
 const char* dgemm_status_string(dgemm_status_t status);
 
-/* Synchronises `stream`, then returns and clears the sticky device-side error
- * flag of the current device (DGEMM_OK, or DGEMM_ERR_DEVICE_TIMEOUT if some
- * kernel on this device gave up a bounded wait since the last query), or
- * DGEMM_ERR_CUDA if the stream itself reports an error. */
-dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream);
+/* Synchronises `stream`, then returns and clears a status word:
+ *   ws != NULL: the status word at the start of that workspace, written by
+ *            the calls that were given it (with at least DGEMM_WS_STATUS_BYTES
+ *            bytes) since the last query of it;
+ *   ws == NULL: the per-device word of the current device, written by the
+ *            calls on this device that had no such workspace (and by the
+ *            allocation-free entry point below).
+ * Returns DGEMM_OK, DGEMM_ERR_DEVICE_TIMEOUT if one of those kernels gave up a
+ * bounded wait, or DGEMM_ERR_CUDA if the stream itself reports an error.
+ * Two calls with different workspaces report their timeouts separately.
+ * [W3] §5.1 (the call returns a status; device errors are read afterwards). */
+dgemm_status_t dgemm_query_device_status(const void* ws, dgemm_stream_t stream);
+
+/* ---- Planner overrides (tuning sweeps and tests) ----------------------------
+ *
+ * By default the planner makes every choice below. These overrides replace
+ * some of its choices for every later call in the process (tests use them to
+ * reach each kernel variant and split path; tuning sweeps to compare them).
+ * A field at its default (dgemm_overrides_init) keeps the planner's choice.
+ * The DGEMM_* environment variables named beside the fields are read once, at
+ * the first call, and only when DGEMM_ENV_OVERRIDES=1 is set too: a stray
+ * variable alone changes nothing. dgemm_plan honours the overrides as well. */
+typedef struct {
+    int tile_n;          /* 0; or 64, 128, 256: single-CTA tiles of this width where
+                            that variant exists (DGEMM_TILE_N)                     */
+    int cta_pair;        /* -1; 0: no CTA pairs; 1: CTA pairs where a pair variant
+                            exists (DGEMM_CTA_PAIR)                                 */
+    int tail_split;      /* -1; 0: never split tiles along K; 1: split the last
+                            partial wave's tiles whatever their length
+                            (DGEMM_TAIL_SPLIT, "force" = 1)                         */
+    int tail_halves;     /* -1; 0: never run tail tiles as N halves (DGEMM_TAIL_HALVES) */
+    int cluster_split;   /* -1; 0: split-K partials always through the workspace
+                            (DGEMM_CLUSTER_SPLIT)                                   */
+    int seg_first;       /* -1; 0: split segments after the whole tiles
+                            (DGEMM_SEG_FIRST)                                       */
+    int raster_group;    /* 0; else tile rows per band of the raster (DGEMM_RASTER_GROUP) */
+    int cooperative;     /* -1; 0: launch nothing cooperatively (for profilers that
+                            cannot launch cooperative cluster grids: the
+                            requantising form's row-band waits then rely on an
+                            otherwise idle GPU); 1: launch every plan whose split
+                            tiles exchange partials through the workspace
+                            cooperatively (DGEMM_COOPERATIVE)                       */
+    int64_t wait_limit_ns;     /* 0: about one second; else the limit of every
+                                  bounded device-side wait (DGEMM_WAIT_LIMIT_NS)    */
+    int64_t stall_after_loads; /* -1; testing the bounded waits: every CTA's operand
+                                  producer stops after this many stage loads, so the
+                                  tensor-core issuer's wait for the next stage runs
+                                  out (DGEMM_ERR_DEVICE_TIMEOUT); no environment
+                                  variable                                          */
+} dgemm_overrides_t;
+
+/* Fills *o with the defaults (every choice left to the planner). */
+void dgemm_overrides_init(dgemm_overrides_t* o);
+/* Sets the overrides for later calls (NULL: the defaults). Out-of-range
+ * fields give DGEMM_ERR_INVALID_VALUE and change nothing. Calls already
+ * launched are not affected. */
+dgemm_status_t dgemm_set_overrides(const dgemm_overrides_t* o);
+/* The overrides in force. */
+dgemm_status_t dgemm_get_overrides(dgemm_overrides_t* o);
 
 /* ---- Allocation-free variant (no counterpart in the paper) ----------------
  *
@@ -249,10 +320,15 @@ dgemm_status_t dgemm_query_device_status(dgemm_stream_t stream);
  *
  *   - The array is DGEMM_NOALLOC_SCRATCH_BYTES (32 MiB) per device and is held
  *     by every GPU that loads the library until the process exits.
- *   - A call needs dgemm_workspace_size(1, M, N, K, b_layout, epi) bytes of it
- *     (about 2*M*N + 4*M + 512); larger problems return
+ *   - A call needs 512 + 4 * ceil(M / 64) * 64 + 2 * M * N bytes of it (the
+ *     requantising workspace without the split area); larger problems return
  *     DGEMM_ERR_WORKSPACE_TOO_SMALL before anything is launched. M*N up to
- *     about 16.7 million elements fits (e.g. 2048 x 8192).
+ *     about 16.7 million elements fits (e.g. 2048 x 8192). The last partial
+ *     wave of tiles is split along K only when the split area fits as well
+ *     (dgemm_workspace_size(1, M, N, K, b_layout, epi) <= the array); otherwise
+ *     it runs as whole tiles, with the same results.
+ *   - Device-side errors of these calls go to the per-device status word:
+ *     read them with dgemm_query_device_status(NULL, stream).
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
  *     CUDA stream capture begins.

@@ -13,6 +13,14 @@ def dev():
     return torch.device("cuda:0")
 
 
+def status_ok(ws=None, stream=None) -> bool:
+    """No bounded device wait gave up: neither in the per-device status word nor,
+    when the call was given one, in its workspace's status word."""
+    dev_word = dg.dgemm_query_device_status(None, stream)
+    ws_word = dg.dgemm_query_device_status(ws, stream) if ws is not None else 0
+    return dev_word == 0 and ws_word == 0
+
+
 def run_workload(w: wl.Workload, d_dtype: str | None = None):
     """Run the library on workload w (tensors on CPU); returns (D, row_scale or None)
     as CPU tensors, after checking the device status word."""
@@ -32,7 +40,7 @@ def run_workload(w: wl.Workload, d_dtype: str | None = None):
         dg.dgemm_bf16(g.A, g.B, D, **kw)
     else:
         dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, k_group=w.k_group, b_block=w.b_block, **kw)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok(ws)
     return D.cpu(), (None if s is None else s.cpu())
 
 

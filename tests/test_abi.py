@@ -31,6 +31,7 @@ def test_header_declares_the_boundary():
     assert names == sorted(["dgemm_bf16", "dgemm_fp8_scaled", "dgemm_fp8_blockscaled", "dgemm_workspace_size",
                             "dgemm_plan",
                             "dgemm_status_string", "dgemm_query_device_status",
+                            "dgemm_overrides_init", "dgemm_set_overrides", "dgemm_get_overrides",
                             "dgemm_fp8_rowquant_noalloc"])
 
 
@@ -91,25 +92,25 @@ def test_argument_errors_return_before_any_device_call(lib):
     assert blk(64) == 2
 
 
-def test_workspace_sizes(lib, monkeypatch):
-    # requantisation: barrier header, row maxima, BF16 stash; 1024 tiles on 76
-    # pairs leave 36 for the last wave, split in halves: plus counters and one
-    # 256 x 256 FP32 partial per unit
-    base = 256 + 8192 * 4 + 8192 * 8192 * 2
+def test_workspace_sizes(lib, knobs):
+    # requantisation: status header, barrier header, row maxima, BF16 stash;
+    # 1024 tiles on 76 pairs leave 36 for the last wave, split in halves: plus
+    # counters and one 256 x 256 FP32 partial per unit
+    base = 256 + 256 + 8192 * 4 + 8192 * 8192 * 2
     ws = dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax")
     assert ws == base + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
     # tail splitting: 256 tiles on 76 pairs leave 28 tiles for the last wave; the
     # workspace bounds one 256 x 256 FP32 partial per unit plus the counters
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p["tail_tiles"], p["tail_split"]) == (28, 2)
-    assert p["workspace_bytes"] == 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
+    assert p["workspace_bytes"] == 256 + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
     # FP8 4096 x 11008 x 4096 has 32 K slices per tile: too short to split along
     # K; its 4 leftover tiles run as 8 N halves instead, with no workspace
     p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
     assert (p["tail_tiles"], p["tail_split"], p["tail_halves"], p["workspace_bytes"]) == (4, 1, 1, 0)
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
+    knobs(tail_halves="0")
     assert dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)["tail_halves"] == 0
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "0")
+    knobs(tail_split="0")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)["workspace_bytes"] == 0
     assert dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax") == base
 
@@ -142,13 +143,74 @@ def test_plan_of_per_group_scales(lib):
         dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=64, num_sms=152)
 
 
-def test_tile_width_and_pair_overrides(lib, monkeypatch):
-    monkeypatch.setenv("DGEMM_TILE_N", "128")
+def test_split_exchange_launch_modes(lib, knobs):
+    """Split tiles that exchange partials through the workspace: the under-filled
+    grid's split-K (the exchange ends the kernel) is launched cooperatively, so
+    its segments may wait for each other; the tail split of 4096^3 (exchange
+    overlapped by whole tiles) is a plain launch, where no segment waits for
+    one that may not have started. Cluster splits need neither."""
+    p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
+    assert p["tail_split"] == 2 and p["cooperative"] == 0
+    knobs(cluster_split="0")
+    p = dg.dgemm_plan(0, 1024, 1024, 4096, "nk", "bf16", num_sms=152)
+    assert p["tail_split"] >= 2 and p["cluster_split"] == 0 and p["cooperative"] == 1
+    knobs(cluster_split="1")
+    p = dg.dgemm_plan(0, 1024, 1024, 4096, "nk", "bf16", num_sms=152)
+    assert p["cluster_split"] == 1 and p["cooperative"] == 0
+    knobs(cooperative="1")
+    assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)["cooperative"] == 1
+    knobs(cooperative="0")
+    p5 = dg.dgemm_plan(1, 8192, 8192, 8192, "nk", "e4m3", out_quant="e4m3_row_amax", num_sms=152)
+    assert p5["cooperative"] == 0
+
+
+def test_overrides_validation_and_defaults(lib):
+    d = dg.get_overrides()
+    assert d == {"tile_n": 0, "cta_pair": -1, "tail_split": -1, "tail_halves": -1, "cluster_split": -1,
+                 "seg_first": -1, "raster_group": 0, "cooperative": -1, "wait_limit_ns": 0,
+                 "stall_after_loads": -1}
+    for bad in ({"cta_pair": 2}, {"tail_halves": 1}, {"cooperative": -2}, {"wait_limit_ns": -1},
+                {"stall_after_loads": -5}, {"tile_n": -64}):
+        with pytest.raises(dg.DgemmError):
+            dg.set_overrides(**bad)
+        assert dg.get_overrides() == d          # a refused set changes nothing
+    with dg.overrides(tile_n=128, wait_limit_ns=5_000_000):
+        assert dg.get_overrides()["tile_n"] == 128
+    assert dg.get_overrides() == d
+
+
+ENV_PROBE = r"""
+import sys
+sys.path.insert(0, {root!r})
+import dense_gemm_persistent_gb300 as dg
+p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
+print(p["tile_n"], p["cta_group"], dg.get_overrides()["tile_n"])
+"""
+
+
+@pytest.mark.parametrize("opt_in,expect", [(None, "256 2 0"), ("1", "128 1 128")])
+def test_environment_knobs_need_the_opt_in(lib, opt_in, expect):
+    """A stray DGEMM_TILE_N in the environment changes nothing; with
+    DGEMM_ENV_OVERRIDES=1 it is read once, at the first call."""
+    import subprocess
+    import sys
+    env = dict(os.environ, DGEMM_TILE_N="128")
+    env.pop("DGEMM_ENV_OVERRIDES", None)
+    if opt_in:
+        env["DGEMM_ENV_OVERRIDES"] = opt_in
+    r = subprocess.run([sys.executable, "-c", ENV_PROBE.format(root=ROOT)], env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == expect
+
+
+def test_tile_width_and_pair_overrides(lib, knobs):
+    knobs(tile_n="128")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tile_n"] == 128
-    monkeypatch.setenv("DGEMM_TILE_N", "96")     # no such variant: ignored
+    knobs(tile_n="96")     # no such variant: ignored
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tile_n"] == 256
-    monkeypatch.delenv("DGEMM_TILE_N")
-    monkeypatch.setenv("DGEMM_CTA_PAIR", "0")
+    knobs(tile_n=None)
+    knobs(cta_pair="0")
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")
     assert (p["cta_group"], p["tile_m"], p["tile_n"], p["num_tiles"], p["stages"]) == (1, 128, 256, 512, 4)
 
@@ -176,6 +238,19 @@ int main(void) {
     st = dgemm_bf16(NULL, NULL, DGEMM_B_KN, NULL, DGEMM_F32, NULL, DGEMM_BF16, 128, 128, 128, 1.0f, 0.0f,
                     NULL, NULL, 0, NULL);
     printf("null %d %s\n", (int)st, dgemm_status_string(st));
+    /* planner overrides: 128-wide single-CTA tiles, then the defaults again */
+    dgemm_overrides_t o;
+    dgemm_overrides_init(&o);
+    o.tile_n = 128;
+    st = dgemm_set_overrides(&o);
+    dgemm_status_t st2 = dgemm_plan(0, 4096, 4096, 4096, DGEMM_B_KN, DGEMM_BF16, NULL, 0, 152, &plan);
+    printf("override %d %d %d %d\n", (int)st, (int)st2, plan.tile_n, plan.cta_group);
+    dgemm_set_overrides(NULL);
+    dgemm_plan(0, 4096, 4096, 4096, DGEMM_B_KN, DGEMM_BF16, NULL, 0, 152, &plan);
+    printf("restored %d\n", plan.tile_n);
+    /* the status of a workspace's calls (no GPU here: the stream sync fails) */
+    st = dgemm_query_device_status((const void*)0, (dgemm_stream_t)0);
+    printf("query %d\n", (int)st);
     return 0;
 }
 """
@@ -204,3 +279,5 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     assert int(lines["ws"]) == ws > 2 * 256 * 512          # at least the BF16 stash
     code, text = lines["null"].split(" ", 1)
     assert int(code) == 1 and text == dg.dgemm_status_string(1)   # DGEMM_ERR_INVALID_VALUE
+    assert lines["override"] == "0 0 128 1" and lines["restored"] == "256"
+    assert int(lines["query"]) in (0, 5)        # DGEMM_OK on a GPU machine, DGEMM_ERR_CUDA without a device

@@ -63,6 +63,28 @@ def test_parse_clock_rows():
     assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
 
 
+def test_clock_summary_of_nvml_samples():
+    """Samples polled in-process while the timed region ran: the median SM
+    clock and the clock-event reasons named from their NVML bits (GPU idle and
+    other bits are not judged)."""
+    samples = [(1900.0, 1200.0, 0x4), (1950.0, 1300.0, 0x0), (1800.0, None, 0x1 | 0x4), (1850.0, 1100.0, 0x0)]
+    c = bench.summarize_clock_samples(samples, 2070.0, before=(2000.0, 300.0, 0), after=(1900.0, 800.0, 0))
+    assert c["sm_mhz"] == 1875.0 and c["samples"] == 4 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"] and c["power_w_max"] == 1300.0
+    assert (c["sm_mhz_min"], c["sm_mhz_max"], c["sm_mhz_before"], c["sm_mhz_after"]) == (1800.0, 1950.0, 2000.0,
+                                                                                        1900.0)
+    hot = bench.summarize_clock_samples([(1500.0, 1000.0, 0x8 | 0x40)], 2070.0)
+    assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    none = bench.summarize_clock_samples([], 2070.0)
+    assert none["sm_mhz"] is None and none["samples"] == 0
+
+
+def test_nvml_sampler_without_a_gpu_is_inert():
+    c = bench.NvmlClocks(0)
+    if not c.ok:
+        assert c.sample() is None
+
+
 def test_workload_selection():
     class A:
         config, k_group = 3, 128
@@ -88,6 +110,12 @@ def test_reference_arm_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+    # both arms describe the workload with the same config dict (run details
+    # such as the plan go under "setup" in the GPU arm)
+    class A:
+        config, shape, k_group, b_block = 1, None, 0, 1
+    assert d["config"] == bench.config_of(A, bench.make_workload(A))
 
 
 def test_shape_option():

@@ -14,7 +14,7 @@ import torch
 import dense_gemm_persistent_gb300 as dg
 import oracle
 import workloads as wl
-from gpu_util import dev
+from gpu_util import dev, status_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -37,16 +37,17 @@ def bf16_case(M, N, K, layout, seed, d_dtype=torch.float32, ws=False):
     A = int_bf16(rng, (M, K))
     B = int_bf16(rng, (K, N) if layout == "kn" else (N, K))
     D = torch.empty(M, N, dtype=d_dtype, device=dev())
-    dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout=layout, ws=workspace(0, M, N, K, layout) if ws else None)
-    assert dg.dgemm_query_device_status() == 0
+    wsb = workspace(0, M, N, K, layout) if ws else None
+    dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout=layout, ws=wsb)
+    assert status_ok(wsb)
     ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), layout)
     return D.cpu().to(torch.float64).numpy(), ref
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("bn", [64, 128, 256])
-def test_bf16_tile_exact(layout, bn, monkeypatch):
-    monkeypatch.setenv("DGEMM_TILE_N", str(bn))
+def test_bf16_tile_exact(layout, bn, knobs):
+    knobs(tile_n=str(bn))
     got, ref = bf16_case(300, 520, 200, layout, seed=bn)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
@@ -78,16 +79,16 @@ def fp8_case(M, N, K, layout, seed, scales="pow2", ws=False):
     else:
         sa, sb = torch.ones(M), torch.ones(N)
     D = torch.empty(M, N, dtype=torch.float32, device=dev())
-    dg.dgemm_fp8_scaled(Aq.to(dev()), Bq.to(dev()), sa.to(dev()), sb.to(dev()), D, b_layout=layout,
-                        ws=workspace(1, M, N, K, layout) if ws else None)
-    assert dg.dgemm_query_device_status() == 0
+    wsb = workspace(1, M, N, K, layout) if ws else None
+    dg.dgemm_fp8_scaled(Aq.to(dev()), Bq.to(dev()), sa.to(dev()), sb.to(dev()), D, b_layout=layout, ws=wsb)
+    assert status_ok(wsb)
     ref = oracle.fp8_gemm_ref(wl.codes_u8(Aq), wl.codes_u8(Bq), layout, sa.numpy(), sb.numpy())
     return D.cpu().to(torch.float64).numpy(), ref
 
 
 @pytest.mark.parametrize("layout,bn", [("nk", 64), ("nk", 128), ("nk", 256), ("kn", 128), ("kn", 256)])
-def test_fp8_tile_exact(layout, bn, monkeypatch):
-    monkeypatch.setenv("DGEMM_TILE_N", str(bn))
+def test_fp8_tile_exact(layout, bn, knobs):
+    knobs(tile_n=str(bn))
     got, ref = fp8_case(300, 528, 272, layout, seed=100 + bn)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
@@ -100,18 +101,18 @@ def test_fp8_swap_exact(layout, M):
 
 
 @pytest.mark.parametrize("kblocks", [1, 2, 3, 4, 5, 9, 13])
-def test_odd_k_block_counts_exact(kblocks, monkeypatch):
+def test_odd_k_block_counts_exact(kblocks, knobs):
     """Odd numbers of K slices expose pipeline-phase bugs (DeepGEMM write-up,
     czchanglian.com/news/51329, §4.3); 640 tiles of 128x64 over at most 152 CTAs
     also carry the stage and accumulator phases across several tiles per CTA."""
-    monkeypatch.setenv("DGEMM_TILE_N", "64")
+    knobs(tile_n="64")
     got, ref = bf16_case(2560, 2048, 64 * kblocks, "nk", seed=kblocks)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
 @pytest.mark.parametrize("kblocks", [1, 3, 4, 5, 7])
-def test_odd_k_block_counts_wide_tile_exact(kblocks, monkeypatch):
-    monkeypatch.setenv("DGEMM_TILE_N", "256")
+def test_odd_k_block_counts_wide_tile_exact(kblocks, knobs):
+    knobs(tile_n="256")
     got, ref = bf16_case(2560, 4096, 64 * kblocks, "kn", seed=50 + kblocks)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
@@ -129,13 +130,13 @@ def test_k_group_promotion_exact(M, kblocks):
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("pair,halves", [("0", "1"), ("1", "0"), ("1", "1")])
-def test_bf16_wide_tile_single_and_pair_exact(layout, pair, halves, monkeypatch):
+def test_bf16_wide_tile_single_and_pair_exact(layout, pair, halves, knobs):
     """128 x 256 tiles on one CTA and 256 x 256 tiles on a CTA pair (cta_group::2),
     with M, N and K tails; the pair's 12 tiles run whole, or (all of them
     being the last wave's) as 24 halves of 128 columns."""
-    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
-    monkeypatch.setenv("DGEMM_TILE_N", "256")
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", halves)
+    knobs(cta_pair=pair)
+    knobs(tile_n="256")
+    knobs(tail_halves=halves)
     plan = dg.dgemm_plan(0, 700, 776, 328, layout, "f32")
     assert plan["cta_group"] == (2 if pair == "1" else 1) and plan["tile_n"] == 256
     assert plan["tail_halves"] == (1 if pair + halves == "11" else 0)
@@ -145,12 +146,12 @@ def test_bf16_wide_tile_single_and_pair_exact(layout, pair, halves, monkeypatch)
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("pair,halves", [("0", "1"), ("1", "0"), ("1", "1")])
-def test_fp8_wide_tile_single_and_pair_exact(layout, pair, halves, monkeypatch):
+def test_fp8_wide_tile_single_and_pair_exact(layout, pair, halves, knobs):
     """As above for E4M3; an MN-major E4M3 B (128-column atoms) has no half
     tiles."""
-    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
-    monkeypatch.setenv("DGEMM_TILE_N", "256")
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", halves)
+    knobs(cta_pair=pair)
+    knobs(tile_n="256")
+    knobs(tail_halves=halves)
     plan = dg.dgemm_plan(1, 700, 784, 400, layout, "f32")
     assert plan["cta_group"] == (2 if pair == "1" else 1) and plan["tile_n"] == 256
     assert plan["tail_halves"] == (1 if pair + halves == "11" and layout == "nk" else 0)
@@ -172,15 +173,15 @@ def test_pair_phases_across_many_tiles_exact(kblocks):
 @pytest.mark.parametrize("shape,layout,pair", [((4096, 4096, 1024), "kn", "1"), ((4096, 4096, 1024), "nk", "0"),
                                                ((2304, 2816, 1024), "nk", "1"), ((2560, 2048, 1024), "kn", "0"),
                                                ((4000, 1288, 1024), "kn", "1")])
-def test_tail_split_exact(shape, layout, pair, seg_first, monkeypatch):
+def test_tail_split_exact(shape, layout, pair, seg_first, knobs):
     """The last partial wave's tiles split along K (FP32 partials in the
     workspace, each segment finishing its share of the units): still
     bit-exact, with the segments run before the whole tiles (at the raster's
     start) and after them (at its end)."""
-    monkeypatch.setenv("DGEMM_SEG_FIRST", seg_first)
-    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")   # split even these short tiles
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")      # along K, not N
+    knobs(seg_first=seg_first)
+    knobs(cta_pair=pair)
+    knobs(tail_split="force")   # split even these short tiles
+    knobs(tail_halves="0")      # along K, not N
     M, N, K = shape
     plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
     assert plan["tail_split"] >= 2
@@ -190,21 +191,21 @@ def test_tail_split_exact(shape, layout, pair, seg_first, monkeypatch):
 
 @pytest.mark.parametrize("seg_first", ["1", "0"])
 @pytest.mark.parametrize("layout", ["nk", "kn"])
-def test_tail_split_fp8_exact(layout, seg_first, monkeypatch):
-    monkeypatch.setenv("DGEMM_SEG_FIRST", seg_first)
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
+def test_tail_split_fp8_exact(layout, seg_first, knobs):
+    knobs(seg_first=seg_first)
+    knobs(tail_split="force")
+    knobs(tail_halves="0")
     plan = dg.dgemm_plan(1, 4096, 11008, 2048, layout, "f32")
     assert plan["tail_split"] >= 2
     got, ref = fp8_case(4096, 11008, 2048, layout, seed=800, ws=True)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
-def test_tail_split_repeated_calls_reuse_workspace(monkeypatch):
+def test_tail_split_repeated_calls_reuse_workspace(knobs):
     """Arrival counters are tagged with a per-launch epoch: the same workspace,
     even filled with garbage first, serves consecutive calls."""
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
+    knobs(tail_split="force")
+    knobs(tail_halves="0")
     M, N, K = 4096, 4096, 1024
     ws = workspace(0, M, N, K, "nk")
     ws.fill_(0xA5)
@@ -213,7 +214,7 @@ def test_tail_split_repeated_calls_reuse_workspace(monkeypatch):
         A = int_bf16(rng, (M, K)); B = int_bf16(rng, (N, K))
         D = torch.empty(M, N, dtype=torch.float32, device=dev())
         dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout="nk", ws=ws)
-        assert dg.dgemm_query_device_status() == 0
+        assert status_ok(ws)
         ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), "nk")
         assert np.array_equal(D.cpu().double().numpy(), ref)
 
@@ -241,10 +242,10 @@ def test_tail_halves_fp8_exact(shape):
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
-def test_tail_split_default_rule_on_long_tiles(monkeypatch):
+def test_tail_split_default_rule_on_long_tiles(knobs):
     """Without forcing, a tail is split along K only for long tiles: 4096^3 BF16
     (64 K slices) splits its 28-tile tail, the same shape at K = 2048 does not."""
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
+    knobs(tail_halves="0")
     assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tail_split"] == 2
     assert dg.dgemm_plan(0, 4096, 4096, 2048, "kn", "bf16")["tail_split"] == 1
     got, ref = bf16_case(2304, 2816, 3072, "nk", seed=900, ws=True)
@@ -255,13 +256,13 @@ def test_tail_split_default_rule_on_long_tiles(monkeypatch):
 @pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("shape,layout", [((1024, 1024, 4096), "nk"), ((1024, 1000, 2048), "kn"),
                                           ((520, 776, 1600), "nk")])
-def test_split_k_underfilled_tile_exact(shape, layout, cluster, monkeypatch):
+def test_split_k_underfilled_tile_exact(shape, layout, cluster, knobs):
     """Grids that do not fill the GPU split every tile along K (up to 4
     segments). Each segment finishes its share of the tile's 32-column units,
     adding the other segments' partials to its own accumulator from TMEM: read
     from the peers' shared memory when the segments form a cluster, else from
     the workspace."""
-    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
+    knobs(cluster_split=cluster)
     M, N, K = shape
     plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
     assert plan["tail_split"] >= 2 and plan["tail_tiles"] == plan["num_tiles"]
@@ -272,10 +273,10 @@ def test_split_k_underfilled_tile_exact(shape, layout, cluster, monkeypatch):
 
 @pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("M,layout", [(1, "nk"), (16, "nk"), (5, "kn"), (40, "nk"), (64, "kn")])
-def test_split_k_small_m_exact(M, layout, cluster, monkeypatch):
+def test_split_k_small_m_exact(M, layout, cluster, knobs):
     """Small-M (transposed) tiles split along K, with the K groups of each
     segment inside the segment's range."""
-    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
+    knobs(cluster_split=cluster)
     N, K = 4096, 4096
     plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
     assert plan["swap_ab"] == 1 and plan["tail_split"] >= 2 and plan["k_groups"] > 1
@@ -286,8 +287,8 @@ def test_split_k_small_m_exact(M, layout, cluster, monkeypatch):
 
 @pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("M", [1, 48, 256])
-def test_split_k_fp8_exact(M, cluster, monkeypatch):
-    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
+def test_split_k_fp8_exact(M, cluster, knobs):
+    knobs(cluster_split=cluster)
     N, K = 2048 if M < 256 else 512, 8192
     plan = dg.dgemm_plan(1, M, N, K, "nk", "f32")
     assert plan["tail_split"] >= 2 and plan["cluster_split"] == int(cluster)

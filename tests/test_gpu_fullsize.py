@@ -1,7 +1,9 @@
 """The five workloads at their full sizes, in the launch configuration the
 benchmark times (the library's own plan), checked on sampled rows that the
-oracle computes one by one (whole rows, so every column tile is covered), and
-in full where the oracle is fast enough (workloads 1 and 4)."""
+oracle computes one by one (whole rows, so every column tile is covered; at
+least one row in every 256-row tile row and the last row of every raster band,
+so every tile of the output is checked), and in full where the oracle is fast
+enough (workloads 1 and 4)."""
 import numpy as np
 import pytest
 
@@ -15,10 +17,23 @@ from tolerances import bf16_ulp_ok, c1_ok, frob_ok, requant_ok
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-def sample_rows(M, n=32, seed=0):
+def sample_rows(M, n=32, seed=0, tile=256, band=2048):
+    """n random rows, plus one random row inside every tile row of `tile`
+    rows, the last row of every raster band (`band` rows: 8 tile rows), and
+    the first and last two rows."""
     rng = np.random.default_rng(seed)
     pick = set(rng.choice(M, size=min(n, M), replace=False).tolist()) | {0, 1, M - 2, M - 1}
+    for t0 in range(0, M, tile):
+        pick.add(int(rng.integers(t0, min(M, t0 + tile))))
+    for b0 in range(0, M, band):
+        pick.add(min(M, b0 + band) - 1)
     return np.array(sorted(pick), dtype=np.int64)
+
+
+def test_sample_rows_touch_every_tile_row_and_band_end():
+    rows = sample_rows(8192, 24, seed=5)
+    assert set(rows // 256) == set(range(32))
+    assert {2047, 4095, 6143, 8191} <= set(rows.tolist())
 
 
 def test_workload1_full():

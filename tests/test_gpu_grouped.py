@@ -17,7 +17,7 @@ import torch
 import dense_gemm_persistent_gb300 as dg
 import oracle
 import workloads as wl
-from gpu_util import dev, run_workload, to_f64
+from gpu_util import dev, run_workload, status_ok, to_f64
 from test_gpu_parity import ref_of
 from tolerances import bf16_ulp_ok, c1_ok
 
@@ -37,7 +37,7 @@ def grouped_int_case(M, N, K, g, layout, seed, d_dtype=torch.float32, b_block=1)
     D = torch.empty(M, N, dtype=d_dtype, device=dev())
     dg.dgemm_fp8_scaled(Aq.to(dev()), Bq.to(dev()), sa.to(dev()), sb.to(dev()), D, b_layout=layout, k_group=g,
                         b_block=b_block, ws=ws)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok(ws)
     ref = oracle.fp8_gemm_ref(wl.codes_u8(Aq), wl.codes_u8(Bq), layout, sa.numpy(), sb.numpy(), k_group=g,
                               b_block=b_block)
     return D.cpu().to(torch.float64).numpy(), ref
@@ -46,11 +46,11 @@ def grouped_int_case(M, N, K, g, layout, seed, d_dtype=torch.float32, b_block=1)
 @pytest.mark.parametrize("g", [128, 384])
 @pytest.mark.parametrize("layout,bn,pair", [("nk", 64, "0"), ("nk", 128, "0"), ("nk", 256, "0"), ("nk", 256, "1"),
                                             ("kn", 128, "0"), ("kn", 256, "0"), ("kn", 256, "1")])
-def test_grouped_tile_exact(layout, bn, pair, g, monkeypatch):
+def test_grouped_tile_exact(layout, bn, pair, g, knobs):
     """Every tile variant, with the plan checked to use it."""
-    monkeypatch.setenv("DGEMM_TILE_N", str(bn))
-    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "0")
+    knobs(tile_n=str(bn))
+    knobs(cta_pair=pair)
+    knobs(tail_split="0")
     plan = dg.dgemm_plan(1, 300, 528, 1040, layout, "f32", k_group=g, num_sms=0)
     assert (plan["tile_n"], plan["cta_group"], plan["k_groups"]) == (bn, 2 if pair == "1" else 1, -(-1040 // g))
     # K = 1040: nine K slices, the last one partial; groups of 128 or 384
@@ -69,10 +69,10 @@ def test_grouped_small_m_exact(layout, M, g):
 
 @pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 4096), (16, 1024, 4096)])
-def test_grouped_split_k_segments_inside_groups_exact(M, N, K, cluster, monkeypatch):
+def test_grouped_split_k_segments_inside_groups_exact(M, N, K, cluster, knobs):
     """Under-filled grids split every tile into K segments of 8 slices; with
     groups of 3 slices (384 elements) most segments start inside a group."""
-    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
+    knobs(cluster_split=cluster)
     plan = dg.dgemm_plan(1, M, N, K, "nk", "f32", k_group=384, num_sms=0)
     assert plan["tail_split"] > 1 and plan["cluster_split"] == int(cluster)
     got, ref = grouped_int_case(M, N, K, 384, "nk", seed=K + M)
@@ -80,11 +80,11 @@ def test_grouped_split_k_segments_inside_groups_exact(M, N, K, cluster, monkeypa
 
 
 @pytest.mark.parametrize("seg_first", ["1", "0"])
-def test_grouped_tail_split_exact(seg_first, monkeypatch):
-    monkeypatch.setenv("DGEMM_SEG_FIRST", seg_first)
-    monkeypatch.setenv("DGEMM_CTA_PAIR", "0")
-    monkeypatch.setenv("DGEMM_TILE_N", "64")
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
+def test_grouped_tail_split_exact(seg_first, knobs):
+    knobs(seg_first=seg_first)
+    knobs(cta_pair="0")
+    knobs(tile_n="64")
+    knobs(tail_split="force")
     M, N, K = 1280, 1024, 2064     # 160 tiles of 128 x 64: the last 8 are split
     plan = dg.dgemm_plan(1, M, N, K, "nk", "f32", k_group=384, num_sms=0)
     assert plan["tail_tiles"] > 0 and plan["tail_split"] == 2
@@ -95,13 +95,13 @@ def test_grouped_tail_split_exact(seg_first, monkeypatch):
 @pytest.mark.parametrize("g", [128, 256])
 @pytest.mark.parametrize("layout,bn,pair", [("nk", 64, "0"), ("nk", 128, "0"), ("nk", 256, "0"), ("nk", 256, "1"),
                                             ("kn", 128, "0"), ("kn", 256, "1")])
-def test_block_scaled_tile_exact(layout, bn, pair, g, monkeypatch):
+def test_block_scaled_tile_exact(layout, bn, pair, g, knobs):
     """Weights scaled per (128-channel block, K group): each warp's columns
     share one scale per group (one fused multiply-add per output). N = 400
     ends inside the fourth block."""
-    monkeypatch.setenv("DGEMM_TILE_N", str(bn))
-    monkeypatch.setenv("DGEMM_CTA_PAIR", pair)
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "0")
+    knobs(tile_n=str(bn))
+    knobs(cta_pair=pair)
+    knobs(tail_split="0")
     got, ref = grouped_int_case(300, 400, 1040, g, layout, seed=bn + g + 7 * int(pair), b_block=128)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
@@ -117,8 +117,8 @@ def test_block_scaled_small_m_exact(layout, M):
 
 
 @pytest.mark.parametrize("cluster", ["1", "0"])
-def test_block_scaled_split_k_exact(cluster, monkeypatch):
-    monkeypatch.setenv("DGEMM_CLUSTER_SPLIT", cluster)
+def test_block_scaled_split_k_exact(cluster, knobs):
+    knobs(cluster_split=cluster)
     plan = dg.dgemm_plan(1, 256, 512, 4096, "nk", "f32", k_group=384, num_sms=0)
     assert plan["tail_split"] > 1 and plan["cluster_split"] == int(cluster)
     got, ref = grouped_int_case(256, 512, 4096, 384, "nk", seed=31, b_block=128)
@@ -178,5 +178,5 @@ def test_grouped_k_zero_gives_beta_c():
     zb = torch.empty(N, 0, dtype=torch.float8_e4m3fn, device=dev())
     sa, sb = torch.ones(M, device=dev()), torch.ones(N, device=dev())   # no K groups: never read
     dg.dgemm_fp8_scaled(z8, zb, sa, sb, D, b_layout="nk", k_group=128, C=C, beta=2.0)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok()
     assert torch.equal(D, 2.0 * C)

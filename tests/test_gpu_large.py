@@ -20,7 +20,7 @@ import torch
 import dense_gemm_persistent_gb300 as dg
 import oracle
 import workloads as wl
-from gpu_util import dev
+from gpu_util import dev, status_ok
 from tolerances import requant_ok
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -61,7 +61,7 @@ def test_tile_path_c_and_d_offsets_beyond_2_31():
     u, v, C = outer_sum_c(rng, M, N)
     D = torch.empty(M, N, dtype=torch.float32, device=dev())
     dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout="kn", C=C, alpha=1.0, beta=1.0)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok()
     rows = np.array(sorted({0, 1, TWO31 // N, TWO31 // N + 1, M - 2, M - 1}
                            | set(np.random.default_rng(7).choice(M, 8, replace=False).tolist())), dtype=np.int64)
     got = D[torch.from_numpy(rows).to(dev())].cpu().numpy().astype(np.float64)
@@ -86,7 +86,7 @@ def test_small_m_transposed_store_offsets_beyond_2_31():
     plan = dg.dgemm_plan(0, M, N, K, "nk", "f32")
     assert plan["swap_ab"] == 1
     dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout="nk", C=C, alpha=1.0, beta=1.0)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok()
     pick = np.random.default_rng(8).choice(N, 512, replace=False)
     cols = np.array(sorted(set(pick.tolist()) | set(range(0, 64)) | set(range(N - 512, N))), dtype=np.int64)
     got = D[:, torch.from_numpy(cols).to(dev())].cpu().numpy().astype(np.float64)
@@ -115,7 +115,7 @@ def test_very_long_k(fp8):
         dg.dgemm_fp8_scaled(A.to(dev()), B.to(dev()), ones_m, ones_n, D, b_layout="nk", ws=ws)
     else:
         dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout="nk", ws=ws)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok(ws)
     rows = np.array([0, 1, 127, 128, 200, M - 1], dtype=np.int64)
     got = D.cpu().numpy().astype(np.float64)[rows]
     if fp8:
@@ -141,7 +141,7 @@ def test_requant_stash_offsets_beyond_2_31():
                      dtype=torch.uint8, device=dev())
     dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, q, b_layout="nk", bias=g.bias, act="silu",
                         out_quant="e4m3_row_amax", out_row_scale=s, ws=ws)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok(ws)
     rows = np.array(sorted({0, TWO31 // N, TWO31 // N + 1, M - 1}
                            | set(np.random.default_rng(9).choice(M, 6, replace=False).tolist())), dtype=np.int64)
     idx = torch.from_numpy(rows).to(dev())

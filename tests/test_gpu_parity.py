@@ -10,7 +10,7 @@ import torch
 import dense_gemm_persistent_gb300 as dg
 import oracle
 import workloads as wl
-from gpu_util import dev, run_workload, to_f64
+from gpu_util import dev, run_workload, status_ok, to_f64
 from tolerances import bf16_ulp_ok, c1_ok, frob_ok, requant_ok
 
 pytestmark = pytest.mark.gpu
@@ -104,7 +104,7 @@ def test_in_place_beta_with_bf16_c():
     g = w.to(dev())
     D = C.to(dev())                         # C and D share storage
     dg.dgemm_bf16(g.A, g.B, D, b_layout="kn", C=D, alpha=0.75, beta=-1.25)
-    assert dg.dgemm_query_device_status() == 0
+    assert status_ok()
     ref = oracle.bf16_gemm_ref(wl.bits_u16(w.A), wl.bits_u16(w.B), "kn", wl.bits_u16(C), 0.75, -1.25)
     ok, msg = bf16_ulp_ok(to_f64(D.cpu()), ref)
     assert ok, msg
@@ -141,13 +141,13 @@ def test_fp8_with_c_bias_and_f32_output(M):
     assert ok, msg
 
 
-def test_requant_tail_split(monkeypatch):
+def test_requant_tail_split(knobs):
     """The requantising epilogue with the last partial wave split along K: the
     split tiles' segments finish their units with plain stores into the stash
     and fold their row maxima in before counting their row band. 90 tiles of 256 x 256
     on 76 pairs: the last 14 (rows 2048-2559 in the banded raster) are split."""
-    monkeypatch.setenv("DGEMM_TAIL_SPLIT", "force")
-    monkeypatch.setenv("DGEMM_TAIL_HALVES", "0")
+    knobs(tail_split="force")
+    knobs(tail_halves="0")
     w = wl.make(5, M=2560, N=2304, K=2048)
     plan = dg.dgemm_plan(1, w.M, w.N, w.K, "nk", "e4m3", out_quant="e4m3_row_amax", act="silu", num_sms=0)
     if plan["cta_group"] != 2 or plan["grid"] != 152:
@@ -224,5 +224,5 @@ def test_repeated_calls_and_streams():
             dg.dgemm_fp8_scaled(g.A, g.B, g.a_scale, g.b_scale, D, b_layout="nk", stream=s)
         outs.append(D)
     s.synchronize()
-    assert dg.dgemm_query_device_status(s) == 0
+    assert status_ok(stream=s)
     assert torch.equal(outs[0], outs[1])
