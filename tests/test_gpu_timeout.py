@@ -50,7 +50,7 @@ def bf16_call(M, N, K, seed, ws_bytes):
                                         (16, 1024, 2048, None)])   # small-M transposed form
 def test_stalled_producer_reports_timeout_through_the_workspace(M, N, K, pair, knobs):
     if pair is not None:
-        knobs(cta_pair=pair)
+        knobs(cta_pair=pair, tile_n="256")   # pairs exist for 256-wide tiles
     ws_bytes = max(dg.dgemm_workspace_size(0, M, N, K, "nk"), 256)
     call, D, ws, ref = bf16_call(M, N, K, seed=M + K, ws_bytes=ws_bytes)
     plan = dg.dgemm_plan(0, M, N, K, "nk", "f32", num_sms=0)
