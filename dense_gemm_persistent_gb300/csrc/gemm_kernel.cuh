@@ -112,19 +112,22 @@ struct Params {
     // every CTA stops after issuing this many stage loads, so that the MMA's
     // wait for the next stage runs out and the kernel drains and returns.
     long long stall_after;
-    // Split tiles (all modes): tiles [0, dp_tiles) run whole; each of the
-    // remaining tiles is split along K into `split` segments (tail_items in
-    // all), every unit taking at most one (before its whole tiles, if any;
-    // with seg_first the split tiles are the first num_tiles - dp_tiles of the
-    // raster instead of the last).
+    // Split tiles (all modes): tiles [0, dp_tiles) run whole; the K slices of
+    // the S = num_tiles - dp_tiles remaining tiles, S * k_blocks in tile order,
+    // are dealt out to the first tail_items units as contiguous ranges (unit u
+    // takes [g(u), g(u + 1)), g(u) = u * S * k_blocks / tail_items), run before
+    // the unit's whole tiles with seg_first (the split tiles are then the
+    // first S of the raster instead of the last). With tail_items = S * split
+    // every tile is cut into `split` equal segments; otherwise a range may end
+    // one tile and start the next (two work items), and a tile has a varying
+    // number of segments (at most 15). `split` > 1 marks a K-split plan.
     // 32-column unit u of each epilogue warp's region belongs to segment
-    // u % split: a segment parks the units others own as FP32 partials in
-    // `partials`, counts its arrival in tail_count, waits (bounded) for every
-    // segment of the region, and finishes its own units from its accumulator
-    // plus the others' partials.
+    // u % (its tile's segments) in the symmetric exchange (split_sym).
     int dp_tiles, split, tail_items;
     int seg_first;           // 1: a unit runs its split item before its whole tiles
-    float* partials;         // [tail_items][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4
+    // [slot][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4; the i-th item
+    // (0 or 1) of unit u parks in slot u + i * tail_items
+    float* partials;
     // Split-K through distributed shared memory (single-CTA kernels, under-
     // filled grids): the split K segments of a tile are the CTAs of one
     // cluster of `split` CTAs (rank = segment); partials go through the idle
@@ -149,34 +152,79 @@ struct Params {
 
 // One unit of work: a whole tile (item < 0) or one K segment of a split tile.
 struct Work {
-    int tile, kb0, kb1, item;
+    int tile, kb0, kb1, item;   // item: the segment's partial slot
     int half;   // -1: the whole tile; 0 / 1: that 128-column half (tail_halves)
+    // K segments: the split tile's index among the split tiles, this
+    // segment's index within the tile, the tile's segment count and the unit
+    // that runs its first segment
+    int stile, seg, nseg, uf;
 };
 
+// Start of unit u's range of split-tile K slices (see Params::tail_items).
+__device__ __forceinline__ long long sk_start(const Params& p, int u) {
+    const long long T = static_cast<long long>(p.num_tiles - p.dp_tiles) * p.k_blocks;
+    return static_cast<long long>(u) * T / p.tail_items;
+}
+
+// The units whose ranges cover split tile t: the first, and how many. The
+// first is the largest u with sk_start(u) <= t * k_blocks, i.e.
+// ceil((x + 1) * tail_items / T) - 1 for x = t * k_blocks.
+__device__ __forceinline__ void sk_span(const Params& p, int t, int& uf, int& n) {
+    const long long T = static_cast<long long>(p.num_tiles - p.dp_tiles) * p.k_blocks;
+    const long long U = p.tail_items;
+    const long long x0 = static_cast<long long>(t) * p.k_blocks;
+    const long long x1 = x0 + p.k_blocks - 1;
+    uf = static_cast<int>(((x0 + 1) * U + T - 1) / T - 1);
+    const int ul = static_cast<int>(((x1 + 1) * U + T - 1) / T - 1);
+    n = ul - uf + 1;
+}
+
+// Partial slot of segment sg of split tile t whose first segment is unit uf's.
+__device__ __forceinline__ int sk_slot(const Params& p, int t, int uf, int sg) {
+    const int u = uf + sg;
+    const int i = t - static_cast<int>(sk_start(p, u) / p.k_blocks);
+    return u + i * p.tail_items;
+}
+
 // The iter-th work item of a unit (a CTA, or a CTA pair): its whole tiles
-// unit, unit + units, ... (dp_tiles of them in all), then its tail item (a K
-// segment or an N half of a split tile), or with seg_first its K segment first.
+// unit, unit + units, ... (dp_tiles of them in all), then its split items (K
+// segments, one or two) or its tail half, or with seg_first its K segments
+// first.
 __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, int iter, Work& w) {
-    // With seg_first, a unit's K segment of a split tile runs before its whole
+    // With seg_first, a unit's K segments of split tiles run before its whole
     // tiles, so that the segments' exchange of partial sums (a chain of L2 round
     // trips) overlaps the next tile's mainloop instead of ending the kernel.
-    // Every segment of a split tile is then its unit's first item, all running
-    // at once, and the split tiles are the raster's first ones (tiles [0, S),
-    // whole tiles from S on), next to the whole tiles started alongside them.
-    const bool front = p.seg_first && p.split > 1 && !p.tail_halves && p.dp_tiles > 0;
-    const bool seg_first = front && unit < p.tail_items;
+    // Every segment of a split tile then runs at the start of the kernel, and
+    // the split tiles are the raster's first ones (tiles [0, S), whole tiles
+    // from S on), next to the whole tiles started alongside them.
+    const bool ksplit = p.split > 1 && !p.tail_halves;
+    const bool front = p.seg_first && ksplit && p.dp_tiles > 0;
     const int dp0 = front ? p.num_tiles - p.dp_tiles : 0;   // first whole tile
-    if (seg_first) {
-        if (iter == 0) {
-            const int seg = unit % p.split;
-            w.half = -1;
-            w.tile = unit / p.split;
-            w.kb0 = (seg * p.k_blocks) / p.split;
-            w.kb1 = ((seg + 1) * p.k_blocks) / p.split;
-            w.item = unit;
+    long long g0 = 0, g1 = 0;
+    int nsplit = 0;   // this unit's split items
+    if (ksplit && unit < p.tail_items) {
+        g0 = sk_start(p, unit);
+        g1 = sk_start(p, unit + 1);
+        nsplit = static_cast<int>((g1 - 1) / p.k_blocks - g0 / p.k_blocks) + 1;
+    }
+    auto split_item = [&](int i) {
+        const int t = static_cast<int>(g0 / p.k_blocks) + i;
+        const long long base = static_cast<long long>(t) * p.k_blocks;
+        w.half = -1;
+        w.stile = t;
+        w.tile = (front ? 0 : p.dp_tiles) + t;
+        w.kb0 = static_cast<int>((g0 > base ? g0 : base) - base);
+        w.kb1 = static_cast<int>((g1 < base + p.k_blocks ? g1 : base + p.k_blocks) - base);
+        w.item = unit + i * p.tail_items;
+        sk_span(p, t, w.uf, w.nseg);
+        w.seg = unit - w.uf;
+    };
+    if (front) {
+        if (iter < nsplit) {
+            split_item(iter);
             return true;
         }
-        --iter;
+        iter -= nsplit;
     }
     const int dp_count = p.dp_tiles > unit ? (p.dp_tiles - unit + units - 1) / units : 0;
     w.half = -1;
@@ -187,10 +235,11 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
         w.item = -1;
         return true;
     }
-    if (seg_first) return false;   // its split item ran first
-    const int j = unit + (iter - dp_count) * units;
-    if (j >= p.tail_items) return false;
+    if (front) return false;   // its split items ran first
+    iter -= dp_count;
     if (p.tail_halves) {
+        const int j = unit + iter * units;
+        if (j >= p.tail_items) return false;
         w.tile = p.dp_tiles + j / 2;
         w.half = j % 2;
         w.kb0 = 0;
@@ -198,14 +247,12 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
         w.item = -1;
         return true;
     }
-    const int seg = j % p.split;
-    w.tile = p.dp_tiles + j / p.split;
-    w.kb0 = (seg * p.k_blocks) / p.split;
-    w.kb1 = ((seg + 1) * p.k_blocks) / p.split;
-    w.item = j;
-    return true;
+    if (iter < nsplit) {
+        split_item(iter);
+        return true;
+    }
+    return false;
 }
-
 
 
 template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false, bool GS_ = false>
@@ -1285,9 +1332,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // stores them directly: about one round trip through L2 per segment
             // instead of a single warp reading every partial unit by unit.
             // Otherwise the last segment to arrive finishes the region (below).
-            const int item0 = part ? (w.item / p.split) * p.split : 0;
-            const int seg = part ? w.item - item0 : 0;
-            auto owner = [&](int u) { return u % p.split; };
+            const int seg = part ? w.seg : 0;
+            const int nseg = part ? w.nseg : 1;   // the tile's segments
+            auto owner = [&](int u) { return u % nseg; };
             // generic writes to buffers the TMA (async proxy) filled
             if (part && p.cluster_split) fence_proxy_async_smem();
             const bool unit_pass = !part || p.cluster_split || p.split_sym;
@@ -1355,10 +1402,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 #pragma unroll
                             for (int o = 0; o < 3; ++o) {
                                 const int peer = o + (o >= seg ? 1 : 0);
-                                const uint32_t base = peer < p.split ? mapa_shared(mine, static_cast<uint32_t>(peer)) : 0u;
+                                const uint32_t base = peer < nseg ? mapa_shared(mine, static_cast<uint32_t>(peer)) : 0u;
 #pragma unroll
                                 for (int j = 0; j < UNIT_F4; ++j)
-                                    f[o][j] = peer < p.split ? ld_shared_cluster_f4(base + 16u * 32u * j)
+                                    f[o][j] = peer < nseg ? ld_shared_cluster_f4(base + 16u * 32u * j)
                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
 #pragma unroll
@@ -1381,7 +1428,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     // (launch epoch << 8) | (segments parked << 4) | arrivals; a word
                     // left by any earlier launch counts as zero of each.
                     unsigned long long* cnt =
-                        p.tail_count + ((w.item / p.split) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
+                        p.tail_count + (static_cast<int64_t>(w.stile) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
                     // lane 0: counts this segment in; returns how many had arrived
                     // before it, or -1 if the word could not be updated.
                     auto arrive = [&]() -> int {
@@ -1406,30 +1453,33 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         }
                         return 1u;
                     };
-                    // v += the other segments' partials of unit u, all loads in flight together
+                    // v += the other segments' partials of unit u, three
+                    // segments' loads in flight at a time
+                    const int64_t uoff = ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS) * (UNIT_F4 * 32) + lane;
                     auto add_partials = [&](int u, float (&v)[32]) {
-                        const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
-                                            ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
-                                                (UNIT_F4 * 32) +
-                                            lane;
-                        float4 f[3][UNIT_F4];
+                        const float4* src = reinterpret_cast<const float4*>(p.partials) + uoff + u * (UNIT_F4 * 32);
+                        for (int o0 = 0; o0 < nseg - 1; o0 += 3) {
+                            float4 f[3][UNIT_F4];
 #pragma unroll
-                        for (int o = 0; o < 3; ++o) {
-                            const int sgi = o + (o >= seg ? 1 : 0);
+                            for (int o = 0; o < 3; ++o) {
+                                const int k = o0 + o;
+                                const int sgi = k + (k >= seg ? 1 : 0);
+                                const int64_t slot = k < nseg - 1 ? sk_slot(p, w.stile, w.uf, sgi) : 0;
 #pragma unroll
-                            for (int j = 0; j < UNIT_F4; ++j)
-                                f[o][j] = sgi < p.split ? __ldcg(src + sgi * ITEM_F4 + 32 * j)
-                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-#pragma unroll
-                        for (int o = 0; o < 3; ++o)
-#pragma unroll
-                            for (int j = 0; j < UNIT_F4; ++j) {
-                                v[4 * j] += f[o][j].x;
-                                v[4 * j + 1] += f[o][j].y;
-                                v[4 * j + 2] += f[o][j].z;
-                                v[4 * j + 3] += f[o][j].w;
+                                for (int j = 0; j < UNIT_F4; ++j)
+                                    f[o][j] = k < nseg - 1 ? __ldcg(src + slot * ITEM_F4 + 32 * j)
+                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
+#pragma unroll
+                            for (int o = 0; o < 3; ++o)
+#pragma unroll
+                                for (int j = 0; j < UNIT_F4; ++j) {
+                                    v[4 * j] += f[o][j].x;
+                                    v[4 * j + 1] += f[o][j].y;
+                                    v[4 * j + 2] += f[o][j].z;
+                                    v[4 * j + 3] += f[o][j].w;
+                                }
+                        }
                     };
                     if (p.split_sym) {
                         // Every segment of the tile is resident (cooperative launch):
@@ -1447,7 +1497,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             if (before < 0) {
                                 record_error(p, ERR_ARRIVAL);
                             } else if (owns) {
-                                const unsigned long long want = (p.epoch << 8) | static_cast<unsigned long long>(p.split);
+                                const unsigned long long want = (p.epoch << 8) | static_cast<unsigned long long>(nseg);
                                 ready = await([&](unsigned long long x) { return x == want; });
                                 __threadfence();
                             } else {
@@ -1483,7 +1533,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         if (before < 0) {
                             if (lane == 0) record_error(p, ERR_ARRIVAL);
                             ok = false;
-                        } else if (before < p.split - 1) {
+                        } else if (before < nseg - 1) {
 #pragma unroll U_UNROLL
                             for (int u = 0; u < NUNITS; ++u) {
                                 float v[32];
@@ -1502,7 +1552,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         } else {
                             unsigned ready = 0;
                             if (lane == 0) {
-                                const unsigned long long want = static_cast<unsigned long long>(p.split - 1);
+                                const unsigned long long want = static_cast<unsigned long long>(nseg - 1);
                                 ready = await([&](unsigned long long x) {
                                     return (x >> 8) == p.epoch && ((x >> 4) & 0xFull) == want;
                                 });

@@ -140,13 +140,19 @@ typedef struct {
                               run first, as the raster's first tiles, and their
                               partial sums are exchanged while whole tiles
                               run; otherwise they run last                    */
-    int tail_split;        /* K segments per tail tile (1 = no splitting)       */
+    int tail_split;        /* K segments per tail tile, the most of any tile
+                              (1 = no splitting)                                */
     int cluster_split;     /* 1: the K segments of each split tile run as one
                               thread-block cluster and are summed through
                               distributed shared memory (no workspace needed) */
     int tail_halves;       /* 1: the tail_tiles run instead as two halves of
                               tile_n / 2 columns each, every half over the
                               whole K range (no workspace needed)            */
+    int tail_units;        /* units (CTAs or CTA pairs) that run the tail's
+                              segments or halves (0 = none). A K-split tail of
+                              the plain form deals the tail tiles' K slices
+                              out evenly to these units, so a unit may finish
+                              one tile's last slices and the next tile's first */
     size_t smem_bytes;     /* dynamic shared memory per CTA                     */
     size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
 } dgemm_plan_t;
@@ -281,6 +287,9 @@ typedef struct {
                             (DGEMM_CLUSTER_SPLIT)                                   */
     int seg_first;       /* -1; 0: split segments after the whole tiles
                             (DGEMM_SEG_FIRST)                                       */
+    int tail_balance;    /* -1; 0: split the plain form's tail tiles into two equal
+                            K halves each instead of dealing their K slices out
+                            to every unit (DGEMM_TAIL_BALANCE)                     */
     int raster_group;    /* 0; else tile rows per band of the raster (DGEMM_RASTER_GROUP) */
     int cooperative;     /* -1; 0: launch nothing cooperatively (for profilers that
                             cannot launch cooperative cluster grids: the

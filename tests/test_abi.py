@@ -99,11 +99,13 @@ def test_workspace_sizes(lib, knobs):
     base = 256 + 256 + 8192 * 4 + 8192 * 8192 * 2
     ws = dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax")
     assert ws == base + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
-    # tail splitting: 256 tiles on 76 pairs leave 28 tiles for the last wave; the
-    # workspace bounds one 256 x 256 FP32 partial per unit plus the counters
+    # tail splitting: 256 tiles on 76 pairs leave 28 tiles for the last wave,
+    # whose 28 x 64 K slices are dealt out evenly to all 76 pairs (a pair may
+    # finish one tile and start the next, so two 256 x 256 FP32 partial slots
+    # per pair) plus the counters
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
-    assert (p["tail_tiles"], p["tail_split"]) == (28, 2)
-    assert p["workspace_bytes"] == 256 + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
+    assert (p["tail_tiles"], p["tail_units"], p["tail_split"]) == (28, 76, 4)
+    assert p["workspace_bytes"] == 256 + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 2 * 76 * 2 * 128 * 256 * 4
     # FP8 4096 x 11008 x 4096 has 32 K slices per tile: too short to split along
     # K; its 4 leftover tiles run as 8 N halves instead, with no workspace
     p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
@@ -121,7 +123,7 @@ def test_plans_for_the_five_workloads(lib):
     p2 = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p2["cta_group"], p2["tile_m"], p2["tile_n"]) == (2, 256, 256)
     assert p2["num_tiles"] == 256 and p2["grid"] == 152 and p2["stages"] == 6
-    assert (p2["tail_tiles"], p2["tail_split"]) == (28, 2)      # 3 full waves + 28 tiles in K halves
+    assert (p2["tail_tiles"], p2["tail_units"]) == (28, 76)     # 3 full waves + 28 tiles over all 76 pairs
     p3 = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
     assert p3["cta_group"] == 2 and p3["num_tiles"] == 16 * 43 and p3["grid"] == 152
     p4 = dg.dgemm_plan(0, 16, 18432, 7168, "nk", "bf16", num_sms=152)
@@ -150,7 +152,7 @@ def test_split_exchange_launch_modes(lib, knobs):
     overlapped by whole tiles) is a plain launch, where no segment waits for
     one that may not have started. Cluster splits need neither."""
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
-    assert p["tail_split"] == 2 and p["cooperative"] == 0
+    assert p["tail_split"] >= 2 and p["cooperative"] == 0
     knobs(cluster_split="0")
     p = dg.dgemm_plan(0, 1024, 1024, 4096, "nk", "bf16", num_sms=152)
     assert p["tail_split"] >= 2 and p["cluster_split"] == 0 and p["cooperative"] == 1
@@ -167,7 +169,7 @@ def test_split_exchange_launch_modes(lib, knobs):
 def test_overrides_validation_and_defaults(lib):
     d = dg.get_overrides()
     assert d == {"tile_n": 0, "cta_pair": -1, "tail_split": -1, "tail_halves": -1, "cluster_split": -1,
-                 "seg_first": -1, "raster_group": 0, "cooperative": -1, "wait_limit_ns": 0,
+                 "seg_first": -1, "tail_balance": -1, "raster_group": 0, "cooperative": -1, "wait_limit_ns": 0,
                  "stall_after_loads": -1}
     for bad in ({"cta_pair": 2}, {"tail_halves": 1}, {"cooperative": -2}, {"wait_limit_ns": -1},
                 {"stall_after_loads": -5}, {"tile_n": -64}):

@@ -246,10 +246,10 @@ def test_tail_split_default_rule_on_long_tiles(knobs):
     """Without forcing, a tail is split along K only for long tiles: 4096^3 BF16
     (64 K slices) splits its 28-tile tail, the same shape at K = 2048 does not."""
     knobs(tail_halves="0")
-    assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tail_split"] == 2
+    assert dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16")["tail_split"] >= 2
     assert dg.dgemm_plan(0, 4096, 4096, 2048, "kn", "bf16")["tail_split"] == 1
     got, ref = bf16_case(2304, 2816, 3072, "nk", seed=900, ws=True)
-    assert dg.dgemm_plan(0, 2304, 2816, 3072, "nk", "f32")["tail_split"] == 2
+    assert dg.dgemm_plan(0, 2304, 2816, 3072, "nk", "f32")["tail_split"] >= 2
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
@@ -293,4 +293,64 @@ def test_split_k_fp8_exact(M, cluster, knobs):
     plan = dg.dgemm_plan(1, M, N, K, "nk", "f32")
     assert plan["tail_split"] >= 2 and plan["cluster_split"] == int(cluster)
     got, ref = fp8_case(M, N, K, "nk", seed=1200 + M, ws=True)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+def sampled_rows(M, tile_m, seed):
+    """A row in every tile row, plus the first and last rows."""
+    rng = np.random.default_rng(seed)
+    pick = {0, M - 1} | {int(rng.integers(t0, min(M, t0 + tile_m))) for t0 in range(0, M, tile_m)}
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def balanced_case(M, N, K, layout, fp8, seed):
+    """Integer operands (exact in FP32), FP32 output, checked bit-exact on a row
+    of every tile row: every split tile's segments are covered."""
+    rng = np.random.default_rng(seed)
+    mk = int_e4m3 if fp8 else int_bf16
+    A = mk(rng, (M, K))
+    B = mk(rng, (K, N) if layout == "kn" else (N, K))
+    D = torch.empty(M, N, dtype=torch.float32, device=dev())
+    ws = workspace(fp8, M, N, K, layout)
+    if fp8:
+        ones_m, ones_n = torch.ones(M, device=dev()), torch.ones(N, device=dev())
+        dg.dgemm_fp8_scaled(A.to(dev()), B.to(dev()), ones_m, ones_n, D, b_layout=layout, ws=ws)
+    else:
+        dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout=layout, ws=ws)
+    assert status_ok(ws)
+    plan = dg.dgemm_plan(fp8, M, N, K, layout, "f32", num_sms=0)
+    rows = sampled_rows(M, plan["tile_m"], seed)
+    if fp8:
+        ref = oracle.fp8_gemm_ref(wl.codes_u8(A), wl.codes_u8(B), layout, np.ones(M, np.float32),
+                                  np.ones(N, np.float32), rows=rows)
+    else:
+        ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), layout, rows=rows)
+    got = D.cpu().double().numpy()[rows]
+    return got, ref, plan
+
+
+@pytest.mark.parametrize("protocol", ["plain", "cooperative"])
+@pytest.mark.parametrize("seg_first", ["1", "0"])
+@pytest.mark.parametrize("shape,layout,fp8,pair", [
+    ((4096, 4096, 4096), "kn", 0, None),     # the 4096^3 plan: 28 tiles over 76 pairs, up to 4 segments
+    ((512, 11008, 4096), "nk", 0, None),     # 10 leftover pair tiles over 76 pairs
+    ((1280, 4096, 4160), "kn", 0, "0"),      # single-CTA tiles: 8 leftover tiles over 65 CTAs
+    ((4096, 11008, 6400), "nk", 1, None),    # FP8: 4 leftover tiles of 50 K slices over 25 pairs
+])
+def test_balanced_tail_split_exact(shape, layout, fp8, pair, seg_first, protocol, knobs):
+    """The last partial wave's tiles, their K slices laid end to end and dealt
+    out in equal ranges, so that a unit may finish one tile and start the next
+    and a tile has a varying number of segments: bit-exact, with the segments
+    run first or last, in a plain launch (the last segment to arrive finishes
+    the tile) and a cooperative one (every segment finishes its own units)."""
+    knobs(seg_first=seg_first)
+    if pair is not None:
+        knobs(cta_pair=pair)
+    if protocol == "cooperative":
+        knobs(cooperative="1")
+    M, N, K = shape
+    got, ref, plan = balanced_case(M, N, K, layout, fp8, seed=1300 + K + M)
+    assert plan["tail_split"] >= 2 and plan["tail_units"] > plan["tail_tiles"]
+    assert plan["tail_units"] % plan["tail_tiles"] != 0          # uneven segments
+    assert plan["cooperative"] == (1 if protocol == "cooperative" else 0)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
