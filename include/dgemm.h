@@ -287,9 +287,12 @@ typedef struct {
                             (DGEMM_CLUSTER_SPLIT)                                   */
     int seg_first;       /* -1; 0: split segments after the whole tiles
                             (DGEMM_SEG_FIRST)                                       */
-    int tail_balance;    /* -1; 0: split the plain form's tail tiles into two equal
-                            K halves each instead of dealing their K slices out
-                            to every unit (DGEMM_TAIL_BALANCE)                     */
+    int tail_balance;    /* -1 or 0: split the plain form's tail tiles into two
+                            equal K halves each; 1: deal their K slices out in
+                            equal ranges to every unit (a unit may finish one
+                            tile and start the next; measured slower on 4096^3:
+                            the larger exchange of partials competes with the
+                            operand feed) (DGEMM_TAIL_BALANCE)                     */
     int raster_group;    /* 0; else tile rows per band of the raster (DGEMM_RASTER_GROUP) */
     int cooperative;     /* -1; 0: launch nothing cooperatively (for profilers that
                             cannot launch cooperative cluster grids: the

@@ -100,12 +100,18 @@ def test_workspace_sizes(lib, knobs):
     ws = dg.dgemm_workspace_size(1, 8192, 8192, 8192, "nk", out_quant="e4m3_row_amax")
     assert ws == base + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
     # tail splitting: 256 tiles on 76 pairs leave 28 tiles for the last wave,
-    # whose 28 x 64 K slices are dealt out evenly to all 76 pairs (a pair may
-    # finish one tile and start the next, so two 256 x 256 FP32 partial slots
-    # per pair) plus the counters
+    # each split in two K halves on 56 pairs; the workspace bounds one 256 x 256
+    # FP32 partial per unit plus the counters
+    p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
+    assert (p["tail_tiles"], p["tail_units"], p["tail_split"]) == (28, 56, 2)
+    assert p["workspace_bytes"] == 256 + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
+    # with the K slices dealt out to every pair instead, a pair may finish one
+    # tile and start the next: two partial slots per pair
+    knobs(tail_balance="1")
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p["tail_tiles"], p["tail_units"], p["tail_split"]) == (28, 76, 4)
     assert p["workspace_bytes"] == 256 + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 2 * 76 * 2 * 128 * 256 * 4
+    knobs(tail_balance=None)
     # FP8 4096 x 11008 x 4096 has 32 K slices per tile: too short to split along
     # K; its 4 leftover tiles run as 8 N halves instead, with no workspace
     p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
@@ -123,7 +129,7 @@ def test_plans_for_the_five_workloads(lib):
     p2 = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p2["cta_group"], p2["tile_m"], p2["tile_n"]) == (2, 256, 256)
     assert p2["num_tiles"] == 256 and p2["grid"] == 152 and p2["stages"] == 6
-    assert (p2["tail_tiles"], p2["tail_units"]) == (28, 76)     # 3 full waves + 28 tiles over all 76 pairs
+    assert (p2["tail_tiles"], p2["tail_split"], p2["tail_units"]) == (28, 2, 56)   # 3 full waves + 28 tiles in K halves
     p3 = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
     assert p3["cta_group"] == 2 and p3["num_tiles"] == 16 * 43 and p3["grid"] == 152
     p4 = dg.dgemm_plan(0, 16, 18432, 7168, "nk", "bf16", num_sms=152)

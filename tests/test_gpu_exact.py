@@ -343,7 +343,7 @@ def test_balanced_tail_split_exact(shape, layout, fp8, pair, seg_first, protocol
     and a tile has a varying number of segments: bit-exact, with the segments
     run first or last, in a plain launch (the last segment to arrive finishes
     the tile) and a cooperative one (every segment finishes its own units)."""
-    knobs(seg_first=seg_first)
+    knobs(seg_first=seg_first, tail_balance="1")
     if pair is not None:
         knobs(cta_pair=pair)
     if protocol == "cooperative":
