@@ -182,6 +182,7 @@ __device__ __forceinline__ void sk_span(const Params& p, int t, int& uf, int& n)
 // Partial slot of segment sg of split tile t whose first segment is unit uf's.
 __device__ __forceinline__ int sk_slot(const Params& p, int t, int uf, int sg) {
     const int u = uf + sg;
+    if (p.tail_items == (p.num_tiles - p.dp_tiles) * p.split) return u;   // equal segments
     const int i = t - static_cast<int>(sk_start(p, u) / p.k_blocks);
     return u + i * p.tail_items;
 }
@@ -200,14 +201,35 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
     const bool ksplit = p.split > 1 && !p.tail_halves;
     const bool front = p.seg_first && ksplit && p.dp_tiles > 0;
     const int dp0 = front ? p.num_tiles - p.dp_tiles : 0;   // first whole tile
+    // Equal segments (tail_items = S * split, the default): 32-bit arithmetic
+    // only -- this runs on the MMA thread between tiles, where every cycle is
+    // tensor-pipe time.
+    const bool uniform = ksplit && p.tail_items == (p.num_tiles - p.dp_tiles) * p.split;
     long long g0 = 0, g1 = 0;
     int nsplit = 0;   // this unit's split items
     if (ksplit && unit < p.tail_items) {
-        g0 = sk_start(p, unit);
-        g1 = sk_start(p, unit + 1);
-        nsplit = static_cast<int>((g1 - 1) / p.k_blocks - g0 / p.k_blocks) + 1;
+        if (uniform) {
+            nsplit = 1;
+        } else {
+            g0 = sk_start(p, unit);
+            g1 = sk_start(p, unit + 1);
+            nsplit = static_cast<int>((g1 - 1) / p.k_blocks - g0 / p.k_blocks) + 1;
+        }
     }
     auto split_item = [&](int i) {
+        if (uniform) {
+            const int t = unit / p.split;
+            w.half = -1;
+            w.stile = t;
+            w.tile = (front ? 0 : p.dp_tiles) + t;
+            w.seg = unit - t * p.split;
+            w.kb0 = (w.seg * p.k_blocks) / p.split;
+            w.kb1 = ((w.seg + 1) * p.k_blocks) / p.split;
+            w.item = unit;
+            w.uf = t * p.split;
+            w.nseg = p.split;
+            return;
+        }
         const int t = static_cast<int>(g0 / p.k_blocks) + i;
         const long long base = static_cast<long long>(t) * p.k_blocks;
         w.half = -1;
@@ -790,13 +812,16 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 bool ok = true;
                 int local = 0;
                 Work w;
-                // The MMAs of one K slice (a pipeline stage) into accumulator d_tmem;
-                // `first` starts a fresh accumulation.
-                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc) {
+                // MMAs k0 .. k1 - 1 of one K slice (a pipeline stage, NK MMAs of
+                // 32 bytes of K each) into accumulator d_tmem; `first` starts a
+                // fresh accumulation.
+                constexpr int NK = CF::BK / CF::UMMA_K;
+                auto issue_mmas = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc, int k0, int k1) {
                     const uint64_t ad = a_desc0 + st * STAGE_STEP;
                     const uint64_t bd = b_desc0 + st * STAGE_STEP;
     #pragma unroll
-                    for (int k = 0; k < CF::BK / CF::UMMA_K; ++k) {
+                    for (int k = 0; k < NK; ++k) {
+                        if (k < k0 || k >= k1) continue;
                         const uint32_t acc = (!first || k > 0) ? 1u : 0u;
                         if constexpr (CF::PAIR) {
                             if constexpr (CF::FP8)
@@ -810,11 +835,17 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                 mma_bf16(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
                         }
                     }
-                    // the stage is free (in both CTAs of a pair) once these MMAs have read it
+                };
+                // the stage is free (in both CTAs of a pair) once its MMAs have read it
+                auto release_stage = [&](uint32_t st) {
                     if constexpr (CF::PAIR)
                         mma_commit_pair(&empty[st], 3);
                     else
                         mma_commit(&empty[st]);
+                };
+                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc) {
+                    issue_mmas(d_tmem, st, first, idesc, 0, NK);
+                    release_stage(st);
                 };
                 if constexpr (CF::GS) {
                     // Per-K-group scales: every scale group of every work item gets
@@ -878,12 +909,20 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     uint32_t d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                     // a tail half is one MMA of half the width
                     const uint32_t idesc_item = (CF::HALVES && w.half >= 0) ? CF::IDESC_HALF : CF::IDESC;
+                    // The wait for the next stage's operands (and the fence after
+                    // it) comes before this stage's last MMA, so it overlaps MMAs
+                    // already queued on the tensor core instead of running while
+                    // the tensor core's queue is empty.
+                    bool have_stage = false;   // full[stage] already waited for
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
-                            ok = false;
-                            break;
+                        if (!have_stage) {
+                            if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
                         }
-                        tc_fence_after();
+                        have_stage = false;
                         bool first_in_group = (kb == w.kb0);
                         if (kb == next_group_start) {
                             ++group;
@@ -891,11 +930,24 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
                             d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                         }
-                        issue_stage(d_tmem, stage, first_in_group, idesc_item);
-                        if (++stage == S) {
-                            stage = 0;
-                            phase ^= 1;
+                        issue_mmas(d_tmem, stage, first_in_group, idesc_item, 0, NK - 1);
+                        uint32_t nstage = stage + 1, nphase = phase;
+                        if (nstage == S) {
+                            nstage = 0;
+                            nphase ^= 1;
                         }
+                        if (kb + 1 < w.kb1) {
+                            if (!mbar_wait(&full[nstage], nphase, abort_flag, p.wait_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            have_stage = true;
+                        }
+                        issue_mmas(d_tmem, stage, first_in_group, idesc_item, NK - 1, NK);
+                        release_stage(stage);
+                        if (have_stage) tc_fence_after();
+                        stage = nstage;
+                        phase = nphase;
                     }
                     if (!ok) break;
                     // accumulator ready for the epilogue (of both CTAs of a pair)
