@@ -31,8 +31,7 @@ class Epilogue(ctypes.Structure):
 
 class Overrides(ctypes.Structure):
     _fields_ = [("tile_n", _i32), ("cta_pair", _i32), ("tail_split", _i32), ("tail_halves", _i32),
-                ("cluster_split", _i32), ("seg_first", _i32), ("tail_balance", _i32), ("raster_group", _i32),
-                ("cooperative", _i32),
+                ("cluster_split", _i32), ("seg_first", _i32), ("raster_group", _i32), ("cooperative", _i32),
                 ("wait_limit_ns", _i64), ("stall_after_loads", _i64)]
 
 

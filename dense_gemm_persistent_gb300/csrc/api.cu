@@ -46,7 +46,6 @@ void overrides_defaults(dgemm_overrides_t* o) {
     o->tail_halves = -1;
     o->cluster_split = -1;
     o->seg_first = -1;
-    o->tail_balance = -1;
     o->raster_group = 0;
     o->cooperative = -1;
     o->wait_limit_ns = 0;
@@ -76,7 +75,6 @@ void init_overrides() {
         o.tail_halves = env_int("DGEMM_TAIL_HALVES", -1);
         o.cluster_split = env_int("DGEMM_CLUSTER_SPLIT", -1);
         o.seg_first = env_int("DGEMM_SEG_FIRST", -1);
-        o.tail_balance = env_int("DGEMM_TAIL_BALANCE", -1);
         o.raster_group = env_int("DGEMM_RASTER_GROUP", 0);
         o.cooperative = env_int("DGEMM_COOPERATIVE", -1);
         if (const char* w = std::getenv("DGEMM_WAIT_LIMIT_NS")) o.wait_limit_ns = std::atoll(w);
@@ -140,21 +138,6 @@ int pair_ctas(int pair) { return pair ? 2 : 1; }
 // Split-K for grids that do not fill the GPU: K segments per tile so that
 // tiles x segments <= units, each segment at least 8 K slices, at most 4 (the
 // last-arriving warp sums the others' partials with all loads in flight).
-// Balanced K split of S tiles of kb K slices over us units (unit u takes the
-// slices [u * S * kb / us, (u + 1) * S * kb / us) of the tiles laid end to
-// end): the most units whose ranges cover one tile.
-int64_t sk_max_segments(int64_t S, int64_t kb, int64_t us) {
-    const int64_t T = S * kb;
-    int64_t worst = 0;
-    for (int64_t t = 0; t < S; ++t) {
-        const int64_t x0 = t * kb, x1 = x0 + kb - 1;
-        const int64_t uf = ((x0 + 1) * us + T - 1) / T - 1;
-        const int64_t ul = ((x1 + 1) * us + T - 1) / T - 1;
-        if (ul - uf + 1 > worst) worst = ul - uf + 1;
-    }
-    return worst;
-}
-
 int64_t underfill_split(int64_t tiles, int64_t units, int64_t k_blocks) {
     if (tiles <= 0 || tiles >= units) return 1;
     int64_t s = units / tiles;
@@ -354,18 +337,14 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.tail_count_bytes = 0;
     // workspace: status header, per-warp arrival counters, one FP32 partial
     // tile per unit
-    // (`items` units take the split tiles' K slices; a balanced split whose
-    // units may each end one tile and start the next needs two partial slots
-    // per unit)
     size_t split_bytes = 0;
-    auto use_split = [&](int dp_tiles, int split, int items, int slots_per_unit = 1) {
+    auto use_split = [&](int dp_tiles, int split, int items) {
         p.dp_tiles = dp_tiles;
         p.split = split;
         p.tail_items = items;
         p.pub.grid = pair_ctas(pair) * (items > units ? units : (dp_tiles > 0 ? units : items));
         p.tail_count_bytes = round_up(static_cast<size_t>(units) * pair_ctas(pair) * k->epi_warps * 8, 256);
-        split_bytes = p.tail_count_bytes + static_cast<size_t>(slots_per_unit) * static_cast<size_t>(units) *
-                                               pair_ctas(pair) * 128 * static_cast<size_t>(bn) * 4;
+        split_bytes = p.tail_count_bytes + static_cast<size_t>(units) * pair_ctas(pair) * 128 * static_cast<size_t>(bn) * 4;
         p.split_offset = kWsStatus;
         p.pub.workspace_bytes = kWsStatus + split_bytes;
     };
@@ -391,34 +370,11 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     } else if ((p.mode == dg::MODE_TILE || p.mode == dg::MODE_ROWQ) && split_ok && k_blocks > 0) {
         const int rem = p.pub.num_tiles % units;
         if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks >= kMinTailSlices)) {
-            if (p.mode == dg::MODE_TILE && !gs && ov.tail_balance == 1) {
-                // Balanced (override only): the rem tiles' K slices laid end to
-                // end and dealt out in equal ranges of at least 8 slices to as
-                // many units as that allows (all of them for long tiles), so
-                // that every unit ends within a fraction of a K slice of the
-                // others; a range may end one tile and start the next. A tile is
-                // covered by at most 15 ranges (4-bit arrival counts). Measured
-                // on 4096^3 BF16 (same GPU, 300-step runs): 1556-1559 TFLOP/s
-                // against 1631 for the two-way split below -- the finishing
-                // segment reads up to three full partial tiles through the
-                // SM's L2 port while its next tile's operands stream through
-                // it -- and on FP8 4096 x 11008 x 4096 2895-2921 against
-                // 3122-3126 with tail halves.
-                int64_t us = static_cast<int64_t>(rem) * k_blocks / 8;
-                if (us > units) us = units;
-                if (us > 14 * static_cast<int64_t>(rem)) us = 14 * static_cast<int64_t>(rem);
-                if (us > rem) {
-                    const bool uniform = us % rem == 0;
-                    use_split(p.pub.num_tiles - rem, static_cast<int>(sk_max_segments(rem, k_blocks, us)),
-                              static_cast<int>(us), uniform ? 1 : 2);
-                }
-            } else {
-                int64_t split64 = units / rem;
-                if (split64 > k_blocks / 8) split64 = k_blocks / 8;
-                if (split64 > 2) split64 = 2;   // a third or fourth partial costs more than it saves
-                const int split = static_cast<int>(split64);
-                if (split >= 2) use_split(p.pub.num_tiles - rem, split, rem * split);
-            }
+            int64_t split64 = units / rem;
+            if (split64 > k_blocks / 8) split64 = k_blocks / 8;
+            if (split64 > 2) split64 = 2;   // a third or fourth partial costs more than it saves
+            const int split = static_cast<int>(split64);
+            if (split >= 2) use_split(p.pub.num_tiles - rem, split, rem * split);
         }
         // N halves (CTA-pair 256-wide kernels) where the K split does not
         // apply: when twice the leftover tiles fit in the last wave, each runs
@@ -905,7 +861,7 @@ dgemm_status_t dgemm_set_overrides(const dgemm_overrides_t* o) {
     if (o) {
         if (o->tile_n < 0 || o->cta_pair < -1 || o->cta_pair > 1 || o->tail_split < -1 || o->tail_split > 1 ||
             o->tail_halves < -1 || o->tail_halves > 0 || o->cluster_split < -1 || o->cluster_split > 0 ||
-            o->seg_first < -1 || o->seg_first > 1 || o->tail_balance < -1 || o->tail_balance > 1 ||
+            o->seg_first < -1 || o->seg_first > 1 ||
             o->raster_group < 0 || o->cooperative < -1 ||
             o->cooperative > 1 || o->wait_limit_ns < 0 || o->stall_after_loads < -1)
             return DGEMM_ERR_INVALID_VALUE;

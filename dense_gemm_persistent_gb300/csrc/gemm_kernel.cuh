@@ -112,22 +112,19 @@ struct Params {
     // every CTA stops after issuing this many stage loads, so that the MMA's
     // wait for the next stage runs out and the kernel drains and returns.
     long long stall_after;
-    // Split tiles (all modes): tiles [0, dp_tiles) run whole; the K slices of
-    // the S = num_tiles - dp_tiles remaining tiles, S * k_blocks in tile order,
-    // are dealt out to the first tail_items units as contiguous ranges (unit u
-    // takes [g(u), g(u + 1)), g(u) = u * S * k_blocks / tail_items), run before
-    // the unit's whole tiles with seg_first (the split tiles are then the
-    // first S of the raster instead of the last). With tail_items = S * split
-    // every tile is cut into `split` equal segments; otherwise a range may end
-    // one tile and start the next (two work items), and a tile has a varying
-    // number of segments (at most 15). `split` > 1 marks a K-split plan.
+    // Split tiles (all modes): tiles [0, dp_tiles) run whole; each of the
+    // remaining tiles is split along K into `split` segments (tail_items in
+    // all), every unit taking at most one (before its whole tiles, if any;
+    // with seg_first the split tiles are the first num_tiles - dp_tiles of the
+    // raster instead of the last).
     // 32-column unit u of each epilogue warp's region belongs to segment
-    // u % (its tile's segments) in the symmetric exchange (split_sym).
+    // u % split: a segment parks the units others own as FP32 partials in
+    // `partials`, counts its arrival in tail_count, waits (bounded) for every
+    // segment of the region, and finishes its own units from its accumulator
+    // plus the others' partials.
     int dp_tiles, split, tail_items;
     int seg_first;           // 1: a unit runs its split item before its whole tiles
-    // [slot][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4; the i-th item
-    // (0 or 1) of unit u parks in slot u + i * tail_items
-    float* partials;
+    float* partials;         // [tail_items][CTAS][EPI_WARPS][units][UNIT/4][32 lanes] float4
     // Split-K through distributed shared memory (single-CTA kernels, under-
     // filled grids): the split K segments of a tile are the CTAs of one
     // cluster of `split` CTAs (rank = segment); partials go through the idle
@@ -152,101 +149,34 @@ struct Params {
 
 // One unit of work: a whole tile (item < 0) or one K segment of a split tile.
 struct Work {
-    int tile, kb0, kb1, item;   // item: the segment's partial slot
+    int tile, kb0, kb1, item;
     int half;   // -1: the whole tile; 0 / 1: that 128-column half (tail_halves)
-    // K segments: the split tile's index among the split tiles, this
-    // segment's index within the tile, the tile's segment count and the unit
-    // that runs its first segment
-    int stile, seg, nseg, uf;
 };
 
-// Start of unit u's range of split-tile K slices (see Params::tail_items).
-__device__ __forceinline__ long long sk_start(const Params& p, int u) {
-    const long long T = static_cast<long long>(p.num_tiles - p.dp_tiles) * p.k_blocks;
-    return static_cast<long long>(u) * T / p.tail_items;
-}
-
-// The units whose ranges cover split tile t: the first, and how many. The
-// first is the largest u with sk_start(u) <= t * k_blocks, i.e.
-// ceil((x + 1) * tail_items / T) - 1 for x = t * k_blocks.
-__device__ __forceinline__ void sk_span(const Params& p, int t, int& uf, int& n) {
-    const long long T = static_cast<long long>(p.num_tiles - p.dp_tiles) * p.k_blocks;
-    const long long U = p.tail_items;
-    const long long x0 = static_cast<long long>(t) * p.k_blocks;
-    const long long x1 = x0 + p.k_blocks - 1;
-    uf = static_cast<int>(((x0 + 1) * U + T - 1) / T - 1);
-    const int ul = static_cast<int>(((x1 + 1) * U + T - 1) / T - 1);
-    n = ul - uf + 1;
-}
-
-// Partial slot of segment sg of split tile t whose first segment is unit uf's.
-__device__ __forceinline__ int sk_slot(const Params& p, int t, int uf, int sg) {
-    const int u = uf + sg;
-    if (p.tail_items == (p.num_tiles - p.dp_tiles) * p.split) return u;   // equal segments
-    const int i = t - static_cast<int>(sk_start(p, u) / p.k_blocks);
-    return u + i * p.tail_items;
-}
-
 // The iter-th work item of a unit (a CTA, or a CTA pair): its whole tiles
-// unit, unit + units, ... (dp_tiles of them in all), then its split items (K
-// segments, one or two) or its tail half, or with seg_first its K segments
-// first.
+// unit, unit + units, ... (dp_tiles of them in all), then its tail item (a K
+// segment or an N half of a split tile), or with seg_first its K segment first.
 __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, int iter, Work& w) {
-    // With seg_first, a unit's K segments of split tiles run before its whole
+    // With seg_first, a unit's K segment of a split tile runs before its whole
     // tiles, so that the segments' exchange of partial sums (a chain of L2 round
     // trips) overlaps the next tile's mainloop instead of ending the kernel.
-    // Every segment of a split tile then runs at the start of the kernel, and
-    // the split tiles are the raster's first ones (tiles [0, S), whole tiles
-    // from S on), next to the whole tiles started alongside them.
-    const bool ksplit = p.split > 1 && !p.tail_halves;
-    const bool front = p.seg_first && ksplit && p.dp_tiles > 0;
+    // Every segment of a split tile is then its unit's first item, all running
+    // at once, and the split tiles are the raster's first ones (tiles [0, S),
+    // whole tiles from S on), next to the whole tiles started alongside them.
+    const bool front = p.seg_first && p.split > 1 && !p.tail_halves && p.dp_tiles > 0;
+    const bool seg_first = front && unit < p.tail_items;
     const int dp0 = front ? p.num_tiles - p.dp_tiles : 0;   // first whole tile
-    // Equal segments (tail_items = S * split, the default): 32-bit arithmetic
-    // only -- this runs on the MMA thread between tiles, where every cycle is
-    // tensor-pipe time.
-    const bool uniform = ksplit && p.tail_items == (p.num_tiles - p.dp_tiles) * p.split;
-    long long g0 = 0, g1 = 0;
-    int nsplit = 0;   // this unit's split items
-    if (ksplit && unit < p.tail_items) {
-        if (uniform) {
-            nsplit = 1;
-        } else {
-            g0 = sk_start(p, unit);
-            g1 = sk_start(p, unit + 1);
-            nsplit = static_cast<int>((g1 - 1) / p.k_blocks - g0 / p.k_blocks) + 1;
-        }
-    }
-    auto split_item = [&](int i) {
-        if (uniform) {
-            const int t = unit / p.split;
+    if (seg_first) {
+        if (iter == 0) {
+            const int seg = unit % p.split;
             w.half = -1;
-            w.stile = t;
-            w.tile = (front ? 0 : p.dp_tiles) + t;
-            w.seg = unit - t * p.split;
-            w.kb0 = (w.seg * p.k_blocks) / p.split;
-            w.kb1 = ((w.seg + 1) * p.k_blocks) / p.split;
+            w.tile = unit / p.split;
+            w.kb0 = (seg * p.k_blocks) / p.split;
+            w.kb1 = ((seg + 1) * p.k_blocks) / p.split;
             w.item = unit;
-            w.uf = t * p.split;
-            w.nseg = p.split;
-            return;
-        }
-        const int t = static_cast<int>(g0 / p.k_blocks) + i;
-        const long long base = static_cast<long long>(t) * p.k_blocks;
-        w.half = -1;
-        w.stile = t;
-        w.tile = (front ? 0 : p.dp_tiles) + t;
-        w.kb0 = static_cast<int>((g0 > base ? g0 : base) - base);
-        w.kb1 = static_cast<int>((g1 < base + p.k_blocks ? g1 : base + p.k_blocks) - base);
-        w.item = unit + i * p.tail_items;
-        sk_span(p, t, w.uf, w.nseg);
-        w.seg = unit - w.uf;
-    };
-    if (front) {
-        if (iter < nsplit) {
-            split_item(iter);
             return true;
         }
-        iter -= nsplit;
+        --iter;
     }
     const int dp_count = p.dp_tiles > unit ? (p.dp_tiles - unit + units - 1) / units : 0;
     w.half = -1;
@@ -257,11 +187,10 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
         w.item = -1;
         return true;
     }
-    if (front) return false;   // its split items ran first
-    iter -= dp_count;
+    if (seg_first) return false;   // its split item ran first
+    const int j = unit + (iter - dp_count) * units;
+    if (j >= p.tail_items) return false;
     if (p.tail_halves) {
-        const int j = unit + iter * units;
-        if (j >= p.tail_items) return false;
         w.tile = p.dp_tiles + j / 2;
         w.half = j % 2;
         w.kb0 = 0;
@@ -269,12 +198,14 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
         w.item = -1;
         return true;
     }
-    if (iter < nsplit) {
-        split_item(iter);
-        return true;
-    }
-    return false;
+    const int seg = j % p.split;
+    w.tile = p.dp_tiles + j / p.split;
+    w.kb0 = (seg * p.k_blocks) / p.split;
+    w.kb1 = ((seg + 1) * p.k_blocks) / p.split;
+    w.item = j;
+    return true;
 }
+
 
 
 template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false, bool GS_ = false>
@@ -812,16 +743,13 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 bool ok = true;
                 int local = 0;
                 Work w;
-                // MMAs k0 .. k1 - 1 of one K slice (a pipeline stage, NK MMAs of
-                // 32 bytes of K each) into accumulator d_tmem; `first` starts a
-                // fresh accumulation.
-                constexpr int NK = CF::BK / CF::UMMA_K;
-                auto issue_mmas = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc, int k0, int k1) {
+                // The MMAs of one K slice (a pipeline stage) into accumulator d_tmem;
+                // `first` starts a fresh accumulation.
+                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc) {
                     const uint64_t ad = a_desc0 + st * STAGE_STEP;
                     const uint64_t bd = b_desc0 + st * STAGE_STEP;
     #pragma unroll
-                    for (int k = 0; k < NK; ++k) {
-                        if (k < k0 || k >= k1) continue;
+                    for (int k = 0; k < CF::BK / CF::UMMA_K; ++k) {
                         const uint32_t acc = (!first || k > 0) ? 1u : 0u;
                         if constexpr (CF::PAIR) {
                             if constexpr (CF::FP8)
@@ -835,17 +763,11 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                 mma_bf16(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
                         }
                     }
-                };
-                // the stage is free (in both CTAs of a pair) once its MMAs have read it
-                auto release_stage = [&](uint32_t st) {
+                    // the stage is free (in both CTAs of a pair) once these MMAs have read it
                     if constexpr (CF::PAIR)
                         mma_commit_pair(&empty[st], 3);
                     else
                         mma_commit(&empty[st]);
-                };
-                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc) {
-                    issue_mmas(d_tmem, st, first, idesc, 0, NK);
-                    release_stage(st);
                 };
                 if constexpr (CF::GS) {
                     // Per-K-group scales: every scale group of every work item gets
@@ -909,20 +831,12 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     uint32_t d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                     // a tail half is one MMA of half the width
                     const uint32_t idesc_item = (CF::HALVES && w.half >= 0) ? CF::IDESC_HALF : CF::IDESC;
-                    // The wait for the next stage's operands (and the fence after
-                    // it) comes before this stage's last MMA, so it overlaps MMAs
-                    // already queued on the tensor core instead of running while
-                    // the tensor core's queue is empty.
-                    bool have_stage = false;   // full[stage] already waited for
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                        if (!have_stage) {
-                            if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
+                        if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
+                            ok = false;
+                            break;
                         }
-                        have_stage = false;
+                        tc_fence_after();
                         bool first_in_group = (kb == w.kb0);
                         if (kb == next_group_start) {
                             ++group;
@@ -930,24 +844,11 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
                             d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                         }
-                        issue_mmas(d_tmem, stage, first_in_group, idesc_item, 0, NK - 1);
-                        uint32_t nstage = stage + 1, nphase = phase;
-                        if (nstage == S) {
-                            nstage = 0;
-                            nphase ^= 1;
+                        issue_stage(d_tmem, stage, first_in_group, idesc_item);
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1;
                         }
-                        if (kb + 1 < w.kb1) {
-                            if (!mbar_wait(&full[nstage], nphase, abort_flag, p.wait_ns)) {
-                                ok = false;
-                                break;
-                            }
-                            have_stage = true;
-                        }
-                        issue_mmas(d_tmem, stage, first_in_group, idesc_item, NK - 1, NK);
-                        release_stage(stage);
-                        if (have_stage) tc_fence_after();
-                        stage = nstage;
-                        phase = nphase;
                     }
                     if (!ok) break;
                     // accumulator ready for the epilogue (of both CTAs of a pair)
@@ -1384,9 +1285,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // stores them directly: about one round trip through L2 per segment
             // instead of a single warp reading every partial unit by unit.
             // Otherwise the last segment to arrive finishes the region (below).
-            const int seg = part ? w.seg : 0;
-            const int nseg = part ? w.nseg : 1;   // the tile's segments
-            auto owner = [&](int u) { return u % nseg; };
+            const int item0 = part ? (w.item / p.split) * p.split : 0;
+            const int seg = part ? w.item - item0 : 0;
+            auto owner = [&](int u) { return u % p.split; };
             // generic writes to buffers the TMA (async proxy) filled
             if (part && p.cluster_split) fence_proxy_async_smem();
             const bool unit_pass = !part || p.cluster_split || p.split_sym;
@@ -1454,10 +1355,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 #pragma unroll
                             for (int o = 0; o < 3; ++o) {
                                 const int peer = o + (o >= seg ? 1 : 0);
-                                const uint32_t base = peer < nseg ? mapa_shared(mine, static_cast<uint32_t>(peer)) : 0u;
+                                const uint32_t base = peer < p.split ? mapa_shared(mine, static_cast<uint32_t>(peer)) : 0u;
 #pragma unroll
                                 for (int j = 0; j < UNIT_F4; ++j)
-                                    f[o][j] = peer < nseg ? ld_shared_cluster_f4(base + 16u * 32u * j)
+                                    f[o][j] = peer < p.split ? ld_shared_cluster_f4(base + 16u * 32u * j)
                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
 #pragma unroll
@@ -1480,7 +1381,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     // (launch epoch << 8) | (segments parked << 4) | arrivals; a word
                     // left by any earlier launch counts as zero of each.
                     unsigned long long* cnt =
-                        p.tail_count + (static_cast<int64_t>(w.stile) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
+                        p.tail_count + ((w.item / p.split) * CF::CTAS + rank) * CF::EPI_WARPS + ew;
                     // lane 0: counts this segment in; returns how many had arrived
                     // before it, or -1 if the word could not be updated.
                     auto arrive = [&]() -> int {
@@ -1505,33 +1406,30 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         }
                         return 1u;
                     };
-                    // v += the other segments' partials of unit u, three
-                    // segments' loads in flight at a time
-                    const int64_t uoff = ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS) * (UNIT_F4 * 32) + lane;
+                    // v += the other segments' partials of unit u, all loads in flight together
                     auto add_partials = [&](int u, float (&v)[32]) {
-                        const float4* src = reinterpret_cast<const float4*>(p.partials) + uoff + u * (UNIT_F4 * 32);
-                        for (int o0 = 0; o0 < nseg - 1; o0 += 3) {
-                            float4 f[3][UNIT_F4];
+                        const float4* src = reinterpret_cast<const float4*>(p.partials) + item0 * ITEM_F4 +
+                                            ((static_cast<int64_t>(rank) * CF::EPI_WARPS + ew) * NUNITS + u) *
+                                                (UNIT_F4 * 32) +
+                                            lane;
+                        float4 f[3][UNIT_F4];
 #pragma unroll
-                            for (int o = 0; o < 3; ++o) {
-                                const int k = o0 + o;
-                                const int sgi = k + (k >= seg ? 1 : 0);
-                                const int64_t slot = k < nseg - 1 ? sk_slot(p, w.stile, w.uf, sgi) : 0;
+                        for (int o = 0; o < 3; ++o) {
+                            const int sgi = o + (o >= seg ? 1 : 0);
 #pragma unroll
-                                for (int j = 0; j < UNIT_F4; ++j)
-                                    f[o][j] = k < nseg - 1 ? __ldcg(src + slot * ITEM_F4 + 32 * j)
-                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-#pragma unroll
-                            for (int o = 0; o < 3; ++o)
-#pragma unroll
-                                for (int j = 0; j < UNIT_F4; ++j) {
-                                    v[4 * j] += f[o][j].x;
-                                    v[4 * j + 1] += f[o][j].y;
-                                    v[4 * j + 2] += f[o][j].z;
-                                    v[4 * j + 3] += f[o][j].w;
-                                }
+                            for (int j = 0; j < UNIT_F4; ++j)
+                                f[o][j] = sgi < p.split ? __ldcg(src + sgi * ITEM_F4 + 32 * j)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
+#pragma unroll
+                        for (int o = 0; o < 3; ++o)
+#pragma unroll
+                            for (int j = 0; j < UNIT_F4; ++j) {
+                                v[4 * j] += f[o][j].x;
+                                v[4 * j + 1] += f[o][j].y;
+                                v[4 * j + 2] += f[o][j].z;
+                                v[4 * j + 3] += f[o][j].w;
+                            }
                     };
                     if (p.split_sym) {
                         // Every segment of the tile is resident (cooperative launch):
@@ -1549,7 +1447,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             if (before < 0) {
                                 record_error(p, ERR_ARRIVAL);
                             } else if (owns) {
-                                const unsigned long long want = (p.epoch << 8) | static_cast<unsigned long long>(nseg);
+                                const unsigned long long want = (p.epoch << 8) | static_cast<unsigned long long>(p.split);
                                 ready = await([&](unsigned long long x) { return x == want; });
                                 __threadfence();
                             } else {
@@ -1585,7 +1483,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         if (before < 0) {
                             if (lane == 0) record_error(p, ERR_ARRIVAL);
                             ok = false;
-                        } else if (before < nseg - 1) {
+                        } else if (before < p.split - 1) {
 #pragma unroll U_UNROLL
                             for (int u = 0; u < NUNITS; ++u) {
                                 float v[32];
@@ -1604,7 +1502,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         } else {
                             unsigned ready = 0;
                             if (lane == 0) {
-                                const unsigned long long want = static_cast<unsigned long long>(nseg - 1);
+                                const unsigned long long want = static_cast<unsigned long long>(p.split - 1);
                                 ready = await([&](unsigned long long x) {
                                     return (x >> 8) == p.epoch && ((x >> 4) & 0xFull) == want;
                                 });

@@ -140,8 +140,7 @@ typedef struct {
                               run first, as the raster's first tiles, and their
                               partial sums are exchanged while whole tiles
                               run; otherwise they run last                    */
-    int tail_split;        /* K segments per tail tile, the most of any tile
-                              (1 = no splitting)                                */
+    int tail_split;        /* K segments per tail tile (1 = no splitting)       */
     int cluster_split;     /* 1: the K segments of each split tile run as one
                               thread-block cluster and are summed through
                               distributed shared memory (no workspace needed) */
@@ -149,10 +148,7 @@ typedef struct {
                               tile_n / 2 columns each, every half over the
                               whole K range (no workspace needed)            */
     int tail_units;        /* units (CTAs or CTA pairs) that run the tail's
-                              segments or halves (0 = none). A K-split tail of
-                              the plain form deals the tail tiles' K slices
-                              out evenly to these units, so a unit may finish
-                              one tile's last slices and the next tile's first */
+                              K segments or halves, one each (0 = none)        */
     size_t smem_bytes;     /* dynamic shared memory per CTA                     */
     size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
 } dgemm_plan_t;
@@ -287,12 +283,6 @@ typedef struct {
                             (DGEMM_CLUSTER_SPLIT)                                   */
     int seg_first;       /* -1; 0: split segments after the whole tiles
                             (DGEMM_SEG_FIRST)                                       */
-    int tail_balance;    /* -1 or 0: split the plain form's tail tiles into two
-                            equal K halves each; 1: deal their K slices out in
-                            equal ranges to every unit (a unit may finish one
-                            tile and start the next; measured slower on 4096^3:
-                            the larger exchange of partials competes with the
-                            operand feed) (DGEMM_TAIL_BALANCE)                     */
     int raster_group;    /* 0; else tile rows per band of the raster (DGEMM_RASTER_GROUP) */
     int cooperative;     /* -1; 0: launch nothing cooperatively (for profilers that
                             cannot launch cooperative cluster grids: the

@@ -38,7 +38,6 @@ _KNOB_VALUES = {
     "tail_halves": lambda v: -1 if str(v) == "1" else int(v),     # "0": off
     "cluster_split": lambda v: -1 if str(v) == "1" else int(v),   # "0": through the workspace
     "seg_first": lambda v: int(v),                            # "0": segments last, "1": first
-    "tail_balance": lambda v: int(v),                         # "1": K slices dealt out to every unit
 }
 
 

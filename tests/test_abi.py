@@ -105,13 +105,6 @@ def test_workspace_sizes(lib, knobs):
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p["tail_tiles"], p["tail_units"], p["tail_split"]) == (28, 56, 2)
     assert p["workspace_bytes"] == 256 + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 76 * 2 * 128 * 256 * 4
-    # with the K slices dealt out to every pair instead, a pair may finish one
-    # tile and start the next: two partial slots per pair
-    knobs(tail_balance="1")
-    p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
-    assert (p["tail_tiles"], p["tail_units"], p["tail_split"]) == (28, 76, 4)
-    assert p["workspace_bytes"] == 256 + 256 * ((76 * 2 * 8 * 8 + 255) // 256) + 2 * 76 * 2 * 128 * 256 * 4
-    knobs(tail_balance=None)
     # FP8 4096 x 11008 x 4096 has 32 K slices per tile: too short to split along
     # K; its 4 leftover tiles run as 8 N halves instead, with no workspace
     p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
@@ -175,7 +168,7 @@ def test_split_exchange_launch_modes(lib, knobs):
 def test_overrides_validation_and_defaults(lib):
     d = dg.get_overrides()
     assert d == {"tile_n": 0, "cta_pair": -1, "tail_split": -1, "tail_halves": -1, "cluster_split": -1,
-                 "seg_first": -1, "tail_balance": -1, "raster_group": 0, "cooperative": -1, "wait_limit_ns": 0,
+                 "seg_first": -1, "raster_group": 0, "cooperative": -1, "wait_limit_ns": 0,
                  "stall_after_loads": -1}
     for bad in ({"cta_pair": 2}, {"tail_halves": 1}, {"cooperative": -2}, {"wait_limit_ns": -1},
                 {"stall_after_loads": -5}, {"tile_n": -64}):

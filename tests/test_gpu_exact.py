@@ -303,54 +303,43 @@ def sampled_rows(M, tile_m, seed):
     return np.array(sorted(pick), dtype=np.int64)
 
 
-def balanced_case(M, N, K, layout, fp8, seed):
-    """Integer operands (exact in FP32), FP32 output, checked bit-exact on a row
-    of every tile row: every split tile's segments are covered."""
-    rng = np.random.default_rng(seed)
-    mk = int_e4m3 if fp8 else int_bf16
-    A = mk(rng, (M, K))
-    B = mk(rng, (K, N) if layout == "kn" else (N, K))
+@pytest.mark.parametrize("case", ["tail_split_plain", "underfill_split_cooperative"])
+def test_split_tiles_while_another_stream_holds_the_sms(case, knobs):
+    """A split-tile GEMM launched while a large GEMM on another stream still
+    occupies every SM, so its CTAs become resident a few at a time as the
+    other kernel's CTAs leave. The tail split's plain launch never lets a
+    segment wait for one that has not started; the cooperative launch of the
+    under-filled split-K waits until its whole grid fits. Both must finish,
+    bit-exact, with a clean status."""
+    rng = np.random.default_rng(1500)
+    # the occupying GEMM: 8192^3 BF16 (every SM busy for ~0.6 ms), on a side stream
+    Ab = torch.randn(8192, 8192, device=dev()).to(torch.bfloat16)
+    Bb = torch.randn(8192, 8192, device=dev()).to(torch.bfloat16)
+    Db = torch.empty(8192, 8192, dtype=torch.bfloat16, device=dev())
+    wsb = workspace(0, 8192, 8192, 8192, "nk")
+    side = torch.cuda.Stream()
+    if case == "tail_split_plain":
+        M, N, K, layout = 4096, 4096, 4096, "kn"
+    else:
+        knobs(cluster_split="0")
+        M, N, K, layout = 1024, 1024, 4096, "nk"
+    plan = dg.dgemm_plan(0, M, N, K, layout, "f32", num_sms=0)
+    assert plan["tail_split"] >= 2 and plan["cluster_split"] == 0
+    assert plan["cooperative"] == (0 if case == "tail_split_plain" else 1)
+    A = int_bf16(rng, (M, K))
+    B = int_bf16(rng, (K, N) if layout == "kn" else (N, K))
+    Ad, Bd = A.to(dev()), B.to(dev())
     D = torch.empty(M, N, dtype=torch.float32, device=dev())
-    ws = workspace(fp8, M, N, K, layout)
-    if fp8:
-        ones_m, ones_n = torch.ones(M, device=dev()), torch.ones(N, device=dev())
-        dg.dgemm_fp8_scaled(A.to(dev()), B.to(dev()), ones_m, ones_n, D, b_layout=layout, ws=ws)
-    else:
-        dg.dgemm_bf16(A.to(dev()), B.to(dev()), D, b_layout=layout, ws=ws)
-    assert status_ok(ws)
-    plan = dg.dgemm_plan(fp8, M, N, K, layout, "f32", num_sms=0)
-    rows = sampled_rows(M, plan["tile_m"], seed)
-    if fp8:
-        ref = oracle.fp8_gemm_ref(wl.codes_u8(A), wl.codes_u8(B), layout, np.ones(M, np.float32),
-                                  np.ones(N, np.float32), rows=rows)
-    else:
-        ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), layout, rows=rows)
+    ws = workspace(0, M, N, K, layout)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                dg.dgemm_bf16(Ab, Bb, Db, b_layout="nk", ws=wsb, stream=side)
+        dg.dgemm_bf16(Ad, Bd, D, b_layout=layout, ws=ws)
+    torch.cuda.synchronize()
+    assert status_ok(ws) and status_ok(wsb, stream=side)
+    rows = sampled_rows(M, plan["tile_m"], 1500)
+    ref = oracle.bf16_gemm_ref(wl.bits_u16(A), wl.bits_u16(B), layout, rows=rows)
     got = D.cpu().double().numpy()[rows]
-    return got, ref, plan
-
-
-@pytest.mark.parametrize("protocol", ["plain", "cooperative"])
-@pytest.mark.parametrize("seg_first", ["1", "0"])
-@pytest.mark.parametrize("shape,layout,fp8,pair", [
-    ((4096, 4096, 4096), "kn", 0, None),     # the 4096^3 plan: 28 tiles over 76 pairs, up to 4 segments
-    ((512, 11008, 4096), "nk", 0, None),     # 10 leftover pair tiles over 76 pairs
-    ((1280, 4096, 4160), "kn", 0, "0"),      # single-CTA tiles: 8 leftover tiles over 65 CTAs
-    ((4096, 11008, 6400), "nk", 1, None),    # FP8: 4 leftover tiles of 50 K slices over 25 pairs
-])
-def test_balanced_tail_split_exact(shape, layout, fp8, pair, seg_first, protocol, knobs):
-    """The last partial wave's tiles, their K slices laid end to end and dealt
-    out in equal ranges, so that a unit may finish one tile and start the next
-    and a tile has a varying number of segments: bit-exact, with the segments
-    run first or last, in a plain launch (the last segment to arrive finishes
-    the tile) and a cooperative one (every segment finishes its own units)."""
-    knobs(seg_first=seg_first, tail_balance="1")
-    if pair is not None:
-        knobs(cta_pair=pair)
-    if protocol == "cooperative":
-        knobs(cooperative="1")
-    M, N, K = shape
-    got, ref, plan = balanced_case(M, N, K, layout, fp8, seed=1300 + K + M)
-    assert plan["tail_split"] >= 2 and plan["tail_units"] > plan["tail_tiles"]
-    assert plan["tail_units"] % plan["tail_tiles"] != 0          # uneven segments
-    assert plan["cooperative"] == (1 if protocol == "cooperative" else 0)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
