@@ -549,7 +549,9 @@ __device__ __forceinline__ void tile_store_unit(const float (&v)[32], const Para
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tmD, box, f32_out ? col0 : col0 - 32, row_base);
+            // outputs (and the requantising stash) are not read again before
+            // they leave L2: let them go first, ahead of the evict-last operands
+            tma_store_2d_hint(tmD, box, f32_out ? col0 : col0 - 32, row_base, policy_evict_first());
             bulk_commit();
         }
         ++stores;
@@ -965,7 +967,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < RQ_CHUNK / 256; ++i) {
                 const int g = lane + 32 * i;
-                y[i] = g < len8 ? __ldcg(src + g) : make_uint4(0u, 0u, 0u, 0u);
+                y[i] = g < len8 ? __ldcs(src + g) : make_uint4(0u, 0u, 0u, 0u);   // last use
             }
 #pragma unroll
             for (int i = 0; i < RQ_CHUNK / 256; ++i) {
@@ -975,7 +977,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     const uint32_t w1 = pack_e4m3x2(bf16_lo(y[i].y) * inv, bf16_hi(y[i].y) * inv);
                     const uint32_t w2 = pack_e4m3x2(bf16_lo(y[i].z) * inv, bf16_hi(y[i].z) * inv);
                     const uint32_t w3 = pack_e4m3x2(bf16_lo(y[i].w) * inv, bf16_hi(y[i].w) * inv);
-                    dst[g] = make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));
+                    __stcs(dst + g, make_uint2(w0 | (w1 << 16), w2 | (w3 << 16)));
                 }
             }
         };
