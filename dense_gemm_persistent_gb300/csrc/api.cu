@@ -290,6 +290,33 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
                 pair = c.pair;
             }
         }
+        // At most one wave of single-CTA tiles: the time is the operand bytes
+        // each CTA streams (128-byte K slices of its 128 A rows and bn B rows,
+        // ~150 GB/s per SM) plus the partial sums its K segments exchange,
+        // which move ~4x slower per byte through distributed shared memory
+        // (~8x through the workspace). Measured on 1024 x 1024 x 4096: BF16
+        // 128 x 256 in 4 segments 16.5 us = 128 x 128 in 2 segments 16.4 us
+        // (equal modelled costs); FP8 14.1 us against 11.9 us (the second
+        // modelled cheaper), which the wave model above misorders.
+        const int64_t tiles_w = ((M + 127) / 128) * ((N + bn - 1) / bn);
+        if (!pair && p.mode == dg::MODE_TILE && tiles_w <= num_sms) {
+            double best_t = 1e300;
+            for (const Cand& c : cands) {
+                if (c.pair || (fp8 && p.b_mn && c.bn < 128)) continue;
+                const int64_t tiles = ((M + 127) / 128) * ((N + c.bn - 1) / c.bn);
+                if (tiles > num_sms) continue;
+                const int64_t sk = split_ok ? underfill_split(tiles, num_sms, kb_all) : 1;
+                const bool cl = cluster_ok && (sk == 2 || sk == 4) && tiles <= (sk == 2 ? max_pairs : max_quads);
+                const double stream = static_cast<double>(128 + c.bn) * static_cast<double>((kb_all + sk - 1) / sk) * 128.0;
+                const double xchg = sk > 1 ? 128.0 * c.bn * 4.0 * static_cast<double>(sk - 1) / static_cast<double>(sk) *
+                                                 (cl ? 4.0 : 8.0)
+                                           : 0.0;
+                if (stream + xchg < best_t) {
+                    best_t = stream + xchg;
+                    bn = c.bn;
+                }
+            }
+        }
     }
     // The tile width override applies when such a variant exists (tests reach
     // every variant with it; tuning sweeps).
