@@ -282,3 +282,20 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     assert int(code) == 1 and text == dg.dgemm_status_string(1)   # DGEMM_ERR_INVALID_VALUE
     assert lines["override"] == "0 0 128 1" and lines["restored"] == "256"
     assert int(lines["query"]) in (0, 5)        # DGEMM_OK on a GPU machine, DGEMM_ERR_CUDA without a device
+
+
+def test_underfilled_plans_by_streamed_and_exchanged_bytes(lib):
+    """Under one wave of single-CTA tiles the tile width follows the bytes each
+    CTA streams plus 4x the partial sums its K segments exchange in a cluster:
+    FP8 1024^2 x 4096 takes 128-wide tiles in two segments (streamed 512 KB +
+    exchanged 32 KB per CTA, against 384 KB + 96 KB for 256-wide tiles in four),
+    BF16 keeps 128 x 256 in four (the two cost the same there); full-wave plans
+    are unchanged."""
+    p = dg.dgemm_plan(1, 1024, 1024, 4096, "nk", "bf16", num_sms=152)
+    assert (p["tile_n"], p["cta_group"], p["tail_split"], p["cluster_split"]) == (128, 1, 2, 1)
+    p = dg.dgemm_plan(0, 1024, 1024, 4096, "nk", "bf16", num_sms=152)
+    assert (p["tile_n"], p["cta_group"], p["tail_split"], p["cluster_split"]) == (256, 1, 4, 1)
+    p = dg.dgemm_plan(0, 512, 512, 4096, "nk", "bf16", num_sms=152)
+    assert (p["tile_n"], p["tail_split"]) == (64, 4)
+    p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
+    assert (p["tile_n"], p["cta_group"]) == (256, 2)
