@@ -32,14 +32,14 @@ class Epilogue(ctypes.Structure):
 class Overrides(ctypes.Structure):
     _fields_ = [("tile_n", _i32), ("cta_pair", _i32), ("tail_split", _i32), ("tail_halves", _i32),
                 ("cluster_split", _i32), ("seg_first", _i32), ("raster_group", _i32), ("cooperative", _i32),
-                ("wait_limit_ns", _i64), ("stall_after_loads", _i64)]
+                ("kslices", _i32), ("wait_limit_ns", _i64), ("stall_after_loads", _i64)]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("swap_ab", _i32), ("tile_m", _i32), ("tile_n", _i32), ("cta_group", _i32), ("stages", _i32),
                 ("num_tiles", _i32), ("grid", _i32), ("cooperative", _i32), ("raster_group", _i32), ("k_groups", _i32),
                 ("tail_tiles", _i32), ("tail_split", _i32), ("cluster_split", _i32),
-                ("tail_halves", _i32), ("tail_units", _i32),
+                ("tail_halves", _i32), ("tail_units", _i32), ("k_slices", _i32),
                 ("smem_bytes", _sz), ("workspace_bytes", _sz)]
 
 

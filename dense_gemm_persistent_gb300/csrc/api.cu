@@ -48,6 +48,7 @@ void overrides_defaults(dgemm_overrides_t* o) {
     o->seg_first = -1;
     o->raster_group = 0;
     o->cooperative = -1;
+    o->kslices = -1;
     o->wait_limit_ns = 0;
     o->stall_after_loads = -1;
 }
@@ -77,6 +78,7 @@ void init_overrides() {
         o.seg_first = env_int("DGEMM_SEG_FIRST", -1);
         o.raster_group = env_int("DGEMM_RASTER_GROUP", 0);
         o.cooperative = env_int("DGEMM_COOPERATIVE", -1);
+        o.kslices = env_int("DGEMM_KSLICES", -1);
         if (const char* w = std::getenv("DGEMM_WAIT_LIMIT_NS")) o.wait_limit_ns = std::atoll(w);
     }
     std::lock_guard<std::mutex> lk(g_ovr_mutex);
@@ -116,12 +118,12 @@ void collect_kernels() {
     for (int i = 0; i < n3 && g_nk < 64; ++i) g_kernels[g_nk++] = &t3[i];
 }
 
-int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode, int pair, int gs) {
+int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode, int pair, int gs, int ks = 1) {
     std::call_once(g_kernels_once, collect_kernels);
     for (int i = 0; i < g_nk; ++i) {
         const dg::KernelInfo* k = g_kernels[i];
         if (k->bn == bn && k->fp8 == fp8 && k->a_mn == a_mn && k->b_mn == b_mn && k->mode == mode &&
-            k->pair == pair && k->gs == gs)
+            k->pair == pair && k->gs == gs && k->ks == ks)
             return i;
     }
     return -1;
@@ -193,6 +195,8 @@ struct Plan {
     int a_mn, b_mn;
     int64_t Mm, Nm;    // problem in the MMA's orientation
     int bk;            // K elements per stage
+    int ks;            // K slices (128 bytes of K) per stage: 2 = operands in 3-D TMA copies
+    int slice_k;       // K elements per slice
     int acc_stride;    // TMEM columns between the two accumulator buffers
     int gs;            // per-K-group scales (group_kb K slices per group)
     int group_kb;
@@ -333,6 +337,22 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         pair = 1;
     p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair, gs);
     if (p.kernel < 0) return DGEMM_ERR_NOT_SUPPORTED;
+    // Two K slices per stage for CTA-pair tiles whose operands can be viewed
+    // as stacks of whole 128-byte K slices (K a multiple of the slice; N a
+    // multiple of the 128-byte atom for B stored K x N): each operand of a stage
+    // is then one 32 KB TMA copy instead of two or three 16 KB ones, which the
+    // TMA unit fills faster. The kslices = 1 override keeps one slice.
+    p.ks = 1;
+    p.slice_k = p.bk;
+    if (pair && !gs && (p.mode == dg::MODE_TILE || p.mode == dg::MODE_ROWQ) && K > 0 && K % p.bk == 0 &&
+        (!p.b_mn || N % (128 / static_cast<int64_t>(esz)) == 0) && ov.kslices != 1) {
+        const int k2 = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair, gs, 2);
+        if (k2 >= 0) {
+            p.kernel = k2;
+            p.ks = 2;
+            p.bk = 2 * p.slice_k;
+        }
+    }
     const dg::KernelInfo* k = g_kernels[p.kernel];
     const int tile_m = pair ? 256 : 128;
     const int64_t tiles_m = (p.Mm + tile_m - 1) / tile_m, tiles_n = (p.Nm + bn - 1) / bn;
@@ -357,7 +377,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     // costs a few microseconds, so only long tiles (>= kMinTailSlices K
     // slices) are split, and problems with no full wave are left alone.
     // DGEMM_TAIL_SPLIT=0 disables splitting, =force drops the length rule.
-    const int64_t k_blocks = (K + p.bk - 1) / p.bk;
+    const int64_t k_blocks = (K + p.bk - 1) / p.bk;   // pipeline stages along K
     p.dp_tiles = p.pub.num_tiles;
     p.split = 1;
     p.tail_items = 0;
@@ -380,7 +400,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     // When the segments can form clusters (single-CTA kernels, 2 or 4
     // segments, every cluster resident at once) they are summed through
     // distributed shared memory instead, and no workspace is needed.
-    const int64_t sk = (split_ok && k_blocks > 0) ? underfill_split(p.pub.num_tiles, units, k_blocks) : 1;
+    const int64_t sk = (split_ok && k_blocks > 0) ? underfill_split(p.pub.num_tiles, units, k_blocks * p.ks) : 1;
     p.cluster_split = 0;
     if (sk > 1 && (p.mode == dg::MODE_TILE || p.mode == dg::MODE_SWAP)) {
         if (cluster_ok && !pair && (sk == 2 || sk == 4) && p.pub.num_tiles <= (sk == 2 ? max_pairs : max_quads)) {
@@ -396,9 +416,9 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         }
     } else if ((p.mode == dg::MODE_TILE || p.mode == dg::MODE_ROWQ) && split_ok && k_blocks > 0) {
         const int rem = p.pub.num_tiles % units;
-        if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks >= kMinTailSlices)) {
+        if (rem > 0 && p.pub.num_tiles >= units && (force_split || k_blocks * p.ks >= kMinTailSlices)) {
             int64_t split64 = units / rem;
-            if (split64 > k_blocks / 8) split64 = k_blocks / 8;
+            if (split64 > k_blocks * p.ks / 8) split64 = k_blocks * p.ks / 8;   // >= 8 K slices each
             if (split64 > 2) split64 = 2;   // a third or fourth partial costs more than it saves
             const int split = static_cast<int>(split64);
             if (split >= 2) use_split(p.pub.num_tiles - rem, split, rem * split);
@@ -438,6 +458,7 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     p.pub.tail_tiles = p.pub.num_tiles - p.dp_tiles;
     p.pub.tail_split = p.split;
     p.pub.tail_units = p.split > 1 ? p.tail_items : (p.tail_halves ? p.tail_items : 0);
+    p.pub.k_slices = p.ks;
     p.pub.cluster_split = p.cluster_split;
     p.pub.tail_halves = p.tail_halves;
     // Requantisation: status header, barrier header, row maxima, BF16 stash,
@@ -499,6 +520,24 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D view of a row-major matrix as a stack of 128-byte slices: dims
+// (inner elements of one slice, rows, slices), strides (row pitch, slice
+// pitch) in bytes; box of box_inner x box_rows x box_slices; 128-byte swizzle;
+// out-of-range rows and slices load as zero.
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t rows,
+               uint64_t slices, uint64_t row_pitch, uint64_t slice_pitch, uint32_t box_inner, uint32_t box_rows,
+               uint32_t box_slices) {
+    std::call_once(g_encode_once, init_encode);
+    if (!g_encode) return false;
+    const cuuint64_t dims[3] = {inner, rows, slices};
+    const cuuint64_t strides[2] = {row_pitch, slice_pitch};
+    const cuuint32_t box[3] = {box_inner, box_rows, box_slices};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -650,7 +689,27 @@ dgemm_status_t run(int fp8, const void* A, const void* B, dgemm_b_layout_t bl, c
     // The MMA's operands: X (rows of the MMA's M) and Y (rows of its N).
     const void* X = plan.pub.swap_ab ? B : A;
     const void* Y = plan.pub.swap_ab ? A : B;
-    if (K > 0) {
+    if (K > 0 && plan.ks == 2) {
+        // two K slices per stage: each operand of a stage in one 3-D copy
+        const uint64_t sk = plan.slice_k;   // elements per 128-byte slice
+        const uint64_t nslices = static_cast<uint64_t>(K) / sk;
+        const uint32_t bn_cta = static_cast<uint32_t>(plan.pub.tile_n / plan.pub.cta_group);
+        bool ok = encode_3d(&tmA, tm_type(in_t), X, sk, plan.Mm, nslices, K * esz, 128, sk, 128, 2);
+        if (!ok) return DGEMM_ERR_CUDA;
+        if (plan.b_mn) {   // B stored K x N: N atoms of 128 bytes, 2 slices of K rows each
+            const uint64_t atoms = static_cast<uint64_t>(N) / mn_atom;
+            ok = encode_3d(&tmB, tm_type(in_t), Y, mn_atom, K, atoms, N * esz, 128, mn_atom, 2 * sk,
+                           bn_cta / mn_atom);
+            if (ok && plan.tail_halves)
+                ok = encode_3d(&tmBh, tm_type(in_t), Y, mn_atom, K, atoms, N * esz, 128, mn_atom, 2 * sk,
+                               bn_cta / 2 / mn_atom);
+        } else {           // B stored N x K: K-major like A
+            ok = encode_3d(&tmB, tm_type(in_t), Y, sk, plan.Nm, nslices, K * esz, 128, sk, bn_cta, 2);
+            if (ok && plan.tail_halves)
+                ok = encode_3d(&tmBh, tm_type(in_t), Y, sk, plan.Nm, nslices, K * esz, 128, sk, bn_cta / 2, 2);
+        }
+        if (!ok) return DGEMM_ERR_CUDA;
+    } else if (K > 0) {
         bool ok;
         if (plan.a_mn)  // X = op(B)^T with B stored K x N: MN-major
             ok = encode_2d(&tmA, tm_type(in_t), X, N, K, N * esz, mn_atom, plan.bk);
@@ -889,8 +948,9 @@ dgemm_status_t dgemm_set_overrides(const dgemm_overrides_t* o) {
         if (o->tile_n < 0 || o->cta_pair < -1 || o->cta_pair > 1 || o->tail_split < -1 || o->tail_split > 1 ||
             o->tail_halves < -1 || o->tail_halves > 0 || o->cluster_split < -1 || o->cluster_split > 0 ||
             o->seg_first < -1 || o->seg_first > 1 ||
-            o->raster_group < 0 || o->cooperative < -1 ||
-            o->cooperative > 1 || o->wait_limit_ns < 0 || o->stall_after_loads < -1)
+            o->raster_group < 0 || o->cooperative < -1 || o->cooperative > 1 ||
+            !(o->kslices == -1 || o->kslices == 1 || o->kslices == 2) || o->wait_limit_ns < 0 ||
+            o->stall_after_loads < -1)
             return DGEMM_ERR_INVALID_VALUE;
         v = *o;
     }

@@ -208,7 +208,7 @@ __device__ __forceinline__ bool next_work(const Params& p, int unit, int units, 
 
 
 
-template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false, bool GS_ = false>
+template <int BN_, bool FP8_, bool A_MN_, bool B_MN_, int MODE_, bool PAIR_ = false, bool GS_ = false, int KS_ = 1>
 struct Cfg {
     static constexpr int BM = 128;                // accumulator rows per CTA
     static constexpr bool PAIR = PAIR_;
@@ -226,9 +226,18 @@ struct Cfg {
     static constexpr int BK = 128 / ESZ;          // K elements per stage (128 bytes)
     static constexpr int UMMA_K = 32 / ESZ;       // K elements per MMA (32 bytes)
     static constexpr int MN_ATOM = 128 / ESZ;     // MN elements per 128-byte row (MN-major)
-    static constexpr int A_BYTES = BM * 128;
+    // K slices (128 bytes of K each) per pipeline stage. With 2, each operand
+    // of a stage arrives in one 3-D TMA copy of two consecutive slices (the
+    // TMA unit fills a CTA's shared memory ~16 % faster in 32 KB copies than
+    // in 16 KB ones); the slices land one after the other, each an ordinary
+    // 128B-swizzled slice (K-major), or the N atoms hold 2 x BK rows of K each
+    // (MN-major B).
+    static constexpr int KS = KS_;
+    static constexpr int SLICE_A = BM * 128;      // bytes of one K slice of A
+    static constexpr int A_BYTES = KS * BM * 128;
     static constexpr int BN_CTA = BN / CTAS;      // B rows (N) each CTA loads
-    static constexpr int B_BYTES = BN_CTA * 128;
+    static constexpr int SLICE_B = BN_CTA * 128;  // bytes of one K slice of B (K-major)
+    static constexpr int B_BYTES = KS * BN_CTA * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // Epilogue warps: two per TMEM lane quarter (each takes half of the tile's
     // columns) for tiles of 128 columns or more, whose FP8 mainloop per tile can
@@ -258,7 +267,7 @@ struct Cfg {
     // whole 128-byte atoms of it (MN-major; one for BF16, none fits for E4M3).
     static constexpr bool HALVES = PAIR && BN == 256 && !GS && (!B_MN || (BN_CTA / 2) % MN_ATOM == 0);
     static constexpr uint32_t IDESC_HALF = make_idesc(FP8 ? 0u : 1u, A_MN, B_MN, TILE_M, BN / 2);
-    static constexpr int B_BYTES_HALF = BN_CTA / 2 * 128;
+    static constexpr int B_BYTES_HALF = KS * (BN_CTA / 2) * 128;
     // Per-K-group scales keep each epilogue thread's share of the running sum
     // (EPI_COLS FP32 values) in registers. With 8 epilogue warps that needs more
     // than the 168 registers a thread of a 10-warp block can have, so those
@@ -276,6 +285,7 @@ struct Cfg {
                   "register split exceeds the launch allocation");
 
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
+    static_assert(KS == 1 || (KS == 2 && PAIR && !GS && !A_MN && MODE != MODE_SWAP), "two-slice stages: pair tile forms");
     static_assert(!B_MN || BN_CTA % MN_ATOM == 0, "MN-major B needs whole 128-byte atoms");
     static_assert(!PAIR || (MODE != MODE_SWAP && !A_MN && BN == 256), "CTA pairs: 256 x 256 tiles");
     static_assert(MODE == MODE_SWAP || EPI_COLS % 64 == 0, "tile epilogue works in 64-column boxes");
@@ -669,8 +679,19 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                         }
                         uint8_t* sa = stages + stage * CF::STAGE_BYTES;
                         uint8_t* sb = sa + CF::A_BYTES;
-                        const int k0 = kb * CF::BK;
-                        if constexpr (CF::PAIR) {
+                        const int k0 = kb * CF::KS * CF::BK;   // first K element of the stage
+                        if constexpr (CF::PAIR && CF::KS == 2) {
+                            // one 3-D copy per operand: slices kb * 2 and kb * 2 + 1
+                            if (rank == 0)
+                                mbar_arrive_expect_tx(&full[stage],
+                                                      CF::CTAS * (half ? CF::A_BYTES + CF::B_BYTES_HALF : CF::STAGE_BYTES));
+                            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+                            tma_load_3d_pair(sa, &tmA, fb, 0, row0, kb * 2, pol);
+                            if constexpr (CF::B_MN)   // atoms of MN_ATOM columns, 2 x BK rows of K each
+                                tma_load_3d_pair(sb, half ? &tmBh : &tmB, fb, 0, k0, col0 / CF::MN_ATOM, pol);
+                            else
+                                tma_load_3d_pair(sb, half ? &tmBh : &tmB, fb, 0, col0, kb * 2, pol);
+                        } else if constexpr (CF::PAIR) {
                             // both CTAs' copies complete on the leader's full barrier
                             if (rank == 0)
                                 mbar_arrive_expect_tx(&full[stage],
@@ -736,7 +757,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 // slice here measurably starves the tensor pipe).
                 const uint32_t s0 = smem_u32(stages);
                 const uint64_t a_desc0 = smem_desc_sw128(s0, CF::A_MN ? CF::BK * 128 : 16, 1024);
-                const uint64_t b_desc0 = smem_desc_sw128(s0 + CF::A_BYTES, CF::B_MN ? CF::BK * 128 : 16, 1024);
+                // (MN-major B: N atoms KS x BK rows of K apart)
+                const uint64_t b_desc0 =
+                    smem_desc_sw128(s0 + CF::A_BYTES, CF::B_MN ? CF::KS * CF::BK * 128 : 16, 1024);
                 constexpr uint32_t A_KSTEP = (CF::A_MN ? CF::UMMA_K * 128 : 32) >> 4;
                 constexpr uint32_t B_KSTEP = (CF::B_MN ? CF::UMMA_K * 128 : 32) >> 4;
                 constexpr uint32_t STAGE_STEP = CF::STAGE_BYTES >> 4;
@@ -745,24 +768,30 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 bool ok = true;
                 int local = 0;
                 Work w;
-                // The MMAs of one K slice (a pipeline stage) into accumulator d_tmem;
-                // `first` starts a fresh accumulation.
-                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc) {
+                // The MMAs of one pipeline stage (KS K slices of NK1 MMAs each) into
+                // accumulator d_tmem; `first` starts a fresh accumulation. b_slice:
+                // descriptor step between the stage's K slices of K-major B (a tail
+                // half's B slices are half as tall).
+                constexpr int NK1 = CF::BK / CF::UMMA_K;
+                constexpr uint32_t A_SLICE = CF::SLICE_A >> 4;
+                auto issue_stage = [&](uint32_t d_tmem, uint32_t st, bool first, uint32_t idesc, uint32_t b_slice) {
                     const uint64_t ad = a_desc0 + st * STAGE_STEP;
                     const uint64_t bd = b_desc0 + st * STAGE_STEP;
     #pragma unroll
-                    for (int k = 0; k < CF::BK / CF::UMMA_K; ++k) {
+                    for (int k = 0; k < CF::KS * NK1; ++k) {
                         const uint32_t acc = (!first || k > 0) ? 1u : 0u;
+                        const uint32_t ao = (k / NK1) * A_SLICE + (k % NK1) * A_KSTEP;
+                        const uint32_t bo = CF::B_MN ? k * B_KSTEP : (k / NK1) * b_slice + (k % NK1) * B_KSTEP;
                         if constexpr (CF::PAIR) {
                             if constexpr (CF::FP8)
-                                mma_f8_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
+                                mma_f8_pair(d_tmem, ad + ao, bd + bo, idesc, acc);
                             else
-                                mma_bf16_pair(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
+                                mma_bf16_pair(d_tmem, ad + ao, bd + bo, idesc, acc);
                         } else {
                             if constexpr (CF::FP8)
-                                mma_f8(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
+                                mma_f8(d_tmem, ad + ao, bd + bo, idesc, acc);
                             else
-                                mma_bf16(d_tmem, ad + k * A_KSTEP, bd + k * B_KSTEP, idesc, acc);
+                                mma_bf16(d_tmem, ad + ao, bd + bo, idesc, acc);
                         }
                     }
                     // the stage is free (in both CTAs of a pair) once these MMAs have read it
@@ -797,7 +826,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                                 break;
                             }
                             tc_fence_after();
-                            issue_stage(d_tmem, stage, first, CF::IDESC);
+                            issue_stage(d_tmem, stage, first, CF::IDESC, CF::SLICE_B >> 4);
                             if (++stage == S) {
                                 stage = 0;
                                 phase ^= 1;
@@ -832,7 +861,9 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                     }
                     uint32_t d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                     // a tail half is one MMA of half the width
-                    const uint32_t idesc_item = (CF::HALVES && w.half >= 0) ? CF::IDESC_HALF : CF::IDESC;
+                    const bool half_item = CF::HALVES && w.half >= 0;
+                    const uint32_t idesc_item = half_item ? CF::IDESC_HALF : CF::IDESC;
+                    const uint32_t b_slice = (half_item ? CF::SLICE_B / 2 : CF::SLICE_B) >> 4;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
                             ok = false;
@@ -846,7 +877,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             next_group_start = ((group + 1) * kblocks + ngroups - 1) / ngroups;
                             d_tmem = acc_base + static_cast<uint32_t>(group * CF::BN);
                         }
-                        issue_stage(d_tmem, stage, first_in_group, idesc_item);
+                        issue_stage(d_tmem, stage, first_in_group, idesc_item, b_slice);
                         if (++stage == S) {
                             stage = 0;
                             phase ^= 1;

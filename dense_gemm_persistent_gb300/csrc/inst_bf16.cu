@@ -25,6 +25,11 @@ const KernelInfo* kernels_bf16(int* count) {
         make_info<Cfg<256, false, false, false, MODE_TILE, true>>(),
         make_info<Cfg<256, false, false, false, MODE_ROWQ, true>>(),
         make_info<Cfg<256, false, false, true, MODE_ROWQ, true>>(),
+        // CTA pairs with two K slices per stage (3-D TMA copies)
+        make_info<Cfg<256, false, false, true, MODE_TILE, true, false, 2>>(),
+        make_info<Cfg<256, false, false, false, MODE_TILE, true, false, 2>>(),
+        make_info<Cfg<256, false, false, false, MODE_ROWQ, true, false, 2>>(),
+        make_info<Cfg<256, false, false, true, MODE_ROWQ, true, false, 2>>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;

@@ -18,6 +18,7 @@ using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, con
 
 struct KernelInfo {
     int bn, fp8, a_mn, b_mn, mode, pair, gs;
+    int ks;            // K slices per pipeline stage (2: operands in 3-D TMA copies)
     int halves;        // can run tail tiles as two N halves
     int stages, smem_bytes, tmem_cols, threads, epi_warps;
     int launch_regs;   // register split (setmaxnreg): registers per thread the split assumes at launch; 0 = none
@@ -62,7 +63,7 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
 template <class CF>
 KernelInfo make_info() {
     return KernelInfo{CF::BN,     CF::FP8,    CF::A_MN,       CF::B_MN,      CF::MODE,
-                      CF::PAIR ? 1 : 0, CF::GS ? 1 : 0, CF::HALVES ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
+                      CF::PAIR ? 1 : 0, CF::GS ? 1 : 0, CF::KS, CF::HALVES ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
                       CF::EPI_WARPS, CF::REG_SPLIT ? CF::LAUNCH_REGS : 0,
                       reinterpret_cast<const void*>(&gemm_persistent<CF>), &launch_variant<CF>};
 }

@@ -149,6 +149,8 @@ typedef struct {
                               whole K range (no workspace needed)            */
     int tail_units;        /* units (CTAs or CTA pairs) that run the tail's
                               K segments or halves, one each (0 = none)        */
+    int k_slices;          /* 128-byte K slices per pipeline stage (2: each
+                              operand of a stage arrives in one 3-D TMA copy) */
     size_t smem_bytes;     /* dynamic shared memory per CTA                     */
     size_t workspace_bytes;/* what dgemm_workspace_size returns for this call   */
 } dgemm_plan_t;
@@ -290,6 +292,10 @@ typedef struct {
                             otherwise idle GPU); 1: launch every plan whose split
                             tiles exchange partials through the workspace
                             cooperatively (DGEMM_COOPERATIVE)                       */
+    int kslices;         /* -1; 1: one 128-byte K slice per pipeline stage (the
+                            planner takes two, fetched in 3-D copies, for CTA-pair
+                            tiles whose K, and N when B is stored K x N, are whole
+                            multiples of 128 bytes) (DGEMM_KSLICES)                 */
     int64_t wait_limit_ns;     /* 0: about one second; else the limit of every
                                   bounded device-side wait (DGEMM_WAIT_LIMIT_NS)    */
     int64_t stall_after_loads; /* -1; testing the bounded waits: every CTA's operand

@@ -121,7 +121,8 @@ def test_plans_for_the_five_workloads(lib):
     assert p1["swap_ab"] == 0 and p1["grid"] <= 152 and p1["tile_n"] == 64
     p2 = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p2["cta_group"], p2["tile_m"], p2["tile_n"]) == (2, 256, 256)
-    assert p2["num_tiles"] == 256 and p2["grid"] == 152 and p2["stages"] == 6
+    # two 128-byte K slices per stage: 3 stages of 2 x 32 KB per CTA
+    assert p2["num_tiles"] == 256 and p2["grid"] == 152 and (p2["stages"], p2["k_slices"]) == (3, 2)
     assert (p2["tail_tiles"], p2["tail_split"], p2["tail_units"]) == (28, 2, 56)   # 3 full waves + 28 tiles in K halves
     p3 = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
     assert p3["cta_group"] == 2 and p3["num_tiles"] == 16 * 43 and p3["grid"] == 152
@@ -139,7 +140,9 @@ def test_plan_of_per_group_scales(lib):
     the scale ring takes shared memory); invalid groups fail as the call would."""
     p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=128, num_sms=152)
     assert (p["k_groups"], p["cta_group"], p["tile_n"], p["stages"]) == (32, 2, 256, 5)
-    assert dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)["stages"] == 6
+    p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
+    assert (p["stages"], p["k_slices"]) == (3, 2)   # per-row scales: two K slices per stage
+    assert p["k_slices"] * p["stages"] * 32 == 2 * 96   # the same bytes in flight as 6 single slices
     with pytest.raises(dg.DgemmError):
         dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=64, num_sms=152)
 
@@ -168,7 +171,7 @@ def test_split_exchange_launch_modes(lib, knobs):
 def test_overrides_validation_and_defaults(lib):
     d = dg.get_overrides()
     assert d == {"tile_n": 0, "cta_pair": -1, "tail_split": -1, "tail_halves": -1, "cluster_split": -1,
-                 "seg_first": -1, "raster_group": 0, "cooperative": -1, "wait_limit_ns": 0,
+                 "seg_first": -1, "raster_group": 0, "cooperative": -1, "kslices": -1, "wait_limit_ns": 0,
                  "stall_after_loads": -1}
     for bad in ({"cta_pair": 2}, {"tail_halves": 1}, {"cooperative": -2}, {"wait_limit_ns": -1},
                 {"stall_after_loads": -5}, {"tile_n": -64}):
@@ -299,3 +302,23 @@ def test_underfilled_plans_by_streamed_and_exchanged_bytes(lib):
     assert (p["tile_n"], p["tail_split"]) == (64, 4)
     p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
     assert (p["tile_n"], p["cta_group"]) == (256, 2)
+
+
+def test_two_slice_stages_only_where_the_operands_are_whole_slices(lib, knobs):
+    """CTA-pair tile and requantising plans take two 128-byte K slices per
+    stage (each operand one 3-D TMA copy) when K, and N for B stored K x N,
+    are whole multiples of 128 bytes; otherwise, for single-CTA tiles, the
+    small-M form and per-K-group scales, one slice per stage."""
+    def plan(fp8, M, N, K, layout, **kw):
+        return dg.dgemm_plan(fp8, M, N, K, layout, "bf16", num_sms=152, **kw)
+    assert plan(0, 4096, 4096, 4096, "kn")["k_slices"] == 2
+    assert plan(0, 4096, 4096, 1000, "kn")["k_slices"] == 1          # K not whole 64-element slices
+    assert plan(0, 4096, 4000, 4096, "kn")["k_slices"] == 1          # N not whole 64-column atoms
+    assert plan(0, 4096, 4000, 4096, "nk")["k_slices"] == 2          # (N is free for B stored N x K)
+    assert plan(1, 4096, 11008, 4096, "nk", k_group=128)["k_slices"] == 1
+    assert plan(0, 16, 4096, 4096, "nk")["k_slices"] == 1            # small M
+    assert plan(0, 1024, 1024, 4096, "nk")["k_slices"] == 1          # single-CTA tiles
+    assert dg.dgemm_plan(1, 8192, 8192, 8192, "nk", "e4m3", out_quant="e4m3_row_amax", num_sms=152)["k_slices"] == 2
+    knobs(kslices="1")
+    p = plan(0, 4096, 4096, 4096, "kn")
+    assert (p["k_slices"], p["stages"]) == (1, 6)

@@ -159,12 +159,15 @@ def test_fp8_wide_tile_single_and_pair_exact(layout, pair, halves, knobs):
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
+@pytest.mark.parametrize("kslices", ["2", "1"])
 @pytest.mark.parametrize("kblocks", [1, 5, 6, 7, 13])
-def test_pair_phases_across_many_tiles_exact(kblocks):
+def test_pair_phases_across_many_tiles_exact(kblocks, kslices, knobs):
     """CTA pairs with several tiles each (4096 x 8192 -> 512 tiles over <= 76 pairs)
-    and K-slice counts around the 6-stage ring depth."""
+    and K-slice counts around the ring depth (6 stages of one slice, or 3 of
+    two slices, an odd count leaving the last stage's second slice beyond K)."""
+    knobs(kslices=kslices)
     plan = dg.dgemm_plan(0, 4096, 8192, 64 * kblocks, "nk", "f32")
-    assert plan["cta_group"] == 2
+    assert plan["cta_group"] == 2 and plan["k_slices"] == int(kslices)
     got, ref = bf16_case(4096, 8192, 64 * kblocks, "nk", seed=600 + kblocks)
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
@@ -219,12 +222,14 @@ def test_tail_split_repeated_calls_reuse_workspace(knobs):
         assert np.array_equal(D.cpu().double().numpy(), ref)
 
 
+@pytest.mark.parametrize("kslices", ["2", "1"])
 @pytest.mark.parametrize("shape,layout", [((4096, 4096, 1024), "kn"), ((4096, 4096, 1024), "nk"),
                                           ((4000, 1288, 1024), "kn"), ((2304, 2816, 2000), "nk")])
-def test_tail_halves_exact(shape, layout):
+def test_tail_halves_exact(shape, layout, kslices, knobs):
     """The last partial wave's CTA-pair tiles, too short to split along K, run
     as two 256 x 128 halves each (N = 128 MMAs over the whole K range, half of
     B loaded): bit-exact, ragged edges included."""
+    knobs(kslices=kslices)
     M, N, K = shape
     plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
     assert plan["cta_group"] == 2 and plan["tail_halves"] == 1 and plan["tail_tiles"] > 0
