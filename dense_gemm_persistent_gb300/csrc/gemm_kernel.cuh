@@ -67,6 +67,8 @@ struct Params {
     // Problem in the MMA's orientation: rows M, columns N, reduction K.
     int M, N, K;
     int tiles_m, tiles_n, num_tiles, k_blocks, group_m;
+    int stages;      // depth of the shared-memory ring (at most the variant's STAGES)
+    int tmem_cols;   // Tensor Memory columns each CTA allocates
     // K-group promotion: the K slices of a tile are split into acc_groups
     // contiguous groups, each accumulated by the tensor core into its own TMEM
     // accumulator (BN columns apart) and summed in FP32 by the epilogue.
@@ -255,8 +257,17 @@ struct Cfg {
     static constexpr int GS_BYTES = SC_SLOTS * SLOT_FLOATS * 4;
     static constexpr int BAR_BYTES = GS_SMEM ? 384 : 256;
     static constexpr int SMEM_LIMIT = 232448;  // 227 KB opt-in maximum per CTA
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - STAGING_BYTES - GS_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int SMEM_FIXED = 1024 + STAGING_BYTES + GS_BYTES + BAR_BYTES;   // all but the ring
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - SMEM_FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+    // The small-M (transposed) form also runs in a compact footprint, chosen
+    // per call for short calls: at most half of an SM's 228 KB of shared
+    // memory (less the 1 KB the hardware reserves per CTA) and half of its
+    // Tensor Memory, so that the next call's CTAs become resident and run their
+    // prologue while this call's finish (programmatic dependent launch).
+    static constexpr int STAGES_HALF_FIT = (115712 - SMEM_FIXED) / STAGE_BYTES;
+    static constexpr int STAGES_COMPACT =
+        (MODE == MODE_SWAP && STAGES_HALF_FIT < STAGES) ? STAGES_HALF_FIT : STAGES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + GS_BYTES + BAR_BYTES;
     static constexpr int TMEM_COLS = (MODE == MODE_SWAP && !GS) ? 512
                                    : (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
@@ -289,7 +300,7 @@ struct Cfg {
     static_assert(!B_MN || BN_CTA % MN_ATOM == 0, "MN-major B needs whole 128-byte atoms");
     static_assert(!PAIR || (MODE != MODE_SWAP && !A_MN && BN == 256), "CTA pairs: 256 x 256 tiles");
     static_assert(MODE == MODE_SWAP || EPI_COLS % 64 == 0, "tile epilogue works in 64-column boxes");
-    static_assert(STAGES >= 2, "pipeline depth");
+    static_assert(STAGES >= 2 && STAGES_COMPACT >= 2, "pipeline depth");
     static_assert(!GS || (FP8 && MODE != MODE_ROWQ), "per-K-group scales: FP8, tile or small-M form");
     // block-scaled weights: a warp's columns lie inside one 128-column block
     static_assert(!GS_SMEM || 128 % EPI_COLS == 0, "warp columns within a weight block");
@@ -298,7 +309,7 @@ struct Cfg {
     // full/empty per stage, 2 + 2 accumulator, drain, scale slots; TMEM address + abort flag
     static_assert((2 * STAGES + 5 + 2 * SC_SLOTS) * 8 + 8 <= BAR_BYTES, "barriers fit");
     // split-K through the cluster parks a whole accumulator in the pipeline buffers
-    static_assert(EPI_WARPS * BN / (EPI_WARPS / 4) * 32 * 4 <= STAGES * STAGE_BYTES, "parked partials fit");
+    static_assert(EPI_WARPS * BN / (EPI_WARPS / 4) * 32 * 4 <= STAGES_COMPACT * STAGE_BYTES, "parked partials fit");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
@@ -573,7 +584,10 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmBh,
                     const __grid_constant__ CUtensorMap tmD, const Params p) {
-    constexpr int S = CF::STAGES;
+    // ring depth: chosen per launch for the small-M form (compact or full),
+    // fixed for the others
+    const int S = CF::MODE == MODE_SWAP ? p.stages : CF::STAGES;
+    const uint32_t tmem_cols = CF::MODE == MODE_SWAP ? static_cast<uint32_t>(p.tmem_cols) : CF::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
@@ -627,7 +641,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         __syncthreads();
         cluster_sync();
         if (warp == 1) {
-            tmem_alloc_pair(tmem_slot, CF::TMEM_COLS);
+            tmem_alloc_pair(tmem_slot, tmem_cols);
             tmem_relinquish_pair();
         }
         tc_fence_before();
@@ -635,7 +649,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         cluster_sync();
     } else {
         if (warp == 1) {
-            tmem_alloc(tmem_slot, CF::TMEM_COLS);
+            tmem_alloc(tmem_slot, tmem_cols);
             tmem_relinquish();
         }
         tc_fence_before();
@@ -1636,7 +1650,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         cluster_sync();
         if (warp == 1) {
             tc_fence_after();
-            tmem_dealloc_pair(tmem_base, CF::TMEM_COLS);
+            tmem_dealloc_pair(tmem_base, tmem_cols);
         }
     } else {
         // with split-K through the cluster, no CTA leaves while a peer may
@@ -1644,7 +1658,7 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
         if (p.cluster_split) cluster_sync();
         if (warp == 1) {
             tc_fence_after();
-            tmem_dealloc(tmem_base, CF::TMEM_COLS);
+            tmem_dealloc(tmem_base, tmem_cols);
         }
     }
 }

@@ -12,9 +12,10 @@ namespace dg {
 struct KernelInfo;
 // bh: B's tensor map for the loads of a tail half (K-major B: 64-row box).
 // cluster: CTAs per cluster for kernels that are not CTA pairs (1 = none).
+// smem: dynamic shared memory of this launch (the ring depth is p.stages).
 using LaunchFn = cudaError_t (*)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bh,
                                  const CUtensorMap& d, const Params& p, int grid, cudaStream_t s, bool cooperative,
-                                 int cluster);
+                                 int cluster, size_t smem);
 
 struct KernelInfo {
     int bn, fp8, a_mn, b_mn, mode, pair, gs;
@@ -22,17 +23,20 @@ struct KernelInfo {
     int halves;        // can run tail tiles as two N halves
     int stages, smem_bytes, tmem_cols, threads, epi_warps;
     int launch_regs;   // register split (setmaxnreg): registers per thread the split assumes at launch; 0 = none
+    // compact footprint (small-M form; otherwise the full one): ring depth and
+    // shared memory that leave room for a second CTA on the SM
+    int stages_compact, smem_compact;
     const void* func;  // host stub of the __global__ function (for attributes)
     LaunchFn launch;
 };
 
 template <class CF>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bh, const CUtensorMap& d,
-                           const Params& p, int grid, cudaStream_t s, bool cooperative, int cluster) {
+                           const Params& p, int grid, cudaStream_t s, bool cooperative, int cluster, size_t smem) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(CF::NUM_THREADS);
-    cfg.dynamicSmemBytes = CF::SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[3];
     unsigned n = 0;
@@ -65,6 +69,7 @@ KernelInfo make_info() {
     return KernelInfo{CF::BN,     CF::FP8,    CF::A_MN,       CF::B_MN,      CF::MODE,
                       CF::PAIR ? 1 : 0, CF::GS ? 1 : 0, CF::KS, CF::HALVES ? 1 : 0, CF::STAGES, CF::SMEM_BYTES, CF::TMEM_COLS, CF::NUM_THREADS,
                       CF::EPI_WARPS, CF::REG_SPLIT ? CF::LAUNCH_REGS : 0,
+                      CF::STAGES_COMPACT, CF::SMEM_FIXED + CF::STAGES_COMPACT * CF::STAGE_BYTES,
                       reinterpret_cast<const void*>(&gemm_persistent<CF>), &launch_variant<CF>};
 }
 

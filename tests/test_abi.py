@@ -322,3 +322,25 @@ def test_two_slice_stages_only_where_the_operands_are_whole_slices(lib, knobs):
     knobs(kslices="1")
     p = plan(0, 4096, 4096, 4096, "kn")
     assert (p["k_slices"], p["stages"]) == (1, 6)
+
+
+def test_short_small_m_calls_take_half_an_sm(lib):
+    """Small-M calls whose work items are at most 32 K slices long run in a
+    compact footprint -- at most half of an SM's shared memory (228 KB less the
+    1 KB reserved per CTA, halved) and 256 of its 512 Tensor Memory columns, so
+    the K groups halve -- letting the next call's CTAs become resident early;
+    longer streams keep the full ring and all 512 columns."""
+    def plan(M, N, K):
+        return dg.dgemm_plan(0, M, N, K, "nk", "bf16", num_sms=152)
+    half_sm = (228 * 1024) // 2 - 1024
+    for M in (1, 16):
+        p = plan(M, 4096, 4096)   # 32 tiles x 4 K segments of 16 slices
+        assert p["swap_ab"] == 1 and (p["tail_split"], p["cluster_split"]) == (4, 1)
+        assert p["smem_bytes"] <= half_sm and p["stages"] == 6
+        assert p["k_groups"] == 256 // p["tile_n"]
+    p = plan(16, 18432, 7168)      # 144 tiles, 112 slices each: the full ring
+    assert p["smem_bytes"] > half_sm and p["stages"] == 12 and p["k_groups"] == 512 // 16
+    p = plan(64, 8192, 8192)       # 2 segments of 64 slices
+    assert p["smem_bytes"] > half_sm and p["tail_split"] == 2
+    p = plan(4096, 4096, 4096)     # tile kernels are never compact
+    assert p["smem_bytes"] > half_sm
