@@ -105,18 +105,17 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
 int g_nk = 0;
-const dg::KernelInfo* g_kernels[64];
+constexpr int kMaxKernels = 96;
+const dg::KernelInfo* g_kernels[kMaxKernels];
 std::atomic<unsigned char> g_attr_set[64][kMaxDevices];
 std::once_flag g_kernels_once;
 
 void collect_kernels() {
-    int n1 = 0, n2 = 0, n3 = 0;
-    const dg::KernelInfo* t1 = dg::kernels_bf16(&n1);
-    const dg::KernelInfo* t2 = dg::kernels_fp8(&n2);
-    const dg::KernelInfo* t3 = dg::kernels_fp8_grouped(&n3);
-    for (int i = 0; i < n1 && g_nk < 64; ++i) g_kernels[g_nk++] = &t1[i];
-    for (int i = 0; i < n2 && g_nk < 64; ++i) g_kernels[g_nk++] = &t2[i];
-    for (int i = 0; i < n3 && g_nk < 64; ++i) g_kernels[g_nk++] = &t3[i];
+    int n[4] = {0, 0, 0, 0};
+    const dg::KernelInfo* t[4] = {dg::kernels_bf16(&n[0]), dg::kernels_fp8(&n[1]), dg::kernels_fp8_grouped(&n[2]),
+                                  dg::kernels_two_slice(&n[3])};
+    for (int j = 0; j < 4; ++j)
+        for (int i = 0; i < n[j] && g_nk < kMaxKernels; ++i) g_kernels[g_nk++] = &t[j][i];
 }
 
 int find_kernel(int bn, int fp8, int a_mn, int b_mn, int mode, int pair, int gs, int ks = 1) {
@@ -298,16 +297,25 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
                 pair = c.pair;
             }
         }
-        // At most one wave of single-CTA tiles: the time is the operand bytes
-        // each CTA streams (128-byte K slices of its 128 A rows and bn B rows,
-        // ~150 GB/s per SM) plus the partial sums its K segments exchange,
-        // which move ~4x slower per byte through distributed shared memory
-        // (~8x through the workspace). Measured on 1024 x 1024 x 4096: BF16
-        // 128 x 256 in 4 segments 16.5 us = 128 x 128 in 2 segments 16.4 us
-        // (equal modelled costs); FP8 14.1 us against 11.9 us (the second
-        // modelled cheaper), which the wave model above misorders.
+        // At most one wave of single-CTA tiles: the time is set by each CTA's
+        // TMA copies -- a fixed ~90 ns per copy plus the bytes at ~213 GB/s
+        // per SM, i.e. ~19.2 KB of streaming per copy: one copy of A and one of
+        // B (or one per 128-byte atom of MN-major B) per K slice, or one of each
+        // per two slices where the tile takes two-slice stages -- plus the
+        // partial sums its K segments exchange, ~13x slower per byte through
+        // distributed shared memory (~27x through the workspace). Fitted to
+        // 1024 x 1024 x 4096 BF16 with one slice per stage (128 x 256 in 4
+        // segments 16.5 us = 128 x 128 in 2 segments 16.4 us); with two-slice
+        // stages the second took 15.95 us against 18.5, and FP8 11.9 against
+        // 14.1, the order the model gives.
         const int64_t tiles_w = ((M + 127) / 128) * ((N + bn - 1) / bn);
         if (!pair && p.mode == dg::MODE_TILE && tiles_w <= num_sms) {
+            const int64_t slice_k = static_cast<int64_t>(128 / esz);
+            auto two_slice = [&](int w) {
+                return !gs && ov.kslices != 1 && K % slice_k == 0 && (!p.b_mn || N % slice_k == 0) &&
+                       find_kernel(w, fp8, p.a_mn, p.b_mn, p.mode, 0, gs, 2) >= 0;
+            };
+            constexpr double kCopyBytes = 19170.0;   // ~90 ns at ~213 GB/s
             double best_t = 1e300;
             for (const Cand& c : cands) {
                 if (c.pair || (fp8 && p.b_mn && c.bn < 128)) continue;
@@ -315,9 +323,11 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
                 if (tiles > num_sms) continue;
                 const int64_t sk = split_ok ? underfill_split(tiles, num_sms, kb_all) : 1;
                 const bool cl = cluster_ok && (sk == 2 || sk == 4) && tiles <= (sk == 2 ? max_pairs : max_quads);
-                const double stream = static_cast<double>(128 + c.bn) * static_cast<double>((kb_all + sk - 1) / sk) * 128.0;
+                const double copies = two_slice(c.bn) ? 1.0 : 1.0 + (p.b_mn ? c.bn / static_cast<double>(slice_k) : 1.0);
+                const double stream = (static_cast<double>(128 + c.bn) * 128.0 + copies * kCopyBytes) *
+                                      static_cast<double>((kb_all + sk - 1) / sk);
                 const double xchg = sk > 1 ? 128.0 * c.bn * 4.0 * static_cast<double>(sk - 1) / static_cast<double>(sk) *
-                                                 (cl ? 4.0 : 8.0)
+                                                 (cl ? 13.4 : 26.8)
                                            : 0.0;
                 if (stream + xchg < best_t) {
                     best_t = stream + xchg;
@@ -341,14 +351,16 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         pair = 1;
     p.kernel = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair, gs);
     if (p.kernel < 0) return DGEMM_ERR_NOT_SUPPORTED;
-    // Two K slices per stage for CTA-pair tiles whose operands can be viewed
-    // as stacks of whole 128-byte K slices (K a multiple of the slice; N a
-    // multiple of the 128-byte atom for B stored K x N): each operand of a stage
-    // is then one 32 KB TMA copy instead of two or three 16 KB ones, which the
-    // TMA unit fills faster. The kslices = 1 override keeps one slice.
+    // Two K slices per stage for tile kernels (CTA pairs and single CTAs; not
+    // per-K-group scales) whose operands can be viewed as stacks of whole
+    // 128-byte K slices (K a multiple of the slice; N a multiple of the 128-byte
+    // atom for B stored K x N): each operand of a stage is then one 3-D TMA copy
+    // of twice the bytes, and the TMA unit, which spends a fixed time on every
+    // copy, fills the stages faster. The kslices = 1 override keeps one slice.
     p.ks = 1;
     p.slice_k = p.bk;
-    if (pair && !gs && (p.mode == dg::MODE_TILE || p.mode == dg::MODE_ROWQ) && K > 0 && K % p.bk == 0 &&
+    if ((pair || p.mode == dg::MODE_TILE) && !gs && (p.mode == dg::MODE_TILE || p.mode == dg::MODE_ROWQ) && K > 0 &&
+        K % p.bk == 0 &&
         (!p.b_mn || N % (128 / static_cast<int64_t>(esz)) == 0) && ov.kslices != 1) {
         const int k2 = find_kernel(bn, fp8, p.a_mn, p.b_mn, p.mode, pair, gs, 2);
         if (k2 >= 0) {

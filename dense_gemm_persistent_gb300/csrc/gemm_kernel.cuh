@@ -296,7 +296,8 @@ struct Cfg {
                   "register split exceeds the launch allocation");
 
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
-    static_assert(KS == 1 || (KS == 2 && PAIR && !GS && !A_MN && MODE != MODE_SWAP), "two-slice stages: pair tile forms");
+    static_assert(KS == 1 || (KS == 2 && !GS && !A_MN && MODE != MODE_SWAP && (PAIR || MODE == MODE_TILE)),
+                  "two-slice stages: tile forms");
     static_assert(!B_MN || BN_CTA % MN_ATOM == 0, "MN-major B needs whole 128-byte atoms");
     static_assert(!PAIR || (MODE != MODE_SWAP && !A_MN && BN == 256), "CTA pairs: 256 x 256 tiles");
     static_assert(MODE == MODE_SWAP || EPI_COLS % 64 == 0, "tile epilogue works in 64-column boxes");
@@ -722,6 +723,14 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                             } else {
                                 tma_load_2d_pair(sb, half ? &tmBh : &tmB, fb, k0, col0, pol);
                             }
+                        } else if constexpr (CF::KS == 2) {
+                            // one 3-D copy per operand: slices kb * 2 and kb * 2 + 1
+                            mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
+                            tma_load_3d(sa, &tmA, &full[stage], 0, row0, kb * 2, pol);
+                            if constexpr (CF::B_MN)   // atoms of MN_ATOM columns, 2 x BK rows of K each
+                                tma_load_3d(sb, &tmB, &full[stage], 0, k0, col0 / CF::MN_ATOM, pol);
+                            else
+                                tma_load_3d(sb, &tmB, &full[stage], 0, col0, kb * 2, pol);
                         } else {
                             mbar_arrive_expect_tx(&full[stage], CF::STAGE_BYTES);
                             if constexpr (CF::A_MN) {

@@ -77,5 +77,6 @@ KernelInfo make_info() {
 const KernelInfo* kernels_bf16(int* count);
 const KernelInfo* kernels_fp8(int* count);
 const KernelInfo* kernels_fp8_grouped(int* count);
+const KernelInfo* kernels_two_slice(int* count);
 
 }  // namespace dg

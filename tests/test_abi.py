@@ -287,28 +287,31 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     assert int(lines["query"]) in (0, 5)        # DGEMM_OK on a GPU machine, DGEMM_ERR_CUDA without a device
 
 
-def test_underfilled_plans_by_streamed_and_exchanged_bytes(lib):
-    """Under one wave of single-CTA tiles the tile width follows the bytes each
-    CTA streams plus 4x the partial sums its K segments exchange in a cluster:
-    FP8 1024^2 x 4096 takes 128-wide tiles in two segments (streamed 512 KB +
-    exchanged 32 KB per CTA, against 384 KB + 96 KB for 256-wide tiles in four),
-    BF16 keeps 128 x 256 in four (the two cost the same there); full-wave plans
-    are unchanged."""
-    p = dg.dgemm_plan(1, 1024, 1024, 4096, "nk", "bf16", num_sms=152)
-    assert (p["tile_n"], p["cta_group"], p["tail_split"], p["cluster_split"]) == (128, 1, 2, 1)
+def test_underfilled_plans_by_streamed_and_exchanged_bytes(lib, knobs):
+    """Under one wave of single-CTA tiles the tile width follows each CTA's TMA
+    copies (a fixed cost per copy plus the bytes) and the partial sums its K
+    segments exchange in a cluster. With two-slice stages for 128- and 64-wide
+    tiles, 1024^2 x 4096 takes 128-wide tiles in two segments in BF16 and FP8
+    (with one slice per stage the fit makes that plan and 128 x 256 in four
+    segments cost the same, as measured). Full-wave plans are unchanged."""
+    def plan(fp8, M, N, K, layout):
+        p = dg.dgemm_plan(fp8, M, N, K, layout, "bf16", num_sms=152)
+        return (p["tile_n"], p["cta_group"], p["tail_split"], p["cluster_split"])
+    assert plan(1, 1024, 1024, 4096, "nk") == (128, 1, 2, 1)
+    assert plan(0, 1024, 1024, 4096, "nk") == (128, 1, 2, 1)
+    assert plan(0, 512, 512, 4096, "nk")[::2] == (64, 4)
+    assert plan(0, 4096, 4096, 4096, "kn")[:2] == (256, 2)
+    knobs(kslices="1")
     p = dg.dgemm_plan(0, 1024, 1024, 4096, "nk", "bf16", num_sms=152)
-    assert (p["tile_n"], p["cta_group"], p["tail_split"], p["cluster_split"]) == (256, 1, 4, 1)
-    p = dg.dgemm_plan(0, 512, 512, 4096, "nk", "bf16", num_sms=152)
-    assert (p["tile_n"], p["tail_split"]) == (64, 4)
-    p = dg.dgemm_plan(0, 4096, 4096, 4096, "kn", "bf16", num_sms=152)
-    assert (p["tile_n"], p["cta_group"]) == (256, 2)
+    assert p["k_slices"] == 1 and (p["tile_n"], p["tail_split"]) in ((128, 2), (256, 4))
 
 
 def test_two_slice_stages_only_where_the_operands_are_whole_slices(lib, knobs):
-    """CTA-pair tile and requantising plans take two 128-byte K slices per
-    stage (each operand one 3-D TMA copy) when K, and N for B stored K x N,
-    are whole multiples of 128 bytes; otherwise, for single-CTA tiles, the
-    small-M form and per-K-group scales, one slice per stage."""
+    """CTA-pair tile and requantising plans, and single-CTA tiles 128 or 64
+    wide, take two 128-byte K slices per stage (each operand one 3-D TMA copy)
+    when K, and N for B stored K x N, are whole multiples of 128 bytes;
+    otherwise, and for 128 x 256 single-CTA tiles, the small-M form and
+    per-K-group scales, one slice per stage."""
     def plan(fp8, M, N, K, layout, **kw):
         return dg.dgemm_plan(fp8, M, N, K, layout, "bf16", num_sms=152, **kw)
     assert plan(0, 4096, 4096, 4096, "kn")["k_slices"] == 2
@@ -317,7 +320,14 @@ def test_two_slice_stages_only_where_the_operands_are_whole_slices(lib, knobs):
     assert plan(0, 4096, 4000, 4096, "nk")["k_slices"] == 2          # (N is free for B stored N x K)
     assert plan(1, 4096, 11008, 4096, "nk", k_group=128)["k_slices"] == 1
     assert plan(0, 16, 4096, 4096, "nk")["k_slices"] == 1            # small M
-    assert plan(0, 1024, 1024, 4096, "nk")["k_slices"] == 1          # single-CTA tiles
+    knobs(cta_pair="0")
+    p = plan(0, 4096, 4096, 4096, "nk")                                # single-CTA 128 x 256 tiles
+    assert (p["cta_group"], p["tile_n"], p["k_slices"]) == (1, 256, 1)
+    knobs(cta_pair=None)
+    p = plan(0, 128, 4096, 4096, "nk")                                 # single-CTA 128 x 128 tiles
+    assert (p["cta_group"], p["tile_n"], p["k_slices"], p["stages"]) == (1, 128, 2, 3)
+    p = plan(1, 512, 512, 4096, "nk")                                  # FP8, 128 x 64 tiles
+    assert (p["cta_group"], p["tile_n"], p["k_slices"]) == (1, 64, 2)
     assert dg.dgemm_plan(1, 8192, 8192, 8192, "nk", "e4m3", out_quant="e4m3_row_amax", num_sms=152)["k_slices"] == 2
     knobs(kslices="1")
     p = plan(0, 4096, 4096, 4096, "kn")

@@ -73,7 +73,8 @@ def test_stalled_producer_without_workspace_reports_on_the_device_word(knobs):
     M, N, K = 256, 768, 1024
     call, D, _, ref = bf16_call(M, N, K, seed=77, ws_bytes=0)
     assert dg.dgemm_plan(0, M, N, K, "nk", "f32", num_sms=0)["workspace_bytes"] == 0
-    knobs(wait_limit_ns=LIMIT_NS, stall_after_loads=5)
+    # (each K segment is 4 stages of two slices: stop below that)
+    knobs(wait_limit_ns=LIMIT_NS, stall_after_loads=2)
     call()
     assert dg.dgemm_query_device_status(None) == TIMEOUT
     assert dg.dgemm_query_device_status(None) == 0
