@@ -460,7 +460,7 @@ __device__ __forceinline__ float4 lane_f4(const float4& x, int src_lane) {
 template <bool SWAP>
 __device__ __forceinline__ void epilogue_math(float (&v)[32], const Params& p, int row, int col0,
                                               int ncols, float rs, float bias_row, const float4& cs_l,
-                                              const float4& bias_l, int lane0) {
+                                              const float4& bias_l, int lane0, const float4* cs_sw) {
     const bool row_ok = row < p.M;
     // column-indexed scale (per MMA column)
     if (p.col_scale) {
@@ -469,7 +469,7 @@ __device__ __forceinline__ void epilogue_math(float (&v)[32], const Params& p, i
             if (j < ncols) {
                 float4 s;
                 if constexpr (SWAP)
-                    s = col0 + j < p.N ? ld_bcast4(p.col_scale, col0 + j, p.N) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    s = cs_sw[j / 4];
                 else
                     s = lane_f4(cs_l, lane0 + j / 4);
                 v[j] *= s.x; v[j + 1] *= s.y; v[j + 2] *= s.z; v[j + 3] *= s.w;
@@ -1107,6 +1107,18 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
             };
             if constexpr (CF::MODE != MODE_SWAP && !CF::GS) load_cols();
+            // Small-M form: the MMA columns' (tokens') scales of this warp, 0
+            // past N, likewise fetched before the accumulator is ready.
+            constexpr bool SW_PRE = CF::MODE == MODE_SWAP && !CF::GS;   // (K-group scales: per group)
+            constexpr int SW4 = SW_PRE ? (CF::EPI_COLS + 3) / 4 : 1;
+            float4 cs_sw[SW4];
+            cs_sw[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (SW_PRE) {
+#pragma unroll
+                for (int i = 0; i < SW4; ++i)
+                    cs_sw[i] = (p.col_scale && ocol + 4 * i < p.N) ? ld_bcast4(p.col_scale, ocol + 4 * i, p.N)
+                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             if constexpr (!CF::GS) {
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!mbar_wait(&acc_full[buf], acc_phase, abort_flag, p.wait_ns)) {
@@ -1274,8 +1286,17 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
             // segments of a split tile each finish single units).
             auto finish = [&](int u, float (&v)[32], bool direct) {
                 const int col0 = ocol + u * UNIT;
+                // this unit's token scales, picked with constant indices (registers)
+                float4 cu[SW_PRE ? (UNIT + 3) / 4 : 1];
+#pragma unroll
+                for (int i = 0; i < (SW_PRE ? (UNIT + 3) / 4 : 1); ++i) {
+                    cu[i] = cs_sw[SW_PRE ? i : 0];
+#pragma unroll
+                    for (int uu = 1; uu < NUNITS; ++uu)
+                        if (SW_PRE && u == uu) cu[i] = cs_sw[(uu * UNIT / 4 + i) % SW4];
+                }
                 epilogue_math<CF::MODE == MODE_SWAP>(v, p, row, col0, UNIT, rs, bias_row, cs_l, bias_l,
-                                                     u * UNIT / 4);
+                                                     u * UNIT / 4, cu);
                 if constexpr (CF::MODE == MODE_ROWQ) {
                     if (row < p.M) {
 #pragma unroll
