@@ -100,6 +100,35 @@ def test_fp8_swap_exact(layout, M):
     assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
 
 
+@pytest.mark.parametrize("kslices", ["2", "1"])
+@pytest.mark.parametrize("layout,bn", [("nk", 64), ("nk", 128), ("kn", 64), ("kn", 128)])
+@pytest.mark.parametrize("kblocks", [1, 3, 6])
+def test_single_cta_two_slice_stages_exact(layout, bn, kblocks, kslices, knobs):
+    """Single-CTA 128x64 and 128x128 tiles with one or two 128-byte K slices per
+    stage (two: each operand of a stage one 3-D TMA copy; with an odd slice count
+    the last stage's second slice is zero-filled), ragged M and N, several tiles
+    per CTA; integer inputs, so the result is exact."""
+    knobs(tile_n=str(bn), cta_pair="0", kslices=kslices)
+    M, N, K = 1320, 1984, 64 * kblocks
+    plan = dg.dgemm_plan(0, M, N, K, layout, "f32")
+    assert (plan["cta_group"], plan["tile_n"], plan["k_slices"]) == (1, bn, int(kslices))
+    got, ref = bf16_case(M, N, K, layout, seed=900 + 10 * bn + kblocks)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
+@pytest.mark.parametrize("kslices", ["2", "1"])
+@pytest.mark.parametrize("layout,bn", [("nk", 64), ("nk", 128), ("kn", 128)])
+@pytest.mark.parametrize("kblocks", [1, 3, 6])
+def test_fp8_single_cta_two_slice_stages_exact(layout, bn, kblocks, kslices, knobs):
+    """The same for E4M3 (128-element K slices) with power-of-two scales."""
+    knobs(tile_n=str(bn), cta_pair="0", kslices=kslices)
+    M, N, K = 1320, 1920, 128 * kblocks
+    plan = dg.dgemm_plan(1, M, N, K, layout, "f32")
+    assert (plan["cta_group"], plan["tile_n"], plan["k_slices"]) == (1, bn, int(kslices))
+    got, ref = fp8_case(M, N, K, layout, seed=950 + 10 * bn + kblocks)
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} mismatches"
+
+
 @pytest.mark.parametrize("kblocks", [1, 2, 3, 4, 5, 9, 13])
 def test_odd_k_block_counts_exact(kblocks, knobs):
     """Odd numbers of K slices expose pipeline-phase bugs (DeepGEMM write-up,
