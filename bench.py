@@ -146,7 +146,7 @@ class NvmlClocks:
     """SM clock, power and clock-event reasons read in-process through NVML
     (the driver's libnvidia-ml.so.1, through ctypes; only reads). sample()
     returns (sm_mhz, power_w, reason_bits) or None."""
-    # clock-event reason bits (nvml.h): the ones a run is judged by
+    # clock-event reason bits (nvml.h) that decide whether a timed region stands
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     NVML_CLOCK_SM = 1
