@@ -122,7 +122,9 @@ typedef struct {
                               dimension runs over N (small-M, decode shapes)     */
     int tile_m, tile_n;    /* output tile of one CTA, in the MMA's orientation  */
     int cta_group;         /* CTAs that share one MMA (1 or 2)                  */
-    int stages;            /* shared-memory pipeline depth                      */
+    int stages;            /* shared-memory pipeline depth (the small-M form's
+                              short calls run a compact ring of at most half an
+                              SM's shared memory and 256 TMEM columns)          */
     int num_tiles;         /* output tiles                                      */
     int grid;              /* CTAs launched (persistent: <= SM count)           */
     int cooperative;       /* 1: launched cooperatively, so every CTA is
@@ -294,8 +296,9 @@ typedef struct {
                             cooperatively (DGEMM_COOPERATIVE)                       */
     int kslices;         /* -1; 1: one 128-byte K slice per pipeline stage (the
                             planner takes two, fetched in 3-D copies, for CTA-pair
-                            tiles whose K, and N when B is stored K x N, are whole
-                            multiples of 128 bytes) (DGEMM_KSLICES)                 */
+                            tiles and 128- or 64-wide single-CTA tiles whose K,
+                            and N when B is stored K x N, are whole multiples of
+                            128 bytes) (DGEMM_KSLICES)                              */
     int64_t wait_limit_ns;     /* 0: about one second; else the limit of every
                                   bounded device-side wait (DGEMM_WAIT_LIMIT_NS)    */
     int64_t stall_after_loads; /* -1; testing the bounded waits: every CTA's operand
