@@ -27,7 +27,7 @@ constexpr size_t kWsHeader = 256;  // requantisation: chunk claim counter + row-
 static_assert(8 + 4 * dg::kMaxBands <= kWsHeader, "row-band counters fit the header");
 static_assert(kWsStatus % 256 == 0 && kWsStatus >= 8, "status header keeps the layout 256-byte aligned");
 constexpr int64_t kMinTailSlices = 48;  // shortest tile (K slices) worth splitting
-constexpr int64_t kCompactSlices = 32;  // longest work item (K slices) of a compact small-M call
+constexpr int64_t kCompactSlices = 16;  // longest work item (K slices) of a compact small-M call
 
 struct DeviceState {
     std::once_flag once;
@@ -458,10 +458,12 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
     // Footprint. Short small-M calls (every CTA one work item of at most
     // kCompactSlices K slices) run compact -- at most half of the SM's shared
     // memory and Tensor Memory -- so that the next call's CTAs can be resident
-    // while these finish: 1 x 4096 x 4096 and 16 x 4096 x 4096 took 11.9-12.3
-    // us instead of 12.7-13.1. Longer streams keep the full ring, which the
-    // compact one slows: 16 x 18432 x 7168 47.0 vs 46.3 us, 64 x 8192^2 32.5 vs
-    // 30.0 us (200-step runs on one GPU).
+    // while these finish (with the 16-wide kernel's registers, two CTAs fit):
+    // 1 x 4096 x 4096 and 16 x 4096 x 4096 took 11.9-12.3 us instead of
+    // 12.7-13.1, and 32 x 4096 x 4096 (32 wide) 14.0 instead of 14.5. Longer
+    // streams keep the full ring, which the compact one slows: 16 x 18432 x
+    // 7168 47.0 vs 46.3 us, 64 x 8192^2 32.5 vs 30.0, FP8 64 x 8192^2 (32
+    // slices a segment) 20.2 vs 19.6 (200-step runs and CUDA graphs, one GPU).
     const bool compact = p.mode == dg::MODE_SWAP && p.pub.num_tiles <= units && k_blocks > 0 &&
                          (k_blocks * p.ks + p.split - 1) / p.split <= kCompactSlices;
     p.stages = compact ? k->stages_compact : k->stages;

@@ -243,8 +243,12 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // Epilogue warps: two per TMEM lane quarter (each takes half of the tile's
     // columns) for tiles of 128 columns or more, whose FP8 mainloop per tile can
-    // be shorter than one warp-quarter's epilogue; one per quarter otherwise.
-    static constexpr int EPI_WARPS = (MODE == MODE_SWAP || BN < 128) ? 4 : 8;
+    // be shorter than one warp-quarter's epilogue, and for the 16-wide small-M
+    // form, whose epilogue sums up to 32 K-group accumulators at the end of the
+    // call (a warp reads TMEM at a fixed rate, so two warps a quarter halve
+    // that; its 320 threads still fit twice in an SM's registers for the
+    // compact footprint); one per quarter otherwise.
+    static constexpr int EPI_WARPS = (MODE == MODE_SWAP) ? ((GS || BN != 16) ? 4 : 8) : (BN < 128 ? 4 : 8);
     static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);   // columns per epilogue warp
     static constexpr int STAGING_BYTES = (MODE == MODE_SWAP) ? 0 : EPI_WARPS * 4096;  // one 4 KB box each
     // Per-K-group scales (tile modes): a scale-producer warp copies each
@@ -1250,13 +1254,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 for (; GB > 1 && g + GB <= g1; g += GB) {
                     uint32_t r[GB][UNIT];
 #pragma unroll
-                    for (int h = 0; h < GB; ++h) {
-                        const uint32_t ta = taddr + static_cast<uint32_t>((g + h) * CF::BN + tcol);
-                        if constexpr (UNIT == 32)
-                            tmem_ld32(ta, r[h]);
-                        else
-                            tmem_ld16(ta, r[h]);
-                    }
+                    for (int h = 0; h < GB; ++h)
+                        tmem_ld_unit<UNIT>(taddr + static_cast<uint32_t>((g + h) * CF::BN + tcol), r[h]);
                     tmem_ld_wait();
 #pragma unroll
                     for (int h = 0; h < GB; ++h)
@@ -1265,12 +1264,8 @@ __global__ void __launch_bounds__(CF::NUM_THREADS, 1)
                 }
 #pragma unroll 1
                 for (; g < g1; ++g) {
-                    const uint32_t ta = taddr + static_cast<uint32_t>(g * CF::BN + tcol);
                     uint32_t r[UNIT];
-                    if constexpr (UNIT == 32)
-                        tmem_ld32(ta, r);
-                    else
-                        tmem_ld16(ta, r);
+                    tmem_ld_unit<UNIT>(taddr + static_cast<uint32_t>(g * CF::BN + tcol), r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < UNIT; ++j) v[j] += __uint_as_float(r[j]);

@@ -279,6 +279,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+// One unit of N consecutive columns (8, 16 or 32) of this thread's TMEM lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld_unit(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N == 8 || N == 16 || N == 32, "unit width");
+    if constexpr (N == 32)
+        tmem_ld32(taddr, r);
+    else if constexpr (N == 16)
+        tmem_ld16(taddr, r);
+    else
+        tmem_ld8(taddr, r);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- register reallocation

@@ -335,7 +335,7 @@ def test_two_slice_stages_only_where_the_operands_are_whole_slices(lib, knobs):
 
 
 def test_short_small_m_calls_take_half_an_sm(lib):
-    """Small-M calls whose work items are at most 32 K slices long run in a
+    """Small-M calls whose work items are at most 16 K slices long run in a
     compact footprint -- at most half of an SM's shared memory (228 KB less the
     1 KB reserved per CTA, halved) and 256 of its 512 Tensor Memory columns, so
     the K groups halve -- letting the next call's CTAs become resident early;
@@ -352,5 +352,9 @@ def test_short_small_m_calls_take_half_an_sm(lib):
     assert p["smem_bytes"] > half_sm and p["stages"] == 12 and p["k_groups"] == 512 // 16
     p = plan(64, 8192, 8192)       # 2 segments of 64 slices
     assert p["smem_bytes"] > half_sm and p["tail_split"] == 2
+    p = plan(32, 4096, 4096)       # 32 wide, 4 segments of 16 slices: compact
+    assert p["tile_n"] == 32 and p["smem_bytes"] <= half_sm
+    p = dg.dgemm_plan(1, 64, 8192, 8192, "nk", "bf16", num_sms=152)   # FP8: 2 segments of 32 slices
+    assert p["smem_bytes"] > half_sm
     p = plan(4096, 4096, 4096)     # tile kernels are never compact
     assert p["smem_bytes"] > half_sm
