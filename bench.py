@@ -126,10 +126,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def plan_tile(plan):
+    """The plan's tile as recorded beside a traffic figure: rows x columns x CTAs."""
+    return f"{plan['tile_m']}x{plan['tile_n']}x{plan['cta_group']}"
+
+
+def recorded_traffic(workload, plan=None, path=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    current kernel sources and, where the record names one, on the tile the
+    current plan chooses (else None)."""
+    path = path or os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     want = kernel_source_hash()
@@ -137,6 +143,8 @@ def recorded_traffic(workload):
         if line.startswith("#") or not line.strip():
             continue
         kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if plan is not None and "tile" in kv and kv["tile"] != plan_tile(plan):
+            continue
         if kv.get("workload") == str(workload) and kv.get("kernel_src_sha") == want:
             return int(float(kv["dram_bytes_per_launch"]))
     return None
@@ -611,7 +619,7 @@ def run_ours(args, rank, world, local):
     plan = plan_of(dg, w)
     skinny = is_skinny(w, args.config, args.shape, peaks)
     roof = roofline_of(w, ms_step, clock_rec, peaks, peak_kind, n_sm, skinny, plan,
-                       recorded_traffic(workload_key(args)))
+                       recorded_traffic(workload_key(args), plan))
     l2_note = rig.l2_note()
     rig.free()
     del host, bufs, Dh, sh
@@ -667,7 +675,7 @@ def time_other(number, steps, warmup, dev, stream, barrier, clocks, peaks, peak_
     ms_step = ms_total / steps
     plan = plan_of(dg, w)
     skinny = number == 4
-    roof = roofline_of(w, ms_step, rec, peaks, peak_kind, n_sm, skinny, plan, recorded_traffic(str(number)))
+    roof = roofline_of(w, ms_step, rec, peaks, peak_kind, n_sm, skinny, plan, recorded_traffic(str(number), plan))
     out = {"workload": DESCRIPTIONS[number], "M": w.M, "N": w.N, "K": w.K, "steps": steps, "warmup": warmup,
            "us_per_call": round(ms_step * 1e3, 3),
            "value": round(job_rate(w.flops * steps, world, ms_total * 1e-3) / 1e12, 2), "unit": "TFLOPS",

@@ -279,6 +279,16 @@ dgemm_status_t make_plan(int fp8, int64_t M, int64_t N, int64_t K, dgemm_b_layou
         for (const Cand& c : cands) {
             if (p.mode == dg::MODE_ROWQ && c.bn != 256) continue;
             if (c.pair && (!pairs_ok || M <= 128)) continue;
+            // Per-K-group scales in groups of one or two K slices: the fold,
+            // not the operand feed, sets the pace, and a pair's TMEM buffer
+            // takes its next group only when all 16 epilogue warps of both
+            // CTAs have folded the last one, so single CTAs (8 warps a
+            // buffer) run faster despite more operand copies per FLOP.
+            // 4096 x 11008 x 4096 E4M3, TFLOP/s, single vs pair: g = 128
+            // 1310 vs 1199 per channel, 1866 vs 1752 with weight blocks;
+            // g = 256 1998 vs 1918, 2145 vs 2167; g = 512 2296 vs 2367,
+            // 2395 vs 2540.
+            if (c.pair && gs && p.group_kb <= 2) continue;
             if (fp8 && p.b_mn && c.bn < 128) continue;
             const int64_t tm = c.pair ? 256 : 128;
             const int64_t units = c.pair ? max_pairs : num_sms;

@@ -136,10 +136,16 @@ def test_plans_for_the_five_workloads(lib):
 
 def test_plan_of_per_group_scales(lib):
     """The plan query takes k_group: K groups of 128 on workload 3's shape are
-    32 scale groups on the CTA-pair 256 x 256 kernel with 5 stages (one fewer:
-    the scale ring takes shared memory); invalid groups fail as the call would."""
+    32 scale groups on the single-CTA 128 x 256 kernel with 3 stages (groups of
+    one or two K slices skip CTA pairs; the scale ring takes shared memory);
+    groups of 512 go back to the pair's 5 stages; invalid groups fail as the
+    call would."""
     p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=128, num_sms=152)
-    assert (p["k_groups"], p["cta_group"], p["tile_n"], p["stages"]) == (32, 2, 256, 5)
+    assert (p["k_groups"], p["cta_group"], p["tile_n"], p["stages"]) == (32, 1, 256, 3)
+    p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=256, num_sms=152)
+    assert (p["k_groups"], p["cta_group"], p["tile_n"]) == (16, 1, 256)
+    p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", k_group=512, num_sms=152)
+    assert (p["k_groups"], p["cta_group"], p["tile_n"], p["stages"]) == (8, 2, 256, 5)
     p = dg.dgemm_plan(1, 4096, 11008, 4096, "nk", "bf16", num_sms=152)
     assert (p["stages"], p["k_slices"]) == (3, 2)   # per-row scales: two K slices per stage
     assert p["k_slices"] * p["stages"] * 32 == 2 * 96   # the same bytes in flight as 6 single slices

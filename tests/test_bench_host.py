@@ -127,3 +127,23 @@ def test_shape_option():
     A.config = 3
     with pytest.raises(SystemExit):
         bench.make_workload(A)
+
+
+def test_recorded_traffic_follows_source_hash_and_plan_tile(tmp_path):
+    """A DRAM figure from the traffic records is reported only while the device
+    code hashes the same and, where the record names a tile, while the plan
+    still chooses that tile."""
+    sha = bench.kernel_source_hash()
+    path = tmp_path / "dram_traffic.txt"
+    path.write_text("# test records\n"
+                    f"workload=2 kernel_src_sha={sha} tile=256x256x2 dram_bytes_per_launch=1000\n"
+                    "workload=3 kernel_src_sha=0000000000000000 tile=256x256x2 dram_bytes_per_launch=2000\n"
+                    f"workload=4 kernel_src_sha={sha} dram_bytes_per_launch=3000\n")
+    pair = {"tile_m": 256, "tile_n": 256, "cta_group": 2}
+    single = {"tile_m": 128, "tile_n": 256, "cta_group": 1}
+    assert bench.recorded_traffic("2", pair, str(path)) == 1000
+    assert bench.recorded_traffic("2", None, str(path)) == 1000
+    assert bench.recorded_traffic("2", single, str(path)) is None   # another tile
+    assert bench.recorded_traffic("3", pair, str(path)) is None     # older device code
+    assert bench.recorded_traffic("4", single, str(path)) == 3000   # no tile named
+    assert bench.recorded_traffic("5", pair, str(path)) is None
